@@ -1,0 +1,286 @@
+"""Pins of the oracle's copy, norm and AdamW arithmetic against things other
+than itself: closed forms, math.fsum, torch.optim.AdamW (CPU, fp32), torch's
+bf16 rounding, quantiser properties and the hand-derived fixture
+tests/golden/adam8_step1_worked.txt.
+
+Method: "veScale-FSDP: Flexible and High-Performance FSDP at Scale (MLSys
+2026)" summary page, 核心方法 > Distributed Buffer (fused group copy / scale)
+and 结构感知训练 case study > 8-bit Adam; "FSDP" concept page, 关键观察
+(copy-in / copy-out).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import workloads as W
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "adam8_step1_worked.txt")
+
+
+def f32(x):
+    return np.float32(x)
+
+
+# ---------------------------------------------------------------- copy-in / copy-out
+
+def test_pack_unpack_identity_and_padding_untouched():
+    w = W.tiny()
+    d = oracle.Desc.from_workload(w)
+    S, off = oracle.plan(d, w.m, w.g_coll)
+    grads = [W.grad(w, 1, t) for t in range(d.n)]
+    packed = oracle.pack(grads, off, w.m * S)
+    for t, g in enumerate(grads):
+        assert np.array_equal(packed[off[t]:off[t] + g.size], g)
+    outs = oracle.unpack(packed, [g.size for g in grads], off)
+    for a, b in zip(outs, grads):
+        assert np.array_equal(a, b)
+    real = np.zeros(w.m * S, bool)
+    for t, g in enumerate(grads):
+        real[off[t]:off[t] + g.size] = True
+    assert not packed[~real].any()
+
+
+def test_pack_fp32():
+    a = np.arange(10, dtype=np.float32)
+    b = -np.arange(3, dtype=np.float32)
+    packed = oracle.pack([a, b], [0, 16], 32)
+    assert np.array_equal(packed[:10], a) and np.array_equal(packed[16:19], b)
+
+
+# ---------------------------------------------------------------- norm and scale
+
+def test_sumsq_constant_closed_form():
+    c = 2.0 ** -9
+    bits = np.array([c], np.float32).view(np.uint32)[0] >> 16
+    ts = [np.full(1000, bits, np.uint16), np.full(24, bits | 0x8000, np.uint16)]
+    assert oracle.sumsq(ts) == 1024 * c * c
+
+
+def test_sumsq_matches_fsum():
+    w = W.tiny()
+    grads = [W.grad(w, 1, t) for t in range(len(w.tensors))]
+    n = sum(g.size for g in grads)
+    bound = n * 2.0 ** -53  # textbook bound of a recursive fp64 sum of positive terms
+    got = oracle.sumsq(grads)
+    want = math.fsum(float(x) ** 2 for g in grads for x in synth.bf16_to_f32(g))
+    assert abs(got - want) <= bound * want
+    g32 = [W.grad_f32(w, 1, t) for t in range(len(w.tensors))]
+    got32 = oracle.sumsq(g32)
+    want32 = math.fsum(float(x) ** 2 for g in g32 for x in g)
+    assert abs(got32 - want32) <= bound * want32
+
+
+def test_factor_no_clip_is_exact_inverse_world():
+    for world in (1, 4, 8, 64, 1024, 3):
+        f, norm = oracle.factor(1234.5, world, math.inf)
+        assert f == float(np.float32(1.0 / world))
+        assert norm == math.sqrt(1234.5) / world
+
+
+def test_factor_clip_closed_form():
+    # sumsq = 400 -> sqrt = 20 -> norm over world 4 = 5; c = 1/(5 + 1e-6)
+    f, norm = oracle.factor(400.0, 4, 1.0)
+    assert norm == 5.0
+    assert f == float(np.float32((1.0 / (5.0 + 1e-6)) / 4.0))
+    f2, _ = oracle.factor(400.0, 4, 10.0)  # norm under the limit: no clipping
+    assert f2 == 0.25
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000).astype(np.float32) * 0.02,
+                        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 3.4e38, -0.0,
+                                  1e-40, np.inf, -np.inf], np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_round(float(v)) for v in x], np.uint16)
+    assert np.array_equal(got, want)
+    assert oracle.bf16_round(float("nan")) == 0x7FC0
+
+
+# ---------------------------------------------------------------- AdamW, fp32 state
+
+def adam_fp32_steps(g_list, p0, factor):
+    st = dict(p=p0.copy(), m=np.zeros_like(p0), v=np.zeros_like(p0))
+    for t, g in enumerate(g_list, start=1):
+        st = oracle.adam_block(g, False, factor, st, t, HP)
+    return st
+
+
+def test_first_step_closed_form():
+    """Step 1 with zero state: p1 = p (1 - lr wd) - lr g / (|g| + eps)."""
+    w = W.tiny()
+    g = W.grad(w, 1, 0)
+    p0 = W.master_init(w, 0)
+    factor = 0.25
+    st = adam_fp32_steps([g], p0, factor)
+    gs = factor * synth.bf16_to_f32(g).astype(np.float64)
+    want = p0.astype(np.float64) * (1 - HP["lr"] * HP["weight_decay"]) \
+        - HP["lr"] * gs / (np.abs(gs) + HP["eps"])
+    err = np.abs(st["p"].astype(np.float64) - want)
+    assert np.all(err <= 1e-6 * (np.abs(want) + HP["lr"]))
+    assert np.abs(st["p"] - p0).max() > 5e-4  # the update really happened
+
+
+def test_zero_grad_step_is_pure_decay():
+    p0 = np.array([0.5, -0.25, 0.0, 1e-3], np.float32)
+    g = np.zeros(4, np.uint16)
+    st = adam_fp32_steps([g], p0, 1.0)
+    assert np.array_equal(st["p"], p0 * np.float32(1 - 1e-5))
+
+
+def test_matches_torch_adamw_ten_steps():
+    """Textbook AdamW (torch.optim.AdamW, CPU fp32, single-tensor path)."""
+    w = W.tiny()
+    n = 4096
+    p0 = W.master_init(w, 0)[:n].copy()
+    factor = np.float32(0.25)
+    gs = [W.grad(w, s, 0)[:n].copy() for s in range(1, 11)]
+    st = dict(p=p0.copy(), m=np.zeros(n, np.float32), v=np.zeros(n, np.float32))
+    prm = torch.nn.Parameter(torch.from_numpy(p0.copy()))
+    opt = torch.optim.AdamW([prm], lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                            weight_decay=HP["weight_decay"], foreach=False, fused=False)
+    for t, g in enumerate(gs, start=1):
+        st = oracle.adam_block(g, False, float(factor), st, t, HP)
+        prm.grad = torch.from_numpy(synth.bf16_to_f32(g) * factor)
+        opt.step()
+        ref = prm.detach().numpy().astype(np.float64)
+        err = np.abs(st["p"].astype(np.float64) - ref)
+        assert np.all(err <= 1e-6 * (np.abs(ref) + HP["lr"])), (t, err.max())
+        sref = opt.state[prm]
+        # torch writes m as a lerp, so moments agree to rounding of the largest one
+        for mine, theirs in ((st["m"], sref["exp_avg"].numpy()),
+                             (st["v"], sref["exp_avg_sq"].numpy())):
+            assert np.abs(mine - theirs).max() <= 1e-6 * np.abs(theirs).max()
+
+
+# ---------------------------------------------------------------- quantiser
+
+def test_quantizer_properties():
+    rng = np.random.default_rng(3)
+    for trial in range(50):
+        x = (rng.standard_normal(int(rng.integers(1, 600))) * 10.0 ** rng.integers(-9, 2)).astype(
+            np.float32)
+        c, s, dq = oracle.quantize_m(x)
+        assert s == np.abs(x).max()
+        assert np.all(np.abs(c.astype(int)) <= 127)
+        assert np.abs(c[np.argmax(np.abs(x))]) == 127
+        assert np.all(np.abs(dq.astype(np.float64) - x) <= s / 254 * (1 + 1e-5))
+        c2, s2, _ = oracle.quantize_m(dq)
+        assert np.array_equal(c2, c)  # idempotent on its own grid
+        v = np.abs(x) ** 2
+        cv, sv, dv = oracle.quantize_v(v)
+        assert sv == v.max() and cv[np.argmax(v)] == 255
+        assert np.all(np.abs(dv.astype(np.float64) - v) <= sv / 510 * (1 + 1e-5))
+        cv2, _, _ = oracle.quantize_v(dv)
+        assert np.array_equal(cv2, cv)
+
+
+def test_quantizer_zero_block_and_ties():
+    c, s, dq = oracle.quantize_m(np.zeros(7, np.float32))
+    assert s == 0 and not c.any() and not dq.any()
+    cv, sv, dv = oracle.quantize_v(np.zeros(7, np.float32))
+    assert sv == 0 and not cv.any() and not dv.any()
+    # 127 * [1, 1/254, 3/254] = [127, 0.5, 1.5]: exact halves round to even (0, 2)
+    x = np.array([254.0, 1.0, 3.0], np.float32)
+    c, s, _ = oracle.quantize_m(x)
+    assert list(c) == [127, 0, 2]
+
+
+def load_worked():
+    rows = {}
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, *vals = line.split()
+        rows[k] = vals
+    return rows
+
+
+def test_worked_example_step1():
+    fx = load_worked()
+    g = np.array([int(v, 16) for v in fx["g_bf16"]], np.uint16)
+    p0 = np.array([0.02, -0.02, 0.0, 0.5], np.float32)
+    st = dict(p=p0.copy(), mq=np.zeros(4, np.int8), vq=np.zeros(4, np.uint8),
+              m_scale=0.0, v_scale=0.0)
+    out = oracle.adam_block(g, True, 1.0, st, 1, HP)
+    assert list(out["mq"]) == [int(v) for v in fx["m_codes"]]
+    assert list(out["vq"]) == [int(v) for v in fx["v_codes"]]
+    assert out["m_scale"] == float(np.float32(np.float32(0.1) * np.float32(2.0 ** -10)))
+    assert out["v_scale"] == float(np.float32(np.float32(0.001) * np.float32(2.0 ** -20)))
+    gs = synth.bf16_to_f32(g).astype(np.float64)
+    want = p0 * (1 - 1e-5) - 1e-3 * gs / (np.abs(gs) + 1e-8)
+    assert np.all(np.abs(out["p"] - want) <= 1e-6 * (np.abs(want) + 1e-3))
+
+
+def test_quantized_step1_master_equals_fp32_step1():
+    """At step 1 the update only sees fresh moments: the 8-bit and fp32-state
+    masters agree bit for bit."""
+    w = W.llama_layer()
+    g = W.grad(w, 1, 0, 0, 4096 * 32)
+    p0 = W.master_init(w, 0, 0, 4096 * 32)
+    q = oracle.adam_block(g, True, 0.125, dict(p=p0, mq=np.zeros(g.size, np.int8),
+                                                 vq=np.zeros(g.size, np.uint8),
+                                                 m_scale=0.0, v_scale=0.0), 1, HP)
+    f = oracle.adam_block(g, False, 0.125, dict(p=p0, m=np.zeros(g.size, np.float32),
+                                                  v=np.zeros(g.size, np.float32)), 1, HP)
+    assert np.array_equal(q["p"], f["p"]) and np.array_equal(q["bf16"], f["bf16"])
+    cm, sm, _ = oracle.quantize_m(f["m"])
+    cv, sv, _ = oracle.quantize_v(f["v"])
+    assert np.array_equal(q["mq"], cm) and np.array_equal(q["vq"], cv)
+    assert (q["m_scale"], q["v_scale"]) == (sm, sv)
+
+
+def test_quantized_step_is_dequant_update_requant():
+    """Requantisation follows the update, with the new block scale."""
+    w = W.tiny()
+    n = 8192
+    rng = np.random.default_rng(5)
+    mq = rng.integers(-127, 128, n).astype(np.int8)
+    vq = rng.integers(0, 256, n).astype(np.uint8)
+    ms, vs = 3e-5, 2e-9
+    p0 = W.master_init(w, 0, 0, n)
+    g = W.grad(w, 4, 0, 0, n)
+    q = oracle.adam_block(g, True, 0.25, dict(p=p0, mq=mq, vq=vq, m_scale=ms, v_scale=vs), 4, HP)
+    m_deq = mq.astype(np.float32) * np.float32(np.float32(ms) / np.float32(127))
+    v_deq = vq.astype(np.float32) * np.float32(np.float32(vs) / np.float32(255))
+    f = oracle.adam_block(g, False, 0.25, dict(p=p0, m=m_deq, v=v_deq), 4, HP)
+    assert np.array_equal(q["p"], f["p"])
+    cm, sm, _ = oracle.quantize_m(f["m"])
+    cv, sv, _ = oracle.quantize_v(f["v"])
+    assert np.array_equal(q["mq"], cm) and np.array_equal(q["vq"], cv)
+    assert (q["m_scale"], q["v_scale"]) == (sm, sv)
+
+
+def test_adam_all_matches_blockwise():
+    w = W.tiny()
+    d = oracle.Desc.from_workload(w)
+    S, off = oracle.plan(d, w.m, w.g_coll)
+    qb = oracle.qblocks(d, w.g_coll, off)
+    total = w.m * S
+    grads = [W.grad(w, 1, t) for t in range(d.n)]
+    packed = oracle.pack(grads, off, total)
+    master = oracle.pack([W.master_init(w, t) for t in range(d.n)], off, total)
+    mq, vq = np.zeros(total, np.int8), np.zeros(total, np.uint8)
+    nq = len(qb["base"])
+    ms, vs = np.zeros(nq, np.float32), np.zeros(nq, np.float32)
+    bf = np.zeros(total, np.uint16)
+    oracle.adam_all(qb, packed, 0.25, True, mq, vq, ms, vs, master, bf, 1, HP)
+    # one TILE block (tensor 2, first tile) recomputed on its own
+    q = int(np.nonzero(qb["tensor"] == 2)[0][1])
+    r, c, s, b = (int(qb[k][q]) for k in ("nrows", "ncols", "stride", "base"))
+    idx = (b + np.arange(r)[:, None] * s + np.arange(c)[None, :]).ravel()
+    g = packed[idx]
+    p0 = oracle.pack([W.master_init(w, t) for t in range(d.n)], off, total)[idx]
+    one = oracle.adam_block(g, True, 0.25, dict(p=p0, mq=np.zeros(idx.size, np.int8),
+                                                  vq=np.zeros(idx.size, np.uint8),
+                                                  m_scale=0.0, v_scale=0.0), 1, HP)
+    assert np.array_equal(master[idx], one["p"]) and np.array_equal(mq[idx], one["mq"])
+    assert ms[q] == one["m_scale"]
