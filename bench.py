@@ -1,0 +1,374 @@
+"""Benchmark of the fused shard step (pack -> group norm/scale -> 8-bit AdamW ->
+unpack) through libvsf's C ABI on one GB300, one JSON line on stdout.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Metric: algorithmic HBM bytes of the step per second (GB/s) and parameters
+updated per second, against the measured HBM copy bandwidth. Algorithmic
+bytes per real element (bf16 gradients): pack 2+2, AdamW 2+1+1+4 read and
+1+1+4+2 written, unpack 2+2, i.e. 24 B, plus 16 B of scales per
+quantisation block. Padding is never touched, so it is not counted.
+
+Timing: W untimed steps, then K steps between a barrier and a device
+synchronise, CUDA events on the launch stream; the inputs (4.9 GB per step
+for the Llama layer) are larger than L2, so no flush is needed. Under torchrun
+(N > 1) every rank runs an independent replica of the workload (the m
+virtual ranks of one buffer live on one GPU); value = sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused shard-step HBM GB/s and params/s vs GB300 HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(n_real: int, n_qblocks: int, grad_bytes: int = 2) -> dict:
+    adam = n_real * (grad_bytes + 1 + 1 + 4 + 1 + 1 + 4 + 2) + 16 * n_qblocks
+    return dict(pack=n_real * 2 * grad_bytes, adam=adam, unpack=n_real * 4,
+                step=n_real * 2 * grad_bytes + adam + n_real * 4)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def sample_workload(w, fraction: float):
+    """The same tensor list with every tensor cut to about `fraction` of its
+    rows (whole atoms kept), for the CPU oracle's bounded sample."""
+    from synth.workloads import GRAN_ELEM, TensorSpec
+    ts = []
+    for t in w.tensors:
+        if t.gran == GRAN_ELEM:
+            n = max(w.g_coll, int(round(t.numel * fraction / w.g_coll)) * w.g_coll)
+            ts.append(TensorSpec(t.name, (min(n, t.numel),), t.gran))
+        else:
+            rows = max(t.block_rows, int(round(t.rows * fraction / t.block_rows)) * t.block_rows)
+            rows = min(rows, t.rows)
+            ts.append(TensorSpec(t.name, (rows, t.cols), t.gran, t.block_rows, t.tile_cols))
+    return w.with_(tensors=tuple(ts))
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_steps(w, steps: int):
+    """Runs the oracle's full step (pack, sumsq, factor, AdamW over every block,
+    unpack) `steps` times on workload w; returns (seconds per step, real
+    elements, quantisation blocks). Inputs are drawn outside the timing."""
+    import oracle
+    from synth import workloads as W
+    d = oracle.Desc.from_workload(w)
+    S, off = oracle.plan(d, w.m, w.g_coll)
+    qb = oracle.qblocks(d, w.g_coll, off)
+    total = w.m * S
+    master = oracle.pack([W.master_init(w, t) for t in range(d.n)], off, total)
+    ms, vs = np.zeros(total, np.int8), np.zeros(total, np.uint8)
+    nq = len(qb["base"])
+    msc, vsc = np.zeros(nq, np.float32), np.zeros(nq, np.float32)
+    bf = np.zeros(total, np.uint16)
+    hp = oracle.hparams(w)
+    numels = [t.numel for t in w.tensors]
+    times = []
+    for s in range(1, steps + 1):
+        grads = [W.grad(w, s, t) for t in range(d.n)]
+        t0 = time.perf_counter()
+        packed = oracle.pack(grads, off, total)
+        f, _ = oracle.factor(oracle.sumsq(grads), w.m, w.max_norm)
+        oracle.adam_all(qb, packed, f, True, ms, vs, msc, vsc, master, bf, s, hp)
+        oracle.unpack(bf, numels, off)
+        times.append(time.perf_counter() - t0)
+    return sum(times) / len(times), w.numel, nq
+
+
+def cpu_baseline(w, target_s: float = 12.0):
+    """The oracle as it stands, single thread, on a bounded sample of w."""
+    probe = sample_workload(w, min(1.0, 2e6 / w.numel))
+    t_probe, n_probe, _ = oracle_steps(probe, 1)
+    per_elem = t_probe / n_probe
+    steps = 2
+    frac = min(1.0, target_s / steps / per_elem / w.numel)
+    sw = sample_workload(w, frac)
+    t_step, n, nq = oracle_steps(sw, steps)
+    b = algorithmic_bytes(n, nq)
+    return dict(value=round(b["step"] / t_step / 1e9, 4), unit="GB/s",
+                params_per_s=round(n / t_step, 1), cores=1, kind="oracle",
+                sample=f"{w.name} with every tensor cut to {frac:.4f} of its rows "
+                       f"({n} real elements, {nq} quantisation blocks), {steps} full steps, "
+                       f"single thread; host has {os.cpu_count()} cores")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(rows))
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    from synth import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.get(args.workload)
+    specs = [TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
+    stream = torch.cuda.Stream(dev)
+    ss = ShardStep(specs, w.m, w.g_coll, max_norm=w.max_norm, stream=stream)
+    n_real, nq = ss.info.real, ss.info.n_qblocks
+    nbytes = algorithmic_bytes(n_real, nq)
+
+    # Per-tensor gradients and parameters, 16-byte aligned views of one buffer.
+    starts, cur = [], 0
+    for n in ss.numels:
+        starts.append(cur)
+        cur += (n + 7) // 8 * 8
+    host_g = torch.empty(cur, dtype=torch.int16).pin_memory()
+    hg = host_g.numpy().view(np.uint16)
+    for t, n in enumerate(ss.numels):
+        W.grad(w, 1, t, out=hg[starts[t]:starts[t] + n])
+        ss.load_master(t, torch.from_numpy(W.master_init(w, t)).to(dev))
+    dev_g = host_g.to(dev)
+    dev_p = torch.empty(cur, dtype=torch.int16, device=dev)
+    host_p = torch.empty(cur, dtype=torch.int16).pin_memory()
+    host_norm = torch.empty(2, dtype=torch.float64).pin_memory()
+    grads = [dev_g[s:s + n] for s, n in zip(starts, ss.numels)]
+    params = [dev_p[s:s + n] for s, n in zip(starts, ss.numels)]
+    torch.cuda.synchronize(dev)
+
+    launches_per_step = 2 + 1 + (1 if any(t.gran != W.GRAN_ELEM for t in w.tensors) else 0) + \
+        (1 if any(t.gran == W.GRAN_ELEM for t in w.tensors) else 0)
+    step = 0
+
+    def one_step(ev=None):
+        nonlocal step
+        step += 1
+        if ev is not None:
+            ev[0].record(stream)
+        ss.pack(grads)
+        ss.group_norm_scale()
+        if ev is not None:
+            ev[1].record(stream)
+        ss.adam(step)
+        if ev is not None:
+            ev[2].record(stream)
+        ss.unpack(params)
+        if ev is not None:
+            ev[3].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    torch.cuda.synchronize(dev)
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id  # type: ignore[attr-defined]
+    except Exception:
+        bus = None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(bus)
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            one_step(evs[i])
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    k_pack = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    k_adam = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    k_unpack = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    # End to end through the C ABI with host buffers: H2D of the step's
+    # gradients from pinned memory, the four calls, D2H of the parameters and
+    # of the norm, all inside the timed region.
+    e2e_steps = max(3, min(args.steps, 100))
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(e2e_steps):
+            dev_g.copy_(host_g, non_blocking=True)
+            one_step()
+            host_p.copy_(dev_p, non_blocking=True)
+            host_norm.copy_(ss.norm, non_blocking=True)
+        e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    peak, peak_kind = measured_peak()
+    adam_gbs = nbytes["adam"] / (k_adam * 1e-3) / 1e9
+    value = nbytes["step"] * world / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+        "params_per_s": round(n_real * world / (ms_step * 1e-3), 1),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "real_params": n_real, "m": w.m, "g_coll": w.g_coll,
+                   "S": ss.info.S, "padding_ratio": round(ss.info.padding_ratio, 5),
+                   "n_qblocks": nq, "grad_dtype": "bf16", "state": "int8 m / uint8 v, fp32 master",
+                   "bytes_per_step": nbytes["step"],
+                   "l2": f"inputs larger than L2 ({nbytes['step'] / 1e9:.2f} GB per step), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU, m virtual ranks",
+                   "kernel_ms": {"pack+norm": round(k_pack, 5), "adam8": round(k_adam, 5),
+                                 "unpack": round(k_unpack, 5)},
+                   "frac_of_peak_step": round(value / world / peak, 4)},
+        "roofline": {"bound": "hbm", "achieved": round(adam_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(adam_gbs / peak, 4),
+                     "traffic": TRAFFIC.get(w.name), "kernel": "vsf_adam8_step",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(nbytes["step"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": int(host_g.numel() * 2),
+                "d2h_bytes_per_step": int(host_p.numel() * 2 + 16)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# AdamW launch, from the ncu capture summarised in profiles/; None until taken
+# for the current kernel.
+TRAFFIC: dict = {}
+
+
+def reference_arm(args):
+    from synth import workloads as W
+    w = W.get(args.workload)
+    budget = float(os.environ.get("VSF_REFERENCE_BUDGET_S", "90"))
+    probe = sample_workload(w, min(1.0, 1e6 / w.numel))
+    t_probe, n_probe, _ = oracle_steps(probe, 1)
+    per_elem = t_probe / n_probe
+    frac = min(1.0, max(1e-6, budget / (args.steps + args.warmup) / per_elem / w.numel))
+    sw = sample_workload(w, frac)
+    t_step, n, nq = oracle_steps(sw, args.steps + args.warmup)
+    b = algorithmic_bytes(n, nq)
+    value = b["step"] / t_step / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "params_per_s": round(n / t_step, 1), "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "real_params": w.numel, "m": w.m, "g_coll": w.g_coll,
+                   "sample_real_params": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{w.name} cut to {frac:.5f} of its rows per step ({n} real "
+                                   f"elements), single thread; host has {os.cpu_count()} cores"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="vsf", choices=["vsf", "reference"])
+    ap.add_argument("--workload", default="llama_layer")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = gpu_arm(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            from synth import workloads as W
+            line["cpu_baseline"] = cpu_baseline(W.get(args.workload))
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,368 @@
+// plan.cpp — host-side layout planner of libvsf.
+//
+// Implements the layout rule of "veScale-FSDP: Flexible and High-Performance
+// FSDP at Scale (MLSys 2026)" summary page, 核心方法 › Grouped communication
+// (Algorithm 1) with the atoms of 核心方法 › RaggedShard:
+//   - minimise the uniform per-rank size S (Balanced Load), S a multiple of
+//     g_coll (ranks start on collective units) and S >= ceil(real / m);
+//   - every tensor contiguous (Contiguous Tensor Memory), padding only
+//     between tensors, offsets aligned to lcm(g_coll, atom);
+//   - no rank boundary inside an atom (Non-Sharded Block);
+//   - tensor order: input order, atom size or element count (descending).
+// The page solves placement with a monotone DP; for a fixed order, placing
+// each tensor at its earliest feasible offset is exact, because the earliest
+// feasible start at or after a cursor never decreases as the cursor grows.
+// Feasibility is not monotone in S (one 2-atom tensor of atom 10 on 2 ranks
+// fits S = 10 but not S = 11), so candidates are scanned upward.
+//
+// Speed: for one tensor at offset o the first boundary that cuts an atom is
+// k0*S or (k0+1)*S (k0 = first boundary past o): if k0*S is on an atom
+// boundary and the atom does not divide S, the next boundary is off by
+// S mod atom. So one placement costs O(1) per tensor and retry.
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <numeric>
+
+#include "vsf_internal.h"
+
+namespace vsf {
+
+namespace {
+thread_local std::string g_last_error;
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+int64_t gcd64(int64_t a, int64_t b) { return b == 0 ? a : gcd64(b, a % b); }
+
+int64_t round_up(int64_t x, int64_t a) {
+  int64_t r = x % a;
+  return r == 0 ? x : x + (a - r);
+}
+
+// Earliest feasible offset >= cursor for tensor x under per-rank size S, or
+// -1 if it would end past capacity.
+int64_t earliest_offset(const TensorInfo& x, int64_t S, int64_t capacity, int64_t cursor) {
+  int64_t o = round_up(cursor, x.align);
+  for (;;) {
+    if (o > capacity - x.numel) return -1;
+    const int64_t end = o + x.numel;
+    int64_t k0 = o / S + 1;
+    int64_t cut = -1;
+    for (int64_t k = k0; k <= k0 + 1; ++k) {
+      const int64_t boundary = k * S;
+      if (boundary >= end) break;
+      if ((boundary - o) % x.atom != 0) {
+        cut = boundary;
+        break;
+      }
+      if (S % x.atom == 0) break;  // every later boundary is on an atom edge too
+    }
+    if (cut < 0) return o;
+    o = round_up(cut, x.align);
+  }
+}
+
+bool place_all(const std::vector<TensorInfo>& ts, const std::vector<int>& order, int64_t m,
+               int64_t S, std::vector<int64_t>* offsets) {
+  int64_t capacity;
+  if (!mul_ok(m, S, &capacity)) return false;
+  int64_t cursor = 0;
+  for (int t : order) {
+    const TensorInfo& x = ts[t];
+    // Quick reject: a tensor longer than 2S spans two consecutive boundaries,
+    // which forces atom | S.
+    if (x.numel > 2 * S && S % x.atom != 0) return false;
+    int64_t o = earliest_offset(x, S, capacity, cursor);
+    if (o < 0) return false;
+    if (offsets) (*offsets)[t] = o;
+    cursor = o + x.numel;
+  }
+  return true;
+}
+
+std::vector<int> order_for(const std::vector<TensorInfo>& ts, int policy) {
+  std::vector<int> ord(ts.size());
+  std::iota(ord.begin(), ord.end(), 0);
+  if (policy == VSF_ORDER_BLOCK)
+    std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) { return ts[a].atom > ts[b].atom; });
+  else if (policy == VSF_ORDER_SHAPE)
+    std::stable_sort(ord.begin(), ord.end(),
+                     [&](int a, int b) { return ts[a].numel > ts[b].numel; });
+  return ord;
+}
+
+// Smallest feasible S for one order, or -1.
+int64_t scan_S(const std::vector<TensorInfo>& ts, const std::vector<int>& order, int64_t m,
+               int64_t g, int64_t real, int64_t* S_out_guard) {
+  int64_t lb = round_up((real + m - 1) / m, g);
+  // Everything aligned inside rank 0 always fits: an upper end for the scan.
+  int64_t ub = 0;
+  for (const TensorInfo& x : ts) ub += x.numel + x.align;
+  ub = round_up(ub, g);
+  for (int64_t S = lb; S <= std::max(lb, ub); S += g) {
+    if (place_all(ts, order, m, S, nullptr)) return S;
+  }
+  (void)S_out_guard;
+  return -1;
+}
+
+}  // namespace
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+vsf_status fail(vsf_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+const char* last_error() { return g_last_error.c_str(); }
+
+}  // namespace vsf
+
+using vsf::fail;
+
+extern "C" {
+
+vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, int64_t g_coll,
+                           int32_t order, vsf_plan** out) {
+  const auto t0 = std::chrono::steady_clock::now();
+  if (out == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_create: out is NULL");
+  *out = nullptr;
+  if (descs == nullptr || n < 1) return fail(VSF_ERR_ARG, "vsf_plan_create: no tensors");
+  if (m < 1) return fail(VSF_ERR_ARG, "vsf_plan_create: m must be >= 1");
+  if (g_coll < 1) return fail(VSF_ERR_ARG, "vsf_plan_create: g_coll must be >= 1");
+  if (order < VSF_ORDER_DEFAULT || order > VSF_ORDER_BEST3)
+    return fail(VSF_ERR_ARG, "vsf_plan_create: unknown order policy");
+
+  std::vector<vsf::TensorInfo> ts(n);
+  int64_t real = 0;
+  for (int t = 0; t < n; ++t) {
+    const vsf_tensor_desc& d = descs[t];
+    vsf::TensorInfo& x = ts[t];
+    if (d.ndim < 1 || d.ndim > 8)
+      return fail(VSF_ERR_ARG, "tensor " + std::to_string(t) + ": ndim must be 1..8");
+    int64_t rows = 1;
+    for (int k = 0; k < d.ndim; ++k)
+      if (d.shape[k] < 1) return fail(VSF_ERR_ARG, "tensor " + std::to_string(t) + ": empty dim");
+    for (int k = 0; k + 1 < d.ndim; ++k)
+      if (!vsf::mul_ok(rows, d.shape[k], &rows)) return fail(VSF_ERR_OVERFLOW, "rows overflow");
+    x.rows = rows;
+    x.cols = d.shape[d.ndim - 1];
+    if (!vsf::mul_ok(x.rows, x.cols, &x.numel)) return fail(VSF_ERR_OVERFLOW, "numel overflow");
+    x.gran = d.gran;
+    x.block_rows = d.block_rows;
+    x.tile_cols = d.tile_cols;
+    if (x.gran == VSF_GRAN_ELEM) {
+      x.atom = 1;
+    } else if (x.gran == VSF_GRAN_ROWS || x.gran == VSF_GRAN_TILE) {
+      if (x.block_rows < 1)
+        return fail(VSF_ERR_ARG, "tensor " + std::to_string(t) + ": block_rows must be >= 1");
+      if (x.gran == VSF_GRAN_TILE && x.tile_cols < 1)
+        return fail(VSF_ERR_ARG, "tensor " + std::to_string(t) + ": tile_cols must be >= 1");
+      if (!vsf::mul_ok(x.block_rows, x.cols, &x.atom)) return fail(VSF_ERR_OVERFLOW, "atom");
+    } else {
+      return fail(VSF_ERR_ARG, "tensor " + std::to_string(t) + ": unknown granularity");
+    }
+    const int64_t q = g_coll / vsf::gcd64(g_coll, x.atom);
+    if (!vsf::mul_ok(q, x.atom, &x.align)) return fail(VSF_ERR_OVERFLOW, "alignment overflow");
+    if (real > INT64_MAX - x.numel) return fail(VSF_ERR_OVERFLOW, "total overflow");
+    real += x.numel;
+  }
+  // Headroom so that offsets + spans + alignment never overflow.
+  if (real > (INT64_MAX >> 4)) return fail(VSF_ERR_OVERFLOW, "too many elements");
+
+  int64_t best_S = -1;
+  int used = VSF_ORDER_DEFAULT;
+  const int first = order == VSF_ORDER_BEST3 ? VSF_ORDER_DEFAULT : order;
+  const int last = order == VSF_ORDER_BEST3 ? VSF_ORDER_SHAPE : order;
+  for (int p = first; p <= last; ++p) {
+    int64_t S = vsf::scan_S(ts, vsf::order_for(ts, p), m, g_coll, real, nullptr);
+    if (S >= 0 && (best_S < 0 || S < best_S)) {
+      best_S = S;
+      used = p;
+    }
+  }
+  if (best_S < 0) return fail(VSF_ERR_INFEASIBLE, "no feasible layout");
+
+  std::vector<int64_t> offsets(n);
+  vsf::place_all(ts, vsf::order_for(ts, used), m, best_S, &offsets);
+
+  auto* plan = new vsf_plan();
+  plan->n = n;
+  plan->m = m;
+  plan->g_coll = g_coll;
+  plan->S = best_S;
+  plan->total = (int64_t)m * best_S;
+  plan->real = real;
+  plan->order_used = used;
+  for (int t = 0; t < n; ++t) ts[t].offset = offsets[t];
+  plan->tensors = ts;
+
+  // Quantisation blocks, tensor order ([VSF] case study › 8-bit Adam).
+  for (int t = 0; t < n; ++t) {
+    const vsf::TensorInfo& x = ts[t];
+    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, bool small) {
+      vsf::QBlock b{};
+      b.base = base;
+      b.nrows = (int32_t)nr;
+      b.ncols = (int32_t)nc;
+      b.stride = (int32_t)st;
+      b.tensor = t;
+      (small ? plan->small_blocks : plan->big_blocks).push_back((int32_t)plan->qblocks.size());
+      if (!small) plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
+      plan->qblocks.push_back(b);
+    };
+    if (x.gran == VSF_GRAN_ELEM) {
+      if (g_coll > INT32_MAX) {
+        delete plan;
+        return fail(VSF_ERR_OVERFLOW, "g_coll too large for element-granular blocks");
+      }
+      for (int64_t e = 0; e < x.numel; e += g_coll) {
+        int64_t len = std::min(g_coll, x.numel - e);
+        add(x.offset + e, 1, len, len, true);
+      }
+    } else {
+      const int64_t tc = x.gran == VSF_GRAN_TILE ? x.tile_cols : x.cols;
+      for (int64_t r = 0; r < x.rows; r += x.block_rows) {
+        const int64_t nr = std::min(x.block_rows, x.rows - r);
+        for (int64_t c = 0; c < x.cols; c += tc) {
+          const int64_t nc = std::min(tc, x.cols - c);
+          if (x.gran == VSF_GRAN_ROWS) {
+            // a whole-row block is contiguous: one row of nr*cols elements
+            if (nr * x.cols > INT32_MAX) {
+              delete plan;
+              return fail(VSF_ERR_OVERFLOW, "quantisation block larger than 2^31 elements");
+            }
+            add(x.offset + r * x.cols, 1, nr * x.cols, nr * x.cols, false);
+          } else {
+            if (x.cols > INT32_MAX) {
+              delete plan;
+              return fail(VSF_ERR_OVERFLOW, "row longer than 2^31 elements");
+            }
+            add(x.offset + r * x.cols + c, nr, nc, x.cols, false);
+          }
+        }
+      }
+    }
+  }
+
+  // Device workspace layout (16-byte aligned sections).
+  vsf::DeviceLayout& L = plan->layout;
+  size_t cur = 0;
+  auto section = [&](size_t bytes) {
+    size_t at = (cur + 255) / 256 * 256;
+    cur = at + bytes;
+    return at;
+  };
+  L.tensor_off = section(sizeof(int64_t) * n);
+  L.tensor_numel = section(sizeof(int64_t) * n);
+  L.qblocks = section(sizeof(vsf::QBlock) * plan->qblocks.size());
+  L.big = section(sizeof(int32_t) * std::max<size_t>(1, plan->big_blocks.size()));
+  L.small = section(sizeof(int32_t) * std::max<size_t>(1, plan->small_blocks.size()));
+  L.spans = section(sizeof(vsf::CopySpan) * (vsf::kMaxCopyGrid + 1));
+  L.partials = section(sizeof(double) * vsf::kMaxCopyGrid);
+  L.bytes = (cur + 255) / 256 * 256;
+
+  plan->plan_seconds =
+      std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+  *out = plan;
+  return VSF_OK;
+}
+
+void vsf_plan_destroy(vsf_plan* plan) { delete plan; }
+
+vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return fail(VSF_ERR_ARG, "NULL argument");
+  std::memset(info, 0, sizeof(*info));
+  info->S = plan->S;
+  info->total = plan->total;
+  info->real = plan->real;
+  info->n_qblocks = (int64_t)plan->qblocks.size();
+  info->n_tensors = plan->n;
+  info->m = plan->m;
+  info->g_coll = plan->g_coll;
+  info->padding_ratio = 1.0 - (double)plan->real / (double)plan->total;
+  info->plan_seconds = plan->plan_seconds;
+  info->order_used = plan->order_used;
+  return VSF_OK;
+}
+
+vsf_status vsf_plan_offsets(const vsf_plan* plan, int64_t* offsets) {
+  if (plan == nullptr || offsets == nullptr) return fail(VSF_ERR_ARG, "NULL argument");
+  for (int t = 0; t < plan->n; ++t) offsets[t] = plan->tensors[t].offset;
+  return VSF_OK;
+}
+
+vsf_status vsf_plan_qblocks(const vsf_plan* plan, int32_t* tensor, int64_t* base, int64_t* nrows,
+                            int64_t* ncols, int64_t* stride) {
+  if (plan == nullptr) return fail(VSF_ERR_ARG, "NULL plan");
+  for (size_t q = 0; q < plan->qblocks.size(); ++q) {
+    const vsf::QBlock& b = plan->qblocks[q];
+    const vsf::TensorInfo& x = plan->tensors[b.tensor];
+    // ROWS blocks are stored as one contiguous row; report them as rows x cols.
+    const bool rows_block = x.gran == VSF_GRAN_ROWS;
+    if (tensor) tensor[q] = b.tensor;
+    if (base) base[q] = b.base;
+    if (nrows) nrows[q] = rows_block ? b.ncols / x.cols : b.nrows;
+    if (ncols) ncols[q] = rows_block ? x.cols : b.ncols;
+    if (stride) stride[q] = rows_block ? x.cols : b.stride;
+  }
+  return VSF_OK;
+}
+
+vsf_status vsf_plan_rank_slices(const vsf_plan* plan, int32_t rank, int32_t capacity,
+                                int32_t* count, int32_t* tensor, int64_t* elem_begin,
+                                int64_t* elem_end, int64_t* atom_begin, int64_t* atom_end) {
+  if (plan == nullptr || count == nullptr) return fail(VSF_ERR_ARG, "NULL argument");
+  if (rank < 0 || rank >= plan->m) return fail(VSF_ERR_ARG, "rank out of range");
+  std::vector<int> by_offset(plan->n);
+  std::iota(by_offset.begin(), by_offset.end(), 0);
+  std::sort(by_offset.begin(), by_offset.end(), [&](int a, int b) {
+    return plan->tensors[a].offset < plan->tensors[b].offset;
+  });
+  const int64_t lo = (int64_t)rank * plan->S, hi = lo + plan->S;
+  int32_t k = 0;
+  for (int t : by_offset) {
+    const vsf::TensorInfo& x = plan->tensors[t];
+    const int64_t b = std::max(lo, x.offset), e = std::min(hi, x.offset + x.numel);
+    if (b >= e) continue;
+    if (k < capacity) {
+      if (tensor) tensor[k] = t;
+      if (elem_begin) elem_begin[k] = b - x.offset;
+      if (elem_end) elem_end[k] = e - x.offset;
+      if (atom_begin) atom_begin[k] = (b - x.offset) / x.atom;
+      if (atom_end) atom_end[k] = (e - x.offset + x.atom - 1) / x.atom;
+    }
+    ++k;
+  }
+  *count = k;
+  return VSF_OK;
+}
+
+size_t vsf_plan_workspace_bytes(const vsf_plan* plan) {
+  return plan == nullptr ? 0 : plan->layout.bytes;
+}
+
+const char* vsf_status_string(vsf_status s) {
+  switch (s) {
+    case VSF_OK: return "ok";
+    case VSF_ERR_ARG: return "invalid argument";
+    case VSF_ERR_INFEASIBLE: return "no feasible layout";
+    case VSF_ERR_OVERFLOW: return "size overflow";
+    case VSF_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case VSF_ERR_CUDA: return "CUDA error";
+    case VSF_ERR_STATE: return "call out of order";
+    default: return "unknown status";
+  }
+}
+
+const char* vsf_last_error(void) { return vsf::last_error(); }
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// vsf_internal.h — plan representation shared by the host planner
+// (plan.cpp) and the kernels (vsf_kernels.cu) inside libvsf. Not installed.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "vsf.h"
+
+namespace vsf {
+
+// Most per-tensor device pointers one pack / unpack launch takes by value
+// (16 KB of kernel parameters).
+constexpr int kMaxTensors = 2048;
+// Upper bound of the copy grid, which fixes the workspace size before the
+// device is known.
+constexpr int kMaxCopyGrid = 4096;
+
+// One quantisation block as the kernels see it: a row-major region.
+struct QBlock {
+  int64_t base;    // buffer element of the first element
+  int32_t nrows;   // rows in the block
+  int32_t ncols;   // elements per row
+  int32_t stride;  // elements between row starts
+  int32_t tensor;
+  int64_t pad;
+};
+static_assert(sizeof(QBlock) == 32, "QBlock is a 32-byte device record");
+
+// Where one CTA of the copy grid starts in the concatenation of all real
+// elements (tensor order).
+struct CopySpan {
+  int32_t tensor;
+  int32_t pad;
+  int64_t elem;
+};
+
+struct TensorInfo {
+  int64_t rows, cols, numel;
+  int32_t gran;
+  int64_t block_rows, tile_cols;
+  int64_t atom, align;
+  int64_t offset;
+};
+
+struct DeviceLayout {
+  size_t tensor_off = 0, tensor_numel = 0;  // int64[n] each
+  size_t qblocks = 0;                       // QBlock[n_qblocks]
+  size_t big = 0, small = 0;                // int32 lists of block indices
+  size_t spans = 0;                         // CopySpan[kMaxCopyGrid + 1]
+  size_t partials = 0;                      // double[kMaxCopyGrid]
+  size_t bytes = 0;
+};
+
+}  // namespace vsf
+
+struct vsf_plan {
+  int32_t n = 0, m = 0;
+  int64_t g_coll = 0, S = 0, total = 0, real = 0;
+  int32_t order_used = 0;
+  double plan_seconds = 0.0;
+  std::vector<vsf::TensorInfo> tensors;
+  std::vector<vsf::QBlock> qblocks;
+  std::vector<int32_t> big_blocks;    // ROWS / TILE blocks: cluster kernel
+  std::vector<int32_t> small_blocks;  // ELEM chunks: warp kernel
+  int64_t max_big_elems = 0;
+  vsf::DeviceLayout layout;
+
+  // Set by vsf_plan_upload.
+  bool uploaded = false;
+  unsigned char* d_ws = nullptr;
+  int device = -1;
+  int sm_count = 0;
+  int copy_grid = 0;
+  int adam_cluster = 1;
+  int adam_clusters = 0;
+  std::vector<unsigned char> upload_image;  // host source of the last upload copy
+};
+
+namespace vsf {
+void set_error(const std::string& msg);
+vsf_status fail(vsf_status s, const std::string& msg);
+}  // namespace vsf

@@ -1,0 +1,111 @@
+"""ShardStep: device buffers of one planned DBuffer (allocated with torch)
+and the four per-step calls of libvsf, in order, on one CUDA stream.
+
+Argument marshalling only: every step of the path runs in libvsf's kernels.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import vsf as V
+
+
+@dataclasses.dataclass
+class TensorSpec:
+    shape: tuple
+    gran: int
+    block_rows: int = 0
+    tile_cols: int = 0
+
+
+class ShardStep:
+    """One DBuffer of m virtual ranks on the current CUDA device.
+
+    Buffers (m*S elements each unless noted): packed_grad (bf16 or fp32),
+    master (fp32), m_state / v_state (int8 / uint8 codes, or fp32 when
+    quantized=False), m_scale / v_scale (fp32, one per quantisation block),
+    packed_bf16 (bf16 bits), factor (fp32 scalar), norm (fp64 scalar).
+    """
+
+    def __init__(self, specs, m: int, g_coll: int, *, order: int = V.VSF_ORDER_DEFAULT,
+                 grad_dtype: int = V.VSF_BF16, quantized: bool = True, lr=1e-3, beta1=0.9,
+                 beta2=0.999, eps=1e-8, weight_decay=0.01, max_norm=float("inf"),
+                 world: int | None = None, device=None, stream: torch.cuda.Stream | None = None):
+        self.specs = list(specs)
+        self.m, self.g_coll = m, g_coll
+        self.grad_dtype = grad_dtype
+        self.quantized = quantized
+        descs = [V.make_desc(s.shape, s.gran, s.block_rows, s.tile_cols) for s in self.specs]
+        self.plan = V.vsf_plan_create(descs, m, g_coll, order)
+        self.info = V.vsf_plan_get_info(self.plan)
+        self.offsets = V.vsf_plan_offsets(self.plan, len(self.specs))
+        self.numels = [int(torch.Size(s.shape).numel()) for s in self.specs]
+        self.hp = V.make_hparams(lr, beta1, beta2, eps, weight_decay, max_norm,
+                                 m if world is None else world, int(quantized))
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        total, nq = self.info.total, self.info.n_qblocks
+        dev = self.device
+        gdt = torch.bfloat16 if grad_dtype == V.VSF_BF16 else torch.float32
+        with torch.cuda.device(dev):
+            self.workspace = torch.empty(V.vsf_plan_workspace_bytes(self.plan), dtype=torch.uint8,
+                                         device=dev)
+            self.packed_grad = torch.zeros(total, dtype=gdt, device=dev)
+            self.master = torch.zeros(total, dtype=torch.float32, device=dev)
+            sdt = (torch.int8, torch.uint8) if quantized else (torch.float32, torch.float32)
+            self.m_state = torch.zeros(total, dtype=sdt[0], device=dev)
+            self.v_state = torch.zeros(total, dtype=sdt[1], device=dev)
+            self.m_scale = torch.zeros(max(nq, 1), dtype=torch.float32, device=dev)
+            self.v_scale = torch.zeros(max(nq, 1), dtype=torch.float32, device=dev)
+            self.packed_bf16 = torch.zeros(total, dtype=torch.bfloat16, device=dev)
+            self.factor = torch.zeros(4, dtype=torch.float32, device=dev)
+            self.norm = torch.zeros(2, dtype=torch.float64, device=dev)
+            V.vsf_plan_upload(self.plan, self.workspace.data_ptr(), self.workspace.numel(),
+                              self.stream.cuda_stream)
+
+    def close(self):
+        if self.plan:
+            V.vsf_plan_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- the four per-step calls (asynchronous on self.stream)
+    def pack(self, grads):
+        V.vsf_pack(self.plan, [g.data_ptr() for g in grads], self.grad_dtype,
+                   self.packed_grad.data_ptr(), self.stream.cuda_stream)
+
+    def group_norm_scale(self, standalone: bool = False):
+        V.vsf_group_norm_scale(self.plan, self.packed_grad.data_ptr() if standalone else None,
+                               self.grad_dtype, self.hp, self.factor.data_ptr(),
+                               self.norm.data_ptr(), self.stream.cuda_stream)
+
+    def adam(self, step: int):
+        V.vsf_adam8_step(self.plan, self.packed_grad.data_ptr(), self.grad_dtype,
+                         self.factor.data_ptr(), self.master.data_ptr(), self.m_state.data_ptr(),
+                         self.v_state.data_ptr(), self.m_scale.data_ptr(),
+                         self.v_scale.data_ptr(), self.packed_bf16.data_ptr(), self.hp, step,
+                         self.stream.cuda_stream)
+
+    def unpack(self, params):
+        V.vsf_unpack(self.plan, self.packed_bf16.data_ptr(), [p.data_ptr() for p in params],
+                     self.stream.cuda_stream)
+
+    def step(self, grads, params, step: int):
+        """pack -> group norm/scale -> 8-bit AdamW -> unpack."""
+        self.pack(grads)
+        self.group_norm_scale()
+        self.adam(step)
+        self.unpack(params)
+
+    # ---- harness helpers
+    def load_master(self, t: int, values: torch.Tensor):
+        o = self.offsets[t]
+        self.master[o:o + self.numels[t]].copy_(values.reshape(-1))

@@ -1,0 +1,204 @@
+/*
+ * vsf.h — C ABI of libvsf: the local per-step data path of structure-aware
+ * FSDP on one GB300 (sm_103a), with all m virtual ranks in one buffer.
+ *
+ * Sources, cited by page title and section:
+ *   [VSF]  "veScale-FSDP: Flexible and High-Performance FSDP at Scale
+ *          (MLSys 2026)" summary page:
+ *            核心方法 › RaggedShard            (atoms: element / row / 2-D block)
+ *            核心方法 › Grouped communication  (Algorithm 1: layout planning)
+ *            核心方法 › Distributed Buffer     (one global buffer, fused group
+ *                                               ops add/scale/zero/copy, fixed
+ *                                               address map)
+ *            结构感知训练 case study › 8-bit Adam (per-block quantisation kept
+ *                                               local by intact blocks)
+ *   [FSDP] "FSDP" concept page › 关键观察 (copy-in / copy-out cost around the
+ *          collective buffer).
+ *
+ * Conventions for every call:
+ *   - Every function returns a vsf_status; no exception crosses the ABI.
+ *     vsf_last_error() gives a thread-local message for the last failure.
+ *   - The plan and its host tables are owned by the library. ALL device
+ *     memory (workspace, buffers, per-tensor tensors) is owned by the caller;
+ *     the library never allocates device memory and never synchronises.
+ *   - Device pointers must be 16-byte aligned (VSF_ERR_ALIGN otherwise).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Kernels are enqueued asynchronously on it; a launch failure is
+ *     VSF_ERR_CUDA.
+ *   - Buffers indexed by "buffer element" hold m*S elements (see
+ *     vsf_plan_info.total); virtual rank r owns elements [r*S, (r+1)*S).
+ *     Padding elements are never read or written by the per-step calls.
+ */
+#ifndef VSF_H
+#define VSF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t vsf_status;
+enum {
+  VSF_OK = 0,
+  VSF_ERR_ARG = -1,        /* bad argument or descriptor */
+  VSF_ERR_INFEASIBLE = -2, /* no layout found */
+  VSF_ERR_OVERFLOW = -3,   /* sizes overflow 64-bit element indices */
+  VSF_ERR_ALIGN = -4,      /* a device pointer is not 16-byte aligned */
+  VSF_ERR_CUDA = -5,       /* a CUDA call or kernel launch failed */
+  VSF_ERR_STATE = -6       /* call out of order (e.g. plan not uploaded) */
+};
+
+/* Shard atom of a tensor ([VSF] 核心方法 › RaggedShard). A tensor of shape
+ * [d0 .. dk-1] is viewed as R = d0*..*dk-2 rows of C = dk-1 elements.
+ *   ELEM: atom = 1 element; quantisation blocks are g_coll consecutive
+ *         elements from the tensor start.
+ *   ROWS: atom = block_rows whole rows; one quantisation block per atom.
+ *   TILE: atom = block_rows whole rows (a stripe); one quantisation block
+ *         per block_rows x tile_cols tile of the stripe.
+ * The last block of a tensor may be short. */
+enum { VSF_GRAN_ELEM = 0, VSF_GRAN_ROWS = 1, VSF_GRAN_TILE = 2 };
+
+/* Tensor order tried by the planner ([VSF] Algorithm 1, first step): input
+ * order, atom size descending, element count descending (ties keep input
+ * order), or the best of the three (ties prefer the earlier one). */
+enum { VSF_ORDER_DEFAULT = 0, VSF_ORDER_BLOCK = 1, VSF_ORDER_SHAPE = 2, VSF_ORDER_BEST3 = 3 };
+
+/* Element type of gradients (per-tensor and packed). Parameters are bf16. */
+enum { VSF_BF16 = 0, VSF_FP32 = 1 };
+
+typedef struct {
+  int32_t ndim;       /* 1..8 */
+  int32_t gran;       /* VSF_GRAN_* */
+  int64_t shape[8];   /* shape[0..ndim) */
+  int64_t block_rows; /* ROWS / TILE: rows per atom; ignored for ELEM */
+  int64_t tile_cols;  /* TILE: columns per quantisation tile */
+} vsf_tensor_desc;
+
+/* AdamW hyper-parameters ([VSF] case study › 8-bit Adam, with the readings
+ * documented for vsf_adam8_step). world = number of ranks whose gradients the
+ * packed buffer sums; max_norm <= 0 or non-finite disables clipping;
+ * quantized = 1 for 8-bit moments, 0 for fp32 moments. */
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay, max_norm;
+  int32_t world;
+  int32_t quantized;
+} vsf_adam_hparams;
+
+typedef struct {
+  int64_t S;             /* uniform per-rank size in elements */
+  int64_t total;         /* m * S, elements of every packed buffer */
+  int64_t real;          /* real (non-padding) elements */
+  int64_t n_qblocks;     /* quantisation blocks = entries of m_scale / v_scale */
+  int32_t n_tensors, m;
+  int64_t g_coll;
+  double padding_ratio;  /* 1 - real / total */
+  double plan_seconds;   /* host time spent in vsf_plan_create */
+  int32_t order_used;    /* VSF_ORDER_* actually chosen */
+  int32_t reserved;
+} vsf_plan_info;
+
+typedef struct vsf_plan vsf_plan; /* opaque */
+
+/* Plans the layout ([VSF] 核心方法 › Grouped communication, Algorithm 1): the
+ * smallest uniform per-rank size S, a multiple of g_coll and at least
+ * ceil(real/m), such that tensors placed one after another in the chosen
+ * order, each at the earliest offset that is a multiple of lcm(g_coll, atom)
+ * and that no rank boundary k*S cuts inside an atom, end within m*S. Padding
+ * sits only between tensors. Host only; no CUDA call.
+ * Errors: VSF_ERR_ARG (bad descriptor, n < 1, m < 1, g_coll < 1),
+ * VSF_ERR_OVERFLOW, VSF_ERR_INFEASIBLE. On success *out owns a new plan. */
+vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, int64_t g_coll,
+                           int32_t order, vsf_plan** out);
+void vsf_plan_destroy(vsf_plan* plan);
+
+vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info);
+
+/* Per-tensor element offsets into the m*S buffer; offsets has n entries. */
+vsf_status vsf_plan_offsets(const vsf_plan* plan, int64_t* offsets);
+
+/* Quantisation-block table, in tensor order then stripe, then tile: block q
+ * is the row-major region of nrows rows x ncols elements starting at buffer
+ * element base[q], rows `stride` elements apart, of tensor tensor[q]. Arrays
+ * have n_qblocks entries (any may be NULL). */
+vsf_status vsf_plan_qblocks(const vsf_plan* plan, int32_t* tensor, int64_t* base, int64_t* nrows,
+                            int64_t* ncols, int64_t* stride);
+
+/* RaggedShard slice of virtual rank `rank` ([VSF] 核心方法 › RaggedShard:
+ * uneven, whole atoms): for each tensor overlapping [rank*S, (rank+1)*S), in
+ * buffer order, the tensor index, its element range [elem_begin, elem_end)
+ * and its atom range [atom_begin, atom_end). Writes at most `capacity`
+ * entries and the full count into *count (call with capacity 0 to size). */
+vsf_status vsf_plan_rank_slices(const vsf_plan* plan, int32_t rank, int32_t capacity,
+                                int32_t* count, int32_t* tensor, int64_t* elem_begin,
+                                int64_t* elem_end, int64_t* atom_begin, int64_t* atom_end);
+
+/* Bytes of device workspace the caller must provide to vsf_plan_upload. */
+size_t vsf_plan_workspace_bytes(const vsf_plan* plan);
+
+/* Copies the plan's device tables into the caller's workspace (16-byte
+ * aligned, vsf_plan_workspace_bytes long) on `stream`, zeroes its scratch,
+ * and binds the plan to the current CUDA device. Must precede every per-step
+ * call; the workspace must stay allocated while the plan is used. Calls that
+ * share one plan (and so one workspace) must be ordered on the device. */
+vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void* stream);
+
+/* Copy-in with the fused squared-norm reduction ([FSDP] 关键观察; [VSF]
+ * Distributed Buffer, group copy): packed_grad[offset_t + i] = grads[t][i]
+ * for every real element. grads is a HOST array of n device pointers, each
+ * 16-byte aligned, of the tensor's element type (dtype VSF_BF16 or
+ * VSF_FP32); packed_grad has m*S elements of that type. Also leaves per-CTA
+ * fp64 partial sums of g^2 in the workspace for vsf_group_norm_scale. */
+vsf_status vsf_pack(const vsf_plan* plan, const void* const* grads, int32_t dtype,
+                    void* packed_grad, void* stream);
+
+/* Group norm and scale ([VSF] Distributed Buffer, fused group scale):
+ * sumsq = sum of g^2 over every real element (fp64); norm = sqrt(sumsq) /
+ * world (the norm of the mean gradient, the packed buffer being the sum over
+ * `world` ranks); c = min(1, max_norm / (norm + 1e-6)) when clipping is on,
+ * else 1; writes *d_factor = fp32(c / world) and *d_norm = norm (both device
+ * pointers; d_norm may be NULL). With packed_grad == NULL the partial sums
+ * left by the last vsf_pack on this plan are used; otherwise they are
+ * recomputed from packed_grad (element type dtype). */
+vsf_status vsf_group_norm_scale(const vsf_plan* plan, const void* packed_grad, int32_t dtype,
+                                const vsf_adam_hparams* hp, float* d_factor, double* d_norm,
+                                void* stream);
+
+/* Block-wise 8-bit AdamW on every virtual rank's RaggedShard slice ([VSF]
+ * case study › 8-bit Adam; blocks never cross a rank, so every scale is
+ * local). Per element, in fp32 with every operation rounded once:
+ *   g = factor * grad;  m = b1*m' + (1-b1)*g;  v = b2*v' + (1-b2)*g*g;
+ *   p = p * (1 - lr*wd);  p = p - step_size * (m / (sqrt(v)/bc2s + eps)),
+ *   step_size = lr / (1 - b1^step), bc2s = sqrt(1 - b2^step), the constants
+ *   computed in double and rounded once to fp32; bf16 = RNE(p).
+ * quantized = 1: m' = code_m * (m_scale[q] / 127), v' = code_v *
+ *   (v_scale[q] / 255); after the update each block q gets m_scale[q] =
+ *   max|m|, v_scale[q] = max v and codes round-half-even(m * (127/m_scale)),
+ *   clamped to [-127, 127] (int8), and round-half-even(v * (255/v_scale)),
+ *   clamped to [0, 255] (uint8); a zero scale gives all-zero codes.
+ *   m_state / v_state: int8 / uint8 arrays of m*S; m_scale / v_scale: fp32
+ *   arrays of n_qblocks. Initial state: codes 0, scales 0, step 1.
+ * quantized = 0: m_state / v_state are fp32 arrays of m*S; scales unused.
+ * packed_grad: m*S elements of grad_dtype; d_factor: device fp32 scalar (from
+ * vsf_group_norm_scale); master: fp32 m*S (in/out); packed_bf16: bf16 bits,
+ * m*S (out). step >= 1. */
+vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t grad_dtype,
+                          const float* d_factor, float* master, void* m_state, void* v_state,
+                          float* m_scale, float* v_scale, uint16_t* packed_bf16,
+                          const vsf_adam_hparams* hp, int32_t step, void* stream);
+
+/* Copy-out ([FSDP] 关键观察; [VSF] Distributed Buffer, group copy):
+ * params[t][i] = packed_bf16[offset_t + i]. params is a HOST array of n
+ * device pointers (bf16, 16-byte aligned). */
+vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* const* params,
+                      void* stream);
+
+const char* vsf_status_string(vsf_status s);
+const char* vsf_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSF_H */

@@ -1,0 +1,169 @@
+"""Shared driver for the GPU parity tests: runs the same seeded steps through
+libvsf (via ShardStep) and through the oracle, and compares the results.
+
+Tolerances (the shard-step spec): layout, copy-in and copy-out bit-exact;
+master weights within 1e-6 max relative error; quantised moment codes may
+differ by at most 1 at no more than 1e-4 of positions; scales and bf16
+copies compared after the master check. The kernels are written to be
+bit-exact (same fp32 op order, one rounding per operation), so the tests also
+report how many elements match exactly.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+from synth import workloads as W
+
+MASTER_RTOL = 1e-6
+CODE_FRAC = 1e-4
+
+
+@dataclasses.dataclass
+class Case:
+    specs: list          # (shape, gran, block_rows, tile_cols)
+    m: int
+    g_coll: int
+    steps: int
+    grads: callable      # (step, t) -> np.uint16 (bf16 bits) or np.float32 array
+    masters: callable    # t -> np.float32 array
+    max_norm: float = math.inf
+    quantized: bool = True
+    grad_dtype: int = 0  # 0 bf16, 1 fp32
+    world: int | None = None
+    standalone_norm: bool = False
+
+    @property
+    def numels(self):
+        return [int(np.prod(s[0])) for s in self.specs]
+
+
+def case_from_workload(w: W.Workload, steps=None, **kw) -> Case:
+    fp32 = kw.get("grad_dtype", 0) == 1
+    return Case(specs=[(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors],
+                m=w.m, g_coll=w.g_coll, steps=w.steps if steps is None else steps,
+                grads=(lambda s, t: W.grad_f32(w, s, t)) if fp32 else (lambda s, t: W.grad(w, s, t)),
+                masters=lambda t: W.master_init(w, t), max_norm=w.max_norm, **kw)
+
+
+def hp_dict():
+    return dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+def _desc(case: Case) -> oracle.Desc:
+    rows = [int(np.prod(s[0][:-1])) if len(s[0]) > 1 else 1 for s in case.specs]
+    return oracle.Desc(rows, [s[0][-1] for s in case.specs], [s[1] for s in case.specs],
+                       [s[2] for s in case.specs], [s[3] for s in case.specs])
+
+
+def run_oracle(case: Case):
+    d = _desc(case)
+    S, off = oracle.plan(d, case.m, case.g_coll)
+    qb = oracle.qblocks(d, case.g_coll, off)
+    total = case.m * S
+    nq = len(qb["base"])
+    world = case.m if case.world is None else case.world
+    master = oracle.pack([case.masters(t) for t in range(d.n)], off, total)
+    if case.quantized:
+        ms, vs = np.zeros(total, np.int8), np.zeros(total, np.uint8)
+    else:
+        ms, vs = np.zeros(total, np.float32), np.zeros(total, np.float32)
+    msc, vsc = np.zeros(nq, np.float32), np.zeros(nq, np.float32)
+    bf = np.zeros(total, np.uint16)
+    factors, norms = [], []
+    for s in range(1, case.steps + 1):
+        grads = [case.grads(s, t) for t in range(d.n)]
+        packed = oracle.pack(grads, off, total)
+        f, norm = oracle.factor(oracle.sumsq(grads), world, case.max_norm)
+        factors.append(f)
+        norms.append(norm)
+        oracle.adam_all(qb, packed, f, case.quantized, ms, vs, msc, vsc, master, bf, s, hp_dict())
+    params = oracle.unpack(bf, case.numels, off)
+    return dict(S=S, offsets=off, packed_grad=packed, master=master, m_state=ms, v_state=vs,
+                m_scale=msc, v_scale=vsc, packed_bf16=bf, params=params, factors=factors,
+                norms=norms)
+
+
+def run_gpu(case: Case):
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    specs = [TensorSpec(tuple(s[0]), s[1], s[2], s[3]) for s in case.specs]
+    ss = ShardStep(specs, case.m, case.g_coll, grad_dtype=case.grad_dtype,
+                   quantized=case.quantized, max_norm=case.max_norm, world=case.world)
+    try:
+        dev = ss.device
+        for t in range(len(specs)):
+            ss.load_master(t, torch.from_numpy(case.masters(t)).to(dev))
+        gdt = torch.int16 if case.grad_dtype == 0 else torch.float32
+        grads = [torch.empty(n, dtype=gdt, device=dev) for n in case.numels]
+        params = [torch.empty(n, dtype=torch.int16, device=dev) for n in case.numels]
+        factors, norms = [], []
+        for s in range(1, case.steps + 1):
+            for t, g in enumerate(grads):
+                h = case.grads(s, t)
+                g.copy_(torch.from_numpy(h.view(np.int16) if case.grad_dtype == 0 else h))
+            ss.pack(grads)
+            ss.group_norm_scale(standalone=case.standalone_norm)
+            ss.adam(s)
+            ss.unpack(params)
+            torch.cuda.synchronize()
+            factors.append(float(ss.factor[0].item()))
+            norms.append(float(ss.norm[0].item()))
+        host = lambda x: x.cpu().numpy()  # noqa: E731
+        out = dict(S=ss.info.S, offsets=np.array(ss.offsets), packed_grad=host(ss.packed_grad),
+                   master=host(ss.master), m_state=host(ss.m_state), v_state=host(ss.v_state),
+                   m_scale=host(ss.m_scale)[:ss.info.n_qblocks],
+                   v_scale=host(ss.v_scale)[:ss.info.n_qblocks],
+                   packed_bf16=host(ss.packed_bf16).view(np.uint16),
+                   params=[host(p).view(np.uint16) for p in params], factors=factors,
+                   norms=norms)
+        if case.grad_dtype == 0:
+            out["packed_grad"] = out["packed_grad"].view(np.uint16)
+        return out
+    finally:
+        ss.close()
+
+
+def check_master(got, want, rtol=MASTER_RTOL):
+    got = got.astype(np.float64)
+    want = want.astype(np.float64)
+    denom = np.maximum(np.abs(want), 1e-30)
+    rel = np.abs(got - want) / denom
+    bad = (rel > rtol) & ~(np.isnan(got) & np.isnan(want))
+    assert not bad.any(), f"master: {int(bad.sum())} elements beyond {rtol} (max {rel.max():.3g})"
+    return int((got == want).sum())
+
+
+def check_codes(got, want, name):
+    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert diff.max(initial=0) <= 1, f"{name}: code difference {diff.max()} > 1"
+    frac = float((diff > 0).mean()) if diff.size else 0.0
+    assert frac <= CODE_FRAC, f"{name}: {frac:.3g} of codes differ (> {CODE_FRAC})"
+    return int((diff == 0).sum())
+
+
+def compare(case: Case, g: dict, o: dict, exact: bool = True):
+    """Spec tolerances; with exact=True also every byte equal."""
+    assert g["S"] == o["S"]
+    assert np.array_equal(g["offsets"], o["offsets"])
+    assert np.array_equal(g["packed_grad"].view(np.uint8), o["packed_grad"].view(np.uint8)), \
+        "copy-in differs"
+    assert g["factors"] == o["factors"], (g["factors"], o["factors"])
+    for a, b in zip(g["norms"], o["norms"]):
+        assert abs(a - b) <= 1e-12 * max(abs(b), 1e-300), (a, b)
+    check_master(g["master"], o["master"])
+    if case.quantized:
+        check_codes(g["m_state"], o["m_state"], "m codes")
+        check_codes(g["v_state"], o["v_state"], "v codes")
+    else:
+        check_master(g["m_state"], o["m_state"])
+        check_master(g["v_state"], o["v_state"])
+    if exact:
+        for k in ("master", "m_state", "v_state", "m_scale", "v_scale", "packed_bf16"):
+            assert np.array_equal(g[k].view(np.uint8), o[k].view(np.uint8)), f"{k} not bit-exact"
+    for a, b in zip(g["params"], o["params"]):
+        assert np.array_equal(a, b), "copy-out differs"

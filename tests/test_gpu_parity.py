@@ -1,0 +1,173 @@
+"""GPU parity: every libvsf entry point through the C ABI against the oracle
+on the same seeded inputs (pack, group norm/scale, 8-bit AdamW, unpack).
+Small and ragged cases; the full-size workloads are in test_gpu_fullsize.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from synth import workloads as W
+
+from gpu_harness import Case, case_from_workload, compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _normal_case(specs, m, g, steps, seed=11, **kw):
+    def grads(s, t):
+        n = int(np.prod(specs[t][0]))
+        from synth import DIST_NORMAL, KIND_GRAD, fill_bf16, key
+        return fill_bf16(key(seed, s, t, KIND_GRAD), DIST_NORMAL, 1e-3, 0, np.empty(n, np.uint16))
+
+    def masters(t):
+        n = int(np.prod(specs[t][0]))
+        from synth import DIST_NORMAL, KIND_PARAM, fill_f32, key
+        return fill_f32(key(seed, 0, t, KIND_PARAM), DIST_NORMAL, 0.02, 0, np.empty(n, np.float32))
+
+    return Case(specs=specs, m=m, g_coll=g, steps=steps, grads=grads, masters=masters, **kw)
+
+
+def test_tiny_three_steps_bit_exact():
+    case = case_from_workload(W.tiny())
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_tiny_clip_active():
+    """max_norm 0.01 against a mean-gradient norm near 0.116: c < 1."""
+    case = case_from_workload(W.tiny(), max_norm=0.01)
+    o = run_oracle(case)
+    assert all(f < 0.25 for f in o["factors"])
+    compare(case, run_gpu(case), o)
+
+
+def test_tiny_fp32_grads():
+    case = case_from_workload(W.tiny(), grad_dtype=1)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_tiny_fp32_state():
+    case = case_from_workload(W.tiny(), quantized=False)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_tiny_standalone_norm():
+    case = case_from_workload(W.tiny(), steps=2, standalone_norm=True)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+RAGGED = [
+    ((300, 1000), W.GRAN_ROWS, 32, 0),      # 9 full blocks + a 12-row tail
+    ((45, 77), W.GRAN_TILE, 8, 16),         # ragged right and bottom tiles
+    ((1000,), W.GRAN_ELEM, 0, 0),           # 7 full chunks + one of 104
+    ((1,), W.GRAN_ELEM, 0, 0),              # a one-element tensor
+    ((3, 5), W.GRAN_ROWS, 8, 0),            # atom longer than the tensor
+    ((4, 256, 96), W.GRAN_ROWS, 64, 0),     # 3-D: rows = product of leading dims
+    ((128, 4096), W.GRAN_TILE, 128, 128),   # 32 full 128x128 tiles
+]
+
+
+def test_ragged_mixed_several_steps():
+    case = _normal_case(RAGGED, m=5, g=128, steps=4)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_unaligned_collective_unit_takes_scalar_paths():
+    """g_coll = 3: offsets and blocks are not 16-byte aligned."""
+    case = _normal_case(RAGGED[:5], m=3, g=3, steps=3)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_single_rank_and_many_empty_ranks():
+    one = _normal_case(RAGGED[:3], m=1, g=64, steps=2)
+    compare(one, run_gpu(one), run_oracle(one))
+    many = _normal_case(RAGGED[:2], m=64, g=128, steps=2)
+    compare(many, run_gpu(many), run_oracle(many))
+
+
+def test_all_zero_blocks_keep_zero_codes():
+    specs = [((64, 256), W.GRAN_ROWS, 16, 0), ((512,), W.GRAN_ELEM, 0, 0)]
+    case = _normal_case(specs, m=2, g=128, steps=3)
+    base = case.grads
+    case.grads = lambda s, t: np.zeros_like(base(s, t)) if t == 0 else base(s, t)
+    g, o = run_gpu(case), run_oracle(case)
+    compare(case, g, o)
+    off = int(o["offsets"][0])
+    assert not g["m_state"][off:off + 64 * 256].any()
+    assert not g["v_state"][off:off + 64 * 256].any()
+
+
+def test_large_blocks_use_clusters():
+    """Blocks of 352,256 elements (a 32-row stripe of an 11008-column matrix)."""
+    specs = [((96, 11008), W.GRAN_ROWS, 32, 0), ((256, 4096), W.GRAN_ROWS, 32, 0),
+             ((4096,), W.GRAN_ELEM, 0, 0)]
+    case = _normal_case(specs, m=4, g=128, steps=3)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_heavy_tails_student_t():
+    w = W.dsv3_block()
+    specs = [((512, 1024), W.GRAN_TILE, 128, 128), ((7168,), W.GRAN_ELEM, 0, 0)]
+
+    def grads(s, t):
+        n = int(np.prod(specs[t][0]))
+        from synth import DIST_STUDENT_T3, KIND_GRAD, fill_bf16, key
+        return fill_bf16(key(0, s, t, KIND_GRAD), DIST_STUDENT_T3, 1e-3, 0, np.empty(n, np.uint16))
+
+    case = Case(specs=specs, m=8, g_coll=512, steps=5, grads=grads,
+                masters=lambda t: W.master_init(w, t, 0, int(np.prod(specs[t][0]))))
+    compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_misaligned_pointer_is_an_error_not_a_fault():
+    from fsdp_buffer_layout_gb300 import vsf as V
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    ss = ShardStep([TensorSpec((64, 64), W.GRAN_ROWS, 8)], 2, 128)
+    try:
+        g = torch.zeros(64 * 64 + 8, dtype=torch.int16, device="cuda")
+        with pytest.raises(V.VsfError) as e:
+            V.vsf_pack(ss.plan, [g.data_ptr() + 2], V.VSF_BF16, ss.packed_grad.data_ptr(),
+                       ss.stream.cuda_stream)
+        assert e.value.status == V.VSF_ERR_ALIGN
+        with pytest.raises(V.VsfError) as e:
+            V.vsf_adam8_step(ss.plan, ss.packed_grad.data_ptr() + 4, V.VSF_BF16,
+                             ss.factor.data_ptr(), ss.master.data_ptr(), ss.m_state.data_ptr(),
+                             ss.v_state.data_ptr(), ss.m_scale.data_ptr(), ss.v_scale.data_ptr(),
+                             ss.packed_bf16.data_ptr(), ss.hp, 1, ss.stream.cuda_stream)
+        assert e.value.status == V.VSF_ERR_ALIGN
+        with pytest.raises(V.VsfError) as e:
+            V.vsf_adam8_step(ss.plan, ss.packed_grad.data_ptr(), V.VSF_BF16,
+                             ss.factor.data_ptr(), ss.master.data_ptr(), ss.m_state.data_ptr(),
+                             ss.v_state.data_ptr(), ss.m_scale.data_ptr(), ss.v_scale.data_ptr(),
+                             ss.packed_bf16.data_ptr(), ss.hp, 0, ss.stream.cuda_stream)
+        assert e.value.status == V.VSF_ERR_ARG
+        torch.cuda.synchronize()
+    finally:
+        ss.close()
+
+
+def test_padding_is_never_written():
+    """Canary values in the padding survive a step (no write outside real elements)."""
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    w = W.tiny()
+    specs = [TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
+    ss = ShardStep(specs, w.m, w.g_coll)
+    try:
+        real = torch.zeros(ss.info.total, dtype=torch.bool, device="cuda")
+        for o, n in zip(ss.offsets, ss.numels):
+            real[o:o + n] = True
+        pad = ~real
+        assert int(pad.sum()) > 0
+        for buf in (ss.packed_grad.view(torch.int16), ss.master, ss.m_state, ss.v_state,
+                    ss.packed_bf16.view(torch.int16)):
+            buf[pad] = 77 if buf.dtype != torch.float32 else 77.0
+        grads = [torch.from_numpy(W.grad(w, 1, t).view(np.int16)).cuda() for t in range(4)]
+        params = [torch.empty_like(g) for g in grads]
+        ss.step(grads, params, 1)
+        torch.cuda.synchronize()
+        for buf in (ss.packed_grad.view(torch.int16), ss.master, ss.m_state, ss.v_state,
+                    ss.packed_bf16.view(torch.int16)):
+            assert bool((buf[pad] == 77).all())
+    finally:
+        ss.close()
