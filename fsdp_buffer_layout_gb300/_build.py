@@ -39,8 +39,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-ffp-contract=off",
-              "-I", INCLUDE, "-I", CSRC] + ARCH
+    # -fmad=false: no floating-point multiply-add contraction anywhere in
+    # device code, so every fp32 operation of the update rounds once, in the
+    # order written (explicit __fmaf_rn calls stay fused).
+    common = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler",
+              "-fPIC,-O2,-ffp-contract=off", "-I", INCLUDE, "-I", CSRC] + ARCH
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 

@@ -23,6 +23,7 @@
 // compiler never contracts into an FMA, so each operation rounds once in the
 // order written.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -44,10 +45,6 @@ constexpr int kSmallThreads = 256;
 
 struct TensorPtrs {
   const void* p[kMaxTensors];
-};
-
-struct AdamConsts {
-  float b1, omb1, b2, omb2, eps, decay, step_size, bc2s;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -184,7 +181,8 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
   }
   if (kMode == kUnpack) return;
   __shared__ double red[kCopyThreads / 32];
-  double v = warp_sum((double)acc.hi + (double)acc.lo);
+  // An infinite running sum makes the error term NaN; keep the infinity.
+  double v = warp_sum(isinf(acc.hi) ? (double)acc.hi : (double)acc.hi + (double)acc.lo);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -220,338 +218,7 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __rest
   }
 }
 
-// ------------------------------------------------------------------ AdamW
-
-__device__ __forceinline__ void moments(const AdamConsts& k, float factor, float gin, float dm,
-                                        float dv, int qm, int qv, float& m, float& v) {
-  const float g = __fmul_rn(factor, gin);
-  const float mp = __fmul_rn(__int2float_rn(qm), dm);
-  const float vp = __fmul_rn(__int2float_rn(qv), dv);
-  m = __fadd_rn(__fmul_rn(k.b1, mp), __fmul_rn(k.omb1, g));
-  v = __fadd_rn(__fmul_rn(k.b2, vp), __fmul_rn(k.omb2, __fmul_rn(g, g)));
-}
-
-__device__ __forceinline__ float update_master(const AdamConsts& k, float p, float m, float v) {
-  p = __fmul_rn(p, k.decay);
-  const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), k.bc2s), k.eps);
-  return __fsub_rn(p, __fmul_rn(k.step_size, __fdiv_rn(m, denom)));
-}
-
-__device__ __forceinline__ int quant_m(float m, float inv, bool on) {
-  if (!on) return 0;
-  return __float2int_rn(fminf(fmaxf(__fmul_rn(m, inv), -127.0f), 127.0f));
-}
-__device__ __forceinline__ int quant_v(float v, float inv, bool on) {
-  if (!on) return 0;
-  return __float2int_rn(fminf(fmaxf(__fmul_rn(v, inv), 0.0f), 255.0f));
-}
-
-// Inputs of up to 8 consecutive elements: gradient, m code, v code.
-template <typename GT>
-struct Group {
-  float g[8];
-  int qm[8], qv[8];
-};
-
-template <typename GT>
-__device__ __forceinline__ void load_group(const GT* grad, const int8_t* mq, const uint8_t* vq,
-                                           int64_t e, int cnt, bool vec, Group<GT>& G) {
-  if (vec && cnt == 8) {
-    if constexpr (sizeof(GT) == 2) {
-      const uint4 r = __ldg(reinterpret_cast<const uint4*>(grad + e));
-      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        G.g[2 * i] = bf16_to_f32(w[i] & 0xffffu);
-        G.g[2 * i + 1] = bf16_to_f32(w[i] >> 16);
-      }
-    } else {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(grad + e));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(grad + e) + 1);
-      G.g[0] = a.x; G.g[1] = a.y; G.g[2] = a.z; G.g[3] = a.w;
-      G.g[4] = b.x; G.g[5] = b.y; G.g[6] = b.z; G.g[7] = b.w;
-    }
-    const uint2 cm = __ldg(reinterpret_cast<const uint2*>(mq + e));
-    const uint2 cv = __ldg(reinterpret_cast<const uint2*>(vq + e));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      G.qm[i] = (int)(int8_t)((cm.x >> (8 * i)) & 0xff);
-      G.qm[4 + i] = (int)(int8_t)((cm.y >> (8 * i)) & 0xff);
-      G.qv[i] = (int)((cv.x >> (8 * i)) & 0xff);
-      G.qv[4 + i] = (int)((cv.y >> (8 * i)) & 0xff);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < cnt) {
-        G.g[i] = elem_f32(grad[e + i]);
-        G.qm[i] = mq[e + i];
-        G.qv[i] = vq[e + i];
-      } else {
-        G.g[i] = 0.0f;
-        G.qm[i] = 0;
-        G.qv[i] = 0;
-      }
-    }
-  }
-}
-
-struct BlockCtx {
-  float dm, dv;        // old scales / 127, / 255
-  float im, iv;        // 127 / new m scale, 255 / new v scale
-  bool mon, von;       // new scales non-zero
-};
-
-// Phase 1 on one group: the new moments' maxima.
-template <typename GT>
-__device__ __forceinline__ void group_phase1(const AdamConsts& k, float factor, const BlockCtx& c,
-                                             const GT* grad, const int8_t* mq, const uint8_t* vq,
-                                             int64_t e, int cnt, bool vec, float& mx, float& vx) {
-  Group<GT> G;
-  load_group(grad, mq, vq, e, cnt, vec, G);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < cnt) {
-      float m, v;
-      moments(k, factor, G.g[i], c.dm, c.dv, G.qm[i], G.qv[i], m, v);
-      mx = fmaxf(mx, fabsf(m));
-      vx = fmaxf(vx, v);
-    }
-  }
-}
-
-// Phase 2 on one group: recompute the moments (bit-identical), update the
-// master, requantise with the new scales, write everything.
-template <typename GT>
-__device__ __forceinline__ void group_phase2(const AdamConsts& k, float factor, const BlockCtx& c,
-                                             const GT* grad, int8_t* mq, uint8_t* vq,
-                                             float* master, uint16_t* bf, int64_t e, int cnt,
-                                             bool vec) {
-  Group<GT> G;
-  load_group(grad, mq, vq, e, cnt, vec, G);
-  float p[8];
-  if (vec && cnt == 8) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(master + e));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(master + e) + 1);
-    p[0] = a.x; p[1] = a.y; p[2] = a.z; p[3] = a.w;
-    p[4] = b.x; p[5] = b.y; p[6] = b.z; p[7] = b.w;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) p[i] = i < cnt ? master[e + i] : 0.0f;
-  }
-  uint32_t cm[2] = {0, 0}, cv[2] = {0, 0}, hb[4] = {0, 0, 0, 0};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float m, v;
-    moments(k, factor, G.g[i], c.dm, c.dv, G.qm[i], G.qv[i], m, v);
-    p[i] = update_master(k, p[i], m, v);
-    const uint32_t qm = (uint32_t)(quant_m(m, c.im, c.mon) & 0xff);
-    const uint32_t qv = (uint32_t)quant_v(v, c.iv, c.von);
-    cm[i >> 2] |= qm << (8 * (i & 3));
-    cv[i >> 2] |= qv << (8 * (i & 3));
-    hb[i >> 1] |= f32_to_bf16(p[i]) << (16 * (i & 1));
-  }
-  if (vec && cnt == 8) {
-    __stcs(reinterpret_cast<float4*>(master + e), make_float4(p[0], p[1], p[2], p[3]));
-    __stcs(reinterpret_cast<float4*>(master + e) + 1, make_float4(p[4], p[5], p[6], p[7]));
-    st_stream(bf + e, make_uint4(hb[0], hb[1], hb[2], hb[3]));
-    __stcs(reinterpret_cast<uint2*>(mq + e), make_uint2(cm[0], cm[1]));
-    __stcs(reinterpret_cast<uint2*>(vq + e), make_uint2(cv[0], cv[1]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < cnt) {
-        master[e + i] = p[i];
-        bf[e + i] = (uint16_t)((hb[i >> 1] >> (16 * (i & 1))) & 0xffffu);
-        mq[e + i] = (int8_t)((cm[i >> 2] >> (8 * (i & 3))) & 0xff);
-        vq[e + i] = (uint8_t)((cv[i >> 2] >> (8 * (i & 3))) & 0xff);
-      }
-    }
-  }
-}
-
-// Row / tile blocks: one thread-block cluster per quantisation block. Each
-// CTA of the cluster takes an equal share of the block; phase 1 reads the
-// gradient and the codes (4 B per element for bf16 gradients) and reduces the
-// new absmax; the CTAs exchange their maxima through distributed shared
-// memory and one cluster barrier; phase 2 re-reads the same share (from L2:
-// at most clusters x block bytes are in flight) plus the master and writes
-// master, bf16 copy and codes. HBM sees each byte once.
-template <typename GT>
-__global__ void __launch_bounds__(kAdamThreads) adam_big_kernel(
-    const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist, int nclusters,
-    const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
-    uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int CL = (int)cluster.num_blocks();
-  const int crank = (int)cluster.block_rank();
-  const int cid = blockIdx.x / CL;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kAdamThreads / 32;
-  __shared__ float red[2][2][kWarps];
-  __shared__ float2 slots[2][kMaxCluster];
-  const float factor = *d_factor;
-
-  int par = 0;
-  for (int j = cid; j < nlist; j += nclusters, par ^= 1) {
-    const int q = list[j];
-    const QBlock b = qb[q];
-    BlockCtx c;
-    c.dm = __fdiv_rn(m_scale[q], 127.0f);
-    c.dv = __fdiv_rn(v_scale[q], 255.0f);
-    const bool contiguous = b.nrows == 1;
-    const bool vec = (b.base % 8 == 0) && (contiguous || b.stride % 8 == 0);
-
-    // This CTA's share: vectors [v0, v1) of a contiguous block, or rows
-    // [r0, r1) of a tiled block.
-    int64_t v0 = 0, v1 = 0;
-    int r0 = 0, r1 = 0;
-    const int vpr = (b.ncols + 7) / 8;
-    if (contiguous) {
-      const int64_t nv = vpr;
-      const int64_t per = (nv + CL - 1) / CL;
-      v0 = min64(nv, (int64_t)crank * per);
-      v1 = min64(nv, v0 + per);
-    } else {
-      const int per = (b.nrows + CL - 1) / CL;
-      r0 = min(b.nrows, crank * per);
-      r1 = min(b.nrows, r0 + per);
-    }
-
-    // phase 1
-    float mx = 0.0f, vx = 0.0f;
-    if (contiguous) {
-      for (int64_t v = v0 + tid; v < v1; v += kAdamThreads) {
-        const int64_t off = v * 8;
-        group_phase1<GT>(k, factor, c, grad, mq, vq, b.base + off,
-                         (int)min64(8, b.ncols - off), vec, mx, vx);
-      }
-    } else {
-      for (int r = r0 + warp; r < r1; r += kWarps)
-        for (int v = lane; v < vpr; v += 32)
-          group_phase1<GT>(k, factor, c, grad, mq, vq, b.base + (int64_t)r * b.stride + v * 8,
-                           min(8, b.ncols - v * 8), vec, mx, vx);
-    }
-    mx = warp_max(mx);
-    vx = warp_max(vx);
-    if (lane == 0) {
-      red[par][0][warp] = mx;
-      red[par][1][warp] = vx;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float bm = 0.0f, bv = 0.0f;
-      for (int w = 0; w < kWarps; ++w) {
-        bm = fmaxf(bm, red[par][0][w]);
-        bv = fmaxf(bv, red[par][1][w]);
-      }
-      for (int r = 0; r < CL; ++r) *cluster.map_shared_rank(&slots[par][crank], r) = make_float2(bm, bv);
-    }
-    cluster.sync();
-    float sm = 0.0f, sv = 0.0f;
-    for (int r = 0; r < CL; ++r) {
-      sm = fmaxf(sm, slots[par][r].x);
-      sv = fmaxf(sv, slots[par][r].y);
-    }
-    c.mon = sm > 0.0f;
-    c.von = sv > 0.0f;
-    c.im = c.mon ? __fdiv_rn(127.0f, sm) : 0.0f;
-    c.iv = c.von ? __fdiv_rn(255.0f, sv) : 0.0f;
-    if (crank == 0 && tid == 0) {
-      m_scale[q] = sm;
-      v_scale[q] = sv;
-    }
-
-    // phase 2
-    if (contiguous) {
-      for (int64_t v = v0 + tid; v < v1; v += kAdamThreads) {
-        const int64_t off = v * 8;
-        group_phase2<GT>(k, factor, c, grad, mq, vq, master, bf, b.base + off,
-                         (int)min64(8, b.ncols - off), vec);
-      }
-    } else {
-      for (int r = r0 + warp; r < r1; r += kWarps)
-        for (int v = lane; v < vpr; v += 32)
-          group_phase2<GT>(k, factor, c, grad, mq, vq, master, bf,
-                           b.base + (int64_t)r * b.stride + v * 8, min(8, b.ncols - v * 8), vec);
-    }
-  }
-  cluster.sync();  // no CTA leaves while a peer may still write its slots
-}
-
-// Element-granular chunks (g_coll elements each): one warp per block, two
-// passes over the (L1-resident) chunk.
-template <typename GT>
-__global__ void __launch_bounds__(kSmallThreads) adam_small_kernel(
-    const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist,
-    const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
-    uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k) {
-  const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x * (kSmallThreads / 32) + (threadIdx.x >> 5);
-  if (j >= nlist) return;
-  const int q = list[j];
-  const QBlock b = qb[q];
-  const float factor = *d_factor;
-  BlockCtx c;
-  c.dm = __fdiv_rn(m_scale[q], 127.0f);
-  c.dv = __fdiv_rn(v_scale[q], 255.0f);
-  float mx = 0.0f, vx = 0.0f;
-  for (int i = lane; i < b.ncols; i += 32) {
-    float m, v;
-    moments(k, factor, elem_f32(grad[b.base + i]), c.dm, c.dv, mq[b.base + i], vq[b.base + i],
-            m, v);
-    mx = fmaxf(mx, fabsf(m));
-    vx = fmaxf(vx, v);
-  }
-  const float sm = warp_max(mx), sv = warp_max(vx);
-  c.mon = sm > 0.0f;
-  c.von = sv > 0.0f;
-  c.im = c.mon ? __fdiv_rn(127.0f, sm) : 0.0f;
-  c.iv = c.von ? __fdiv_rn(255.0f, sv) : 0.0f;
-  for (int i = lane; i < b.ncols; i += 32) {
-    const int64_t e = b.base + i;
-    float m, v;
-    moments(k, factor, elem_f32(grad[e]), c.dm, c.dv, mq[e], vq[e], m, v);
-    const float p = update_master(k, master[e], m, v);
-    master[e] = p;
-    bf[e] = (uint16_t)f32_to_bf16(p);
-    mq[e] = (int8_t)quant_m(m, c.im, c.mon);
-    vq[e] = (uint8_t)quant_v(v, c.iv, c.von);
-  }
-  __syncwarp();
-  if (lane == 0) {
-    m_scale[q] = sm;
-    v_scale[q] = sv;
-  }
-}
-
-// fp32 moments (no quantisation): element-wise over the copy spans.
-template <typename GT>
-__global__ void __launch_bounds__(kCopyThreads) adam_fp32_kernel(
-    const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_numel,
-    const CopySpan* __restrict__ spans, const GT* __restrict__ grad,
-    const float* __restrict__ d_factor, float* master, float* m_state, float* v_state,
-    uint16_t* bf, AdamConsts k) {
-  const CopySpan s0 = spans[blockIdx.x];
-  const CopySpan s1 = spans[blockIdx.x + 1];
-  const float factor = *d_factor;
-  for (int t = s0.tensor; t <= s1.tensor; ++t) {
-    const int64_t b = (t == s0.tensor) ? s0.elem : 0;
-    const int64_t e = (t == s1.tensor) ? s1.elem : t_numel[t];
-    const int64_t base = t_off[t];
-    for (int64_t i = b + threadIdx.x; i < e; i += kCopyThreads) {
-      const int64_t x = base + i;
-      const float g = __fmul_rn(factor, elem_f32(grad[x]));
-      const float m = __fadd_rn(__fmul_rn(k.b1, m_state[x]), __fmul_rn(k.omb1, g));
-      const float v = __fadd_rn(__fmul_rn(k.b2, v_state[x]), __fmul_rn(k.omb2, __fmul_rn(g, g)));
-      const float p = update_master(k, master[x], m, v);
-      m_state[x] = m;
-      v_state[x] = v;
-      master[x] = p;
-      bf[x] = (uint16_t)f32_to_bf16(p);
-    }
-  }
-}
+#include "adam8.cuh"
 
 // ------------------------------------------------------------------ host side
 
@@ -578,23 +245,32 @@ const T* ws_ptr(const vsf_plan* plan, size_t off) {
   return reinterpret_cast<const T*>(plan->d_ws + off);
 }
 
+// Step-t constants, each computed in double and rounded once to fp32
+// (beta^t by t repeated multiplications); see adam8.cuh for the update.
 AdamConsts make_consts(const vsf_adam_hparams& hp, int step) {
   double p1 = 1.0, p2 = 1.0;
   for (int i = 0; i < step; ++i) {
     p1 *= hp.beta1;
     p2 *= hp.beta2;
   }
+  const double bc2s = std::sqrt(1.0 - p2);
   AdamConsts k;
   k.b1 = (float)hp.beta1;
   k.omb1 = (float)(1.0 - hp.beta1);
   k.b2 = (float)hp.beta2;
   k.omb2 = (float)(1.0 - hp.beta2);
-  k.eps = (float)hp.eps;
+  k.eps_hat = (float)(hp.eps * bc2s);
   k.decay = (float)(1.0 - hp.lr * hp.weight_decay);
-  k.step_size = (float)(hp.lr / (1.0 - p1));
-  k.bc2s = (float)std::sqrt(1.0 - p2);
+  k.alpha = (float)(hp.lr * bc2s / (1.0 - p1));
   return k;
 }
+
+// Block-kernel variants: wide CTAs for clusters (one CTA per SM), narrower
+// ones when a CTA owns whole blocks (two or more CTAs per SM).
+template <typename GT>
+constexpr auto kBlockKernelCluster = adam_block_kernel<GT, 512, 1, 4, 2>;
+template <typename GT>
+constexpr auto kBlockKernelSolo = adam_block_kernel<GT, 256, 2, 4, 2>;
 
 template <typename T, int kMode>
 vsf_status launch_copy(const vsf_plan* plan, const void* const* tensors, void* packed,
@@ -646,7 +322,7 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
     const int ncl = std::min(plan->adam_clusters, nbig);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncl * CL);
-    cfg.blockDim = dim3(kAdamThreads);
+    cfg.blockDim = dim3(CL > 1 ? 512 : 256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -655,8 +331,8 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, adam_big_kernel<GT>, qb,
-                                       ws_ptr<int32_t>(plan, plan->layout.big), nbig, ncl, g,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, CL > 1 ? kBlockKernelCluster<GT> : kBlockKernelSolo<GT>,
+                                       qb, ws_ptr<int32_t>(plan, plan->layout.big), nbig, ncl, g,
                                        d_factor, master, mq, vq, m_scale, v_scale, bf, k);
     if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (blocks)");
   }
@@ -706,34 +382,36 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     }
   }
 
-  // Cluster size of the block kernel: smallest power of two keeping the
-  // phase-1 bytes in flight (one block per cluster) within ~32 MB of L2.
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, adam_big_kernel<uint16_t>,
-                                                    kAdamThreads, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (occupancy)");
-  occ = std::max(1, occ);
-  int CL = 1;
-  const double budget = 32.0 * 1024 * 1024;
-  while (CL < kMaxCluster &&
-         (double)sms * occ / CL * (double)plan->max_big_elems * 6.0 > budget)
-    CL *= 2;
-  int nclusters = sms * occ / CL;
-  if (CL > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL * 64);
-    cfg.blockDim = dim3(kAdamThreads);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  // Cluster size of the block kernel: the smallest of 1, 2, 4, 8 that keeps
+  // the phase-1 bytes in flight (one block per active cluster, 4 B per
+  // element) within 64 MB of the 126 MB L2, so that phase 2's re-read hits.
+  const double budget = 64.0 * 1024 * 1024;
+  int CL = 0, nclusters = 0;
+  for (int cand = 1; cand <= kMaxCluster; cand *= 2) {
     int active = 0;
-    e = cudaOccupancyMaxActiveClusters(&active, adam_big_kernel<uint16_t>, &cfg);
-    if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (clusters)");
-    if (active > 0) nclusters = active;
+    if (cand == 1) {
+      int occ = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kBlockKernelSolo<uint16_t>, 256, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (occupancy)");
+      active = std::max(1, occ) * sms;
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cand * 64);
+      cfg.blockDim = dim3(512);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cand;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&active, kBlockKernelCluster<uint16_t>, &cfg);
+      if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (clusters)");
+      active = std::max(1, active);
+    }
+    CL = cand;
+    nclusters = active;
+    if ((double)active * (double)plan->max_big_elems * 4.0 <= budget) break;
   }
 
   // Host image of the device tables; it lives in the plan so that the

@@ -193,26 +193,30 @@ std::vector<int> make_order(const std::vector<Tensor>& ts, int policy) {
 // ---------------------------------------------------------------- AdamW
 
 struct AdamConsts {
-  float b1, omb1, b2, omb2, eps, decay, step_size, bc2s;
+  float b1, omb1, b2, omb2, eps_hat, decay, alpha;
 };
 
 // reading: the host-side constants of step t, each computed in double and
-// rounded once to fp32. beta^t is t repeated multiplications.
+// rounded once to fp32; beta^t is t repeated multiplications. The update is
+// the Adam paper's efficient form (Kingma & Ba, "Adam: A Method for
+// Stochastic Optimization", end of section 2): alpha_t = lr sqrt(1-b2^t) /
+// (1-b1^t) and eps_hat = eps sqrt(1-b2^t), which equals the bias-corrected
+// update lr * mhat / (sqrt(vhat) + eps) in exact arithmetic.
 AdamConsts adam_consts(double lr, double beta1, double beta2, double eps, double wd, int t) {
   double p1 = 1.0, p2 = 1.0;
   for (int i = 0; i < t; ++i) {
     p1 *= beta1;
     p2 *= beta2;
   }
+  const double bc2s = std::sqrt(1.0 - p2);
   AdamConsts k;
   k.b1 = (float)beta1;
   k.omb1 = (float)(1.0 - beta1);
   k.b2 = (float)beta2;
   k.omb2 = (float)(1.0 - beta2);
-  k.eps = (float)eps;
+  k.eps_hat = (float)(eps * bc2s);
   k.decay = (float)(1.0 - lr * wd);
-  k.step_size = (float)(lr / (1.0 - p1));
-  k.bc2s = (float)std::sqrt(1.0 - p2);
+  k.alpha = (float)(lr * bc2s / (1.0 - p1));
   return k;
 }
 
@@ -224,14 +228,16 @@ inline void adam_element(const AdamConsts& k, float factor, float g_in, float& m
   m = k.b1 * m + k.omb1 * g;
   v = k.b2 * v + k.omb2 * (g * g);
   p = p * k.decay;
-  const float denom = std::sqrt(v) / k.bc2s + k.eps;
-  p = p - k.step_size * (m / denom);
+  const float denom = std::sqrt(v) + k.eps_hat;
+  p = p - k.alpha * (m / denom);
 }
 
 inline uint16_t bf16_round(float f) {
   uint32_t u;
   std::memcpy(&u, &f, 4);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;  // NaN -> canonical quiet NaN
+  // reading: NaN -> 0x7fff, the canonical NaN of the sm_100-family hardware
+  // bf16 conversion (torch's CPU conversion gives 0x7fc0 instead).
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fff;
   u += 0x7fffu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
@@ -243,17 +249,22 @@ inline float bf16_value(uint16_t h) {
   return f;
 }
 
-// reading (quantiser): symmetric int8 for m, codes in [-127, 127], scale =
-// max |m| of the block; unsigned uint8 for v, codes in [0, 255], scale = max v
-// of the block. Dequantised value = code * (scale / 127) (resp. / 255); code =
-// round-half-even(x * (127 / scale)) clamped; a zero scale means all codes 0.
+// reading (quantiser): symmetric int8 for m with scale = max |m| of the
+// block, unsigned uint8 for v with scale = max v of the block. Dequantised
+// value = code * (scale / 127) (resp. / 255). Code = round-half-even of
+// x * (127 / scale) (resp. 255 / scale), saturated to the code type's range,
+// NaN giving 0; a zero scale means all codes 0. For a finite block scale
+// whose reciprocal is finite, |x * (127 / scale)| stays below 127.5, so m
+// codes lie in [-127, 127].
 inline int8_t quant_m(float x, float inv) {
-  float y = std::fmin(std::fmax(x * inv, -127.0f), 127.0f);
-  return (int8_t)(int)std::nearbyint(y);
+  const float y = x * inv;
+  if (std::isnan(y)) return 0;
+  return (int8_t)(int)std::nearbyint(std::fmin(std::fmax(y, -128.0f), 127.0f));
 }
 inline uint8_t quant_v(float x, float inv) {
-  float y = std::fmin(std::fmax(x * inv, 0.0f), 255.0f);
-  return (uint8_t)(int)std::nearbyint(y);
+  const float y = x * inv;
+  if (std::isnan(y)) return 0;
+  return (uint8_t)(int)std::nearbyint(std::fmin(std::fmax(y, 0.0f), 255.0f));
 }
 
 }  // namespace

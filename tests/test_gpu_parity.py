@@ -171,3 +171,39 @@ def test_padding_is_never_written():
             assert bool((buf[pad] == 77).all())
     finally:
         ss.close()
+
+
+def test_special_values_match_oracle():
+    """NaN, +-inf, values that overflow bf16, fp32 and bf16 denormals, bf16
+    rounding ties and -0 in masters and gradients: same bits as the oracle
+    (NaN payloads aside), including bf16 NaN = 0x7fff and NaN codes = 0."""
+    specs = [((64, 64), W.GRAN_ROWS, 16, 0), ((256,), W.GRAN_ELEM, 0, 0)]
+    case = _normal_case(specs, m=2, g=128, steps=2)
+    base_g, base_m = case.grads, case.masters
+    f32 = lambda x: np.array([x], np.float32)[0]  # noqa: E731
+    specials_m = [np.nan, np.inf, -np.inf, 3.4e38, -3.3e38, 1e-40, -1e-45,
+                  f32(1 + 2 ** -8), f32(1 + 3 * 2 ** -8), -0.0, 0.0]
+
+    def masters(t):
+        x = base_m(t).copy()
+        if t == 0:
+            x[:len(specials_m)] = specials_m        # block 0 of tensor 0
+            x[1024 + 5] = f32(-(1 + 2 ** -8))       # a tie in block 1
+        else:
+            x[3] = np.nan
+        return x
+
+    def grads(s, t):
+        x = base_g(s, t).copy()
+        if t == 0:
+            x[2048 + 1] = 0x7FC0                    # NaN in block 2
+            x[3072 + 2] = 0x7F80                    # +inf in block 3
+            x[1024 + 9] = 0x0001                    # bf16 denormal
+            x[1024 + 10] = 0x8000                   # -0
+            x[1024 + 11] = 0x7F7F                   # largest finite bf16
+        else:
+            x[200] = 0x0001
+        return x
+
+    case.masters, case.grads = masters, grads
+    compare(case, run_gpu(case), run_oracle(case))
