@@ -28,6 +28,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "vsf_internal.h"
@@ -524,3 +525,145 @@ vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* c
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ group norm without allocation
+//
+// For callers that cannot allocate device memory at the point where they need
+// the gradient norm: a hook that runs inside a framework's caching allocator
+// (its out-of-memory or reclaim path, where asking for memory would recurse
+// into the allocator), a runtime that owns the whole device memory budget and
+// forbids raw cudaMalloc, or latency-critical code that cannot afford the
+// device synchronisation cudaMalloc and cudaFree may imply. Everything the
+// computation needs beyond its inputs and outputs lives in the file-scope
+// array below, which every device that loads the library holds until the
+// process exits.
+
+namespace vsf {
+namespace {
+
+constexpr int kStaticPartials = 1024;     // at most this many CTAs, one partial each
+constexpr int kStaticMaxTensors = 1024;   // tensors per call (kernel parameter space)
+
+// Per-CTA partial sums of squares of the allocation-free norm. 8 KB.
+static __device__ __align__(256) double g_static_partials[kStaticPartials];
+
+struct StaticNormArgs {
+  const void* p[kStaticMaxTensors];
+  int64_t prefix[kStaticMaxTensors + 1];  // prefix[t] = elements before tensor t
+  int32_t n;
+};
+
+// CTA c sums g^2 over elements [c*N/G, (c+1)*N/G) of the concatenated tensors
+// (cut on 8-element multiples), like the copy kernel's norm pass, and writes
+// its partial to partials[c]. Every slot in [0, gridDim.x) is written.
+template <typename T>
+__global__ void __launch_bounds__(kCopyThreads) sumsq_static_kernel(StaticNormArgs a,
+                                                                    double* partials) {
+  constexpr int V = 16 / sizeof(T);
+  const int64_t N = a.prefix[a.n];
+  const int64_t G = gridDim.x;
+  const int64_t lo = (N / G * blockIdx.x) / 8 * 8;
+  const int64_t hi = blockIdx.x + 1 == G ? N : (N / G * (blockIdx.x + 1)) / 8 * 8;
+  DF acc;
+  // first tensor with prefix[t + 1] > lo
+  int t0 = 0, t1 = a.n;
+  while (t0 < t1) {
+    const int mid = (t0 + t1) / 2;
+    if (a.prefix[mid + 1] <= lo) t0 = mid + 1; else t1 = mid;
+  }
+  for (int t = t0; t < a.n && a.prefix[t] < hi; ++t) {
+    const int64_t b = max(lo, a.prefix[t]) - a.prefix[t];
+    const int64_t e = min(hi, a.prefix[t + 1]) - a.prefix[t];
+    const T* src = static_cast<const T*>(a.p[t]);
+    int64_t i = b;
+    if (((reinterpret_cast<uintptr_t>(src + b)) & 15) == 0) {
+      const int64_t nvec = (e - b) / V;
+      const uint4* s = reinterpret_cast<const uint4*>(src + b);
+      for (int64_t k = threadIdx.x; k < nvec; k += kCopyThreads) sq_vec<T>(acc, ld_stream(s + k));
+      i = b + nvec * V;
+    }
+    for (int64_t j = i + threadIdx.x; j < e; j += kCopyThreads) acc_sq(acc, elem_f32(src[j]));
+  }
+  __shared__ double red[kCopyThreads / 32];
+  double v = warp_sum(isinf(acc.hi) ? (double)acc.hi : (double)acc.hi + (double)acc.lo);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int w = 0; w < kCopyThreads / 32; ++w) s += red[w];
+    partials[blockIdx.x] = s;
+  }
+}
+
+std::mutex g_static_mu;
+double* g_static_ptr[256] = {};  // device address of g_static_partials, per device
+
+// Looks the array's device address up once per device (with that device
+// current); host code cannot use the symbol itself as a device pointer.
+vsf_status static_partials(int dev, double** out) {
+  if (dev < 0 || dev >= 256) return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: device id");
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_partials);
+    if (e != cudaSuccess) return cuda_fail(e, "vsf_group_norm_scale_static (symbol address)");
+    g_static_ptr[dev] = static_cast<double*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return VSF_OK;
+}
+
+}  // namespace
+}  // namespace vsf
+
+extern "C" vsf_status vsf_group_norm_scale_static(const void* const* grads, const int64_t* numel,
+                                                  int32_t n, int32_t dtype,
+                                                  const vsf_adam_hparams* hp, float* d_factor,
+                                                  double* d_norm, void* stream) {
+  using namespace vsf;
+  if (grads == nullptr || numel == nullptr || hp == nullptr || d_factor == nullptr)
+    return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: NULL argument");
+  if (n < 1 || n > kStaticMaxTensors)
+    return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: n must be 1..1024 tensors, got " +
+                                 std::to_string(n));
+  if (hp->world < 1) return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: world must be >= 1");
+  if (dtype != VSF_BF16 && dtype != VSF_FP32)
+    return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: dtype must be VSF_BF16 or VSF_FP32");
+  StaticNormArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.n = n;
+  a.prefix[0] = 0;
+  for (int t = 0; t < n; ++t) {
+    if (grads[t] == nullptr || numel[t] < 1)
+      return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: tensor " + std::to_string(t) +
+                                   " is NULL or empty");
+    if (misaligned(grads[t]))
+      return fail(VSF_ERR_ALIGN, "vsf_group_norm_scale_static: tensor " + std::to_string(t) +
+                                     " not 16-byte aligned");
+    if (a.prefix[t] > INT64_MAX / 2 - numel[t])
+      return fail(VSF_ERR_OVERFLOW, "vsf_group_norm_scale_static: too many elements");
+    a.p[t] = grads[t];
+    a.prefix[t + 1] = a.prefix[t] + numel[t];
+  }
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "vsf_group_norm_scale_static");
+  double* partials = nullptr;
+  vsf_status s = static_partials(dev, &partials);
+  if (s != VSF_OK) return s;
+  const int grid = std::max(1, std::min(kStaticPartials, sms * 4));
+  if (grid > kStaticPartials)  // the array bounds the grid, never the reverse
+    return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: grid exceeds the static scratch");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == VSF_BF16)
+    sumsq_static_kernel<uint16_t><<<grid, kCopyThreads, 0, st>>>(a, partials);
+  else
+    sumsq_static_kernel<float><<<grid, kCopyThreads, 0, st>>>(a, partials);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "vsf_group_norm_scale_static (sum of squares)");
+  norm_finalize_kernel<<<1, 256, 0, st>>>(partials, grid, hp->world, hp->max_norm, d_factor,
+                                          d_norm);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_group_norm_scale_static (finalize)");
+}

@@ -194,6 +194,33 @@ vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t
 vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* const* params,
                       void* stream);
 
+/* Group norm and scale WITHOUT any device allocation or workspace. The pages
+ * have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory where they need the gradient norm, such as a hook
+ * running inside a framework's caching allocator (its out-of-memory or
+ * reclaim path, where asking for memory would recurse into the allocator), a
+ * runtime that owns the whole device memory budget and forbids raw
+ * cudaMalloc, or latency-critical code that cannot pay for the device
+ * synchronisation cudaMalloc / cudaFree may imply.
+ *   grads: HOST array of n device pointers (16-byte aligned) to the gradient
+ *   tensors, element type dtype (VSF_BF16 or VSF_FP32); numel: HOST array of
+ *   their element counts (each >= 1); 1 <= n <= 1024 (VSF_ERR_ARG beyond).
+ *   Computes what vsf_group_norm_scale computes (sum of g^2 over every
+ *   element, norm = sqrt(sum) / world, clip factor, *d_factor = fp32(c /
+ *   world), *d_norm = norm; d_norm may be NULL) on `stream`.
+ * Scratch: a fixed 8 KB array of per-CTA partial sums (at most 1024 CTAs)
+ * that the library declares at file scope in device memory; every device
+ * that loads the library keeps it until the process exits. No cudaMalloc,
+ * cudaFree or allocating library call is made. The first call on a device
+ * looks up the array's device address for that device (with that device
+ * current) and caches it; make that first call before any stream capture.
+ * Every call on a device shares the array: calls that overlap on the GPU
+ * (different streams without ordering) race and give wrong results. Nothing
+ * needs to start at zero: each call writes every partial it later reads. */
+vsf_status vsf_group_norm_scale_static(const void* const* grads, const int64_t* numel, int32_t n,
+                                       int32_t dtype, const vsf_adam_hparams* hp, float* d_factor,
+                                       double* d_norm, void* stream);
+
 const char* vsf_status_string(vsf_status s);
 const char* vsf_last_error(void);
 
