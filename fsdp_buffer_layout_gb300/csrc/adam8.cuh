@@ -76,6 +76,17 @@ __device__ __forceinline__ void st_v2(void* ptr, uint2 v, uint64_t pol) {
                : "memory");
 }
 
+// Bulk prefetch of [begin, end) into L2 (one instruction per range, no
+// registers held). The range is shrunk to whole 16-byte units inside it, as
+// the bulk copy engine requires, so no byte outside [begin, end) is touched.
+__device__ __forceinline__ void prefetch_l2(const void* begin, const void* end) {
+  const uintptr_t b = (reinterpret_cast<uintptr_t>(begin) + 15) & ~uintptr_t(15);
+  const uintptr_t e = reinterpret_cast<uintptr_t>(end) & ~uintptr_t(15);
+  if (e <= b) return;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b), "r"((uint32_t)(e - b))
+               : "memory");
+}
+
 // ---------------------------------------------------------------- element math
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
@@ -283,9 +294,10 @@ struct Share {
   int64_t base;    // buffer element of the block's first element
   int64_t first;   // first group (contiguous) or first row (tiled)
   int ngroups;     // groups in this share
-  int vpr_log2;    // tiled: log2(groups per row), or -1 for contiguous
+  int vpr_log2;    // tiled: log2(groups per row); -1 contiguous; -2 other rows
   int stride;      // tiled: elements between rows
   int ncols;       // contiguous: block length; tiled: row length
+  bool vec;        // 16-byte vector path allowed
   __device__ __forceinline__ void locate(int i, int64_t& e, int& cnt) const {
     if (vpr_log2 < 0) {
       const int64_t off = (first + i) * 8;
@@ -297,7 +309,58 @@ struct Share {
       cnt = min(8, ncols - v * 8);
     }
   }
+  // L2 prefetch of groups [g0, g1) of this share for the arrays given
+  // (element size in bytes; null arrays skipped): thread 0 issues one bulk
+  // prefetch per array. Only contiguous shares are prefetched; a tile's rows
+  // would need one prefetch each, which costs more than it hides.
+  __device__ __forceinline__ void prefetch(int g0, int g1, const void* a, int ea, const void* b,
+                                           int eb, const void* c, int ec, int tid,
+                                           int /*nthreads*/) const {
+    g1 = min(g1, ngroups);
+    if (g0 >= g1) return;
+    auto one = [&](int64_t e0, int64_t e1) {
+      if (a) prefetch_l2((const char*)a + e0 * ea, (const char*)a + e1 * ea);
+      if (b) prefetch_l2((const char*)b + e0 * eb, (const char*)b + e1 * eb);
+      if (c) prefetch_l2((const char*)c + e0 * ec, (const char*)c + e1 * ec);
+    };
+    if (vpr_log2 == -1) {
+      if (tid == 0)
+        one(base + (first + g0) * 8, base + min64((first + g1) * 8, (int64_t)ncols));
+    }
+  }
 };
+
+// The share of CTA `crank` of a CL-CTA cluster in block b.
+__device__ __forceinline__ Share make_share(const QBlock& b, int CL, int crank) {
+  Share sh;
+  sh.base = b.base;
+  sh.ncols = b.ncols;
+  sh.stride = b.stride;
+  const int vpr = (b.ncols + 7) >> 3;
+  sh.vec = (b.base & 7) == 0;
+  if (b.nrows == 1) {
+    const int per = (vpr + CL - 1) / CL;
+    const int g0 = min(vpr, crank * per);
+    sh.first = g0;
+    sh.ngroups = min(vpr, g0 + per) - g0;
+    sh.vpr_log2 = -1;
+  } else {
+    const int per = (b.nrows + CL - 1) / CL;
+    const int r0 = min(b.nrows, crank * per);
+    const int nr = min(b.nrows, r0 + per) - r0;
+    sh.first = r0;
+    sh.vec = sh.vec && (b.stride & 7) == 0;
+    const int lg = 31 - __clz(vpr);
+    if ((1 << lg) == vpr) {
+      sh.vpr_log2 = lg;
+      sh.ngroups = nr * vpr;
+    } else {
+      sh.vpr_log2 = -2;  // rows whose group count is not a power of two: row by row
+      sh.ngroups = nr;
+    }
+  }
+  return sh;
+}
 
 // Row / tile blocks, one cluster per block. kThreads threads per CTA; phase 1
 // keeps kU1 groups of loads in flight per thread, phase 2 kU2.
@@ -334,38 +397,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) adam_block_kernel(
     c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
     c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
 
-    Share sh;
-    sh.base = b.base;
-    sh.ncols = b.ncols;
-    sh.stride = b.stride;
+    const Share sh = make_share(b, CL, crank);
+    const bool vec = sh.vec;
     const int vpr = (b.ncols + 7) >> 3;
-    bool vec = (b.base & 7) == 0;
-    if (b.nrows == 1) {
-      const int per = (vpr + CL - 1) / CL;
-      const int g0 = min(vpr, crank * per);
-      sh.first = g0;
-      sh.ngroups = min(vpr, g0 + per) - g0;
-      sh.vpr_log2 = -1;
-    } else {
-      const int per = (b.nrows + CL - 1) / CL;
-      const int r0 = min(b.nrows, crank * per);
-      const int nr = min(b.nrows, r0 + per) - r0;
-      sh.first = r0;
-      vec = vec && (b.stride & 7) == 0;
-      const int lg = 31 - __clz(vpr);
-      if ((1 << lg) == vpr) {
-        sh.vpr_log2 = lg;
-        sh.ngroups = nr * vpr;
-      } else {
-        sh.vpr_log2 = -2;  // non power-of-two rows: handled row by row below
-        sh.ngroups = nr;
-      }
-    }
+    constexpr int kStep1 = kThreads * kU1, kStep2 = kThreads * kU2;
+    if (j == cid) sh.prefetch(0, 2 * kStep1, grad, sizeof(GT), mq, 1, vq, 1, tid, kThreads);
 
     // ---- phase 1
     float mx = 0.0f, vx = 0.0f;
     if (sh.vpr_log2 >= -1) {
-      for (int i0 = tid; i0 < sh.ngroups; i0 += kThreads * kU1) {
+      for (int i0 = tid; i0 < sh.ngroups; i0 += kStep1) {
+        const int it0 = i0 - tid;
+        sh.prefetch(it0 + 2 * kStep1, it0 + 3 * kStep1, grad, sizeof(GT), mq, 1, vq, 1, tid,
+                    kThreads);
         Raw r[kU1];
         bool full[kU1];
         int64_t e[kU1];
@@ -397,6 +441,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) adam_block_kernel(
       }
     }
 
+    // master of the first phase-2 iterations, fetched across the barrier
+    sh.prefetch(0, 2 * kStep2, master, 4, nullptr, 0, nullptr, 0, tid, kThreads);
+
     // ---- block maxima: warp, CTA, then cluster through distributed smem
     mx = warp_max(mx);
     vx = warp_max(vx);
@@ -427,9 +474,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) adam_block_kernel(
       v_scale[q] = sv;
     }
 
-    // ---- phase 2
+    // ---- phase 2 (and the next block's first phase-1 data)
+    if (j + nclusters < nlist) {
+      const Share nx = make_share(qb[list[j + nclusters]], CL, crank);
+      nx.prefetch(0, 2 * kStep1, grad, sizeof(GT), mq, 1, vq, 1, tid, kThreads);
+    }
     if (sh.vpr_log2 >= -1) {
-      for (int i0 = tid; i0 < sh.ngroups; i0 += kThreads * kU2) {
+      for (int i0 = tid; i0 < sh.ngroups; i0 += kStep2) {
+        const int it0 = i0 - tid;
+        sh.prefetch(it0 + 2 * kStep2, it0 + 3 * kStep2, master, 4, nullptr, 0, nullptr, 0, tid,
+                    kThreads);
         Raw r[kU2];
         uint4 pa[kU2], pb[kU2];
         bool full[kU2];
@@ -474,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) adam_block_kernel(
       }
     }
   }
+  __syncwarp();
   cluster.sync();  // no CTA leaves while a peer may still write its slots
 }
 

@@ -1,0 +1,300 @@
+// adam8_tma.cuh — the 8-bit AdamW block kernel for contiguous blocks, with a
+// TMA (bulk-copy) pipeline. Included by vsf_kernels.cu after adam8.cuh (same
+// element math, same results bit for bit).
+//
+// Structure of one CTA: warp 0..kConsumerWarps-1 compute, the last warp is
+// the producer. The producer streams fixed-size chunks of the CTA's share of
+// each block from global memory into a ring of shared-memory slots with
+// cp.async.bulk (the Blackwell bulk-copy engine), each slot guarded by a
+// "full" mbarrier (transaction bytes) and an "empty" mbarrier (one arrival per
+// consumer warp). Per block the sequence is: every phase-1 chunk (gradient and
+// codes, kept in L2 with an evict-last hint), then every phase-2 chunk
+// (gradient and codes again, now L2 hits, plus the master). The producer runs
+// ahead across phases and blocks as far as the ring allows, so HBM requests
+// keep flowing while the consumers wait for the block maxima.
+//
+// Block maxima: after phase 1 each CTA's consumers reduce their maxima; one
+// thread writes the CTA's pair into a slot of every CTA of the cluster
+// (distributed shared memory) and arrives remotely on that CTA's mbarrier
+// (release at cluster scope); consumers wait on their own barrier (acquire).
+// Slots and barriers alternate between two sets by block parity.
+//
+// Every wait is bounded: after kWaitLimit polls it sets bit 1 of the device
+// error word and carries on as if the wait had succeeded (the results are
+// then wrong but every CTA still finishes, so no thread hangs and no CTA
+// leaves while a copy or a peer's write into it is still pending).
+
+constexpr int kTmaChunk = 4096;           // elements per chunk
+constexpr int kConsumerWarps = 16;        // 512 consumer threads: one 8-element group each
+constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+template <typename GT>
+struct TmaLayout {
+  // ring depth: as many 32 KB (bf16) or 40 KB (fp32) slots as fit in 200 KB
+  static constexpr int slots = sizeof(GT) == 2 ? 6 : 5;
+  static constexpr uint32_t grad = 0;
+  static constexpr uint32_t mq = kTmaChunk * sizeof(GT);
+  static constexpr uint32_t vq = mq + kTmaChunk;
+  static constexpr uint32_t master = vq + kTmaChunk;
+  static constexpr uint32_t slot = master + kTmaChunk * 4;  // bytes per slot
+  static constexpr uint32_t ring = slot * slots;
+  // then: full[slots], empty[slots], maxbar[2] (8 B each), maxima[2][8] (float2)
+  static constexpr uint32_t bars = ring;
+  static constexpr uint32_t maxima = bars + 8 * (2 * slots + 2);
+  static constexpr uint32_t total = maxima + 2 * kMaxCluster * 8;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Bounded wait for the phase of the given parity; returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  atomicOr(err, 2u);
+  return false;
+}
+
+// The same at cluster scope (acquire), for barriers that peers arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  atomicOr(err, 2u);
+  return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// global -> shared bulk copy completing on `bar`, with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// Remote (cluster) store of a float2 and arrive on the peer's barrier.
+__device__ __forceinline__ void dsmem_put_arrive(uint32_t local_slot, uint32_t local_bar,
+                                                 uint32_t rank, float2 v) {
+  uint32_t rs, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(local_slot), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(rs), "f"(v.x), "f"(v.y)
+               : "memory");
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb)
+               : "memory");
+}
+
+// Chunks [c0, c1) of block b that CTA `crank` of CL owns.
+__device__ __forceinline__ void tma_share(const QBlock& b, int CL, int crank, int& c0, int& c1) {
+  const int nch = (b.ncols + kTmaChunk - 1) / kTmaChunk;
+  const int per = (nch + CL - 1) / CL;
+  c0 = min(nch, crank * per);
+  c1 = min(nch, c0 + per);
+}
+
+template <typename GT>
+__global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
+    const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist, int nclusters,
+    const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
+    uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k, unsigned* err) {
+  using Lay = TmaLayout<GT>;
+  constexpr int kTmaSlots = Lay::slots;
+  extern __shared__ __align__(128) unsigned char smem[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = (int)cluster.num_blocks();
+  const int crank = (int)cluster.block_rank();
+  const int cid = blockIdx.x / CL;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t s0 = smem_u32(smem);
+  auto full_bar = [&](int s) { return s0 + Lay::bars + 8u * s; };
+  auto empty_bar = [&](int s) { return s0 + Lay::bars + 8u * (kTmaSlots + s); };
+  auto max_bar = [&](int par) { return s0 + Lay::bars + 8u * (2 * kTmaSlots + par); };
+  float2* maxima = reinterpret_cast<float2*>(smem + Lay::maxima);
+
+  if (tid == 0) {
+    for (int s = 0; s < kTmaSlots; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kConsumerWarps);
+    }
+    mbar_init(max_bar(0), CL);
+    mbar_init(max_bar(1), CL);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  cluster.sync();
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: one lane issues every copy
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t drop = l2_policy_evict_first();
+      uint32_t p = 0;  // position in the ring sequence
+      for (int j = cid; j < nlist; j += nclusters) {
+        const QBlock b = qb[list[j]];
+        int c0, c1;
+        tma_share(b, CL, crank, c0, c1);
+        for (int ph = 0; ph < 2; ++ph) {
+          for (int c = c0; c < c1; ++c, ++p) {
+            const int s = p % kTmaSlots;
+            const uint32_t round = p / kTmaSlots;
+            if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
+            const int64_t e = b.base + (int64_t)c * kTmaChunk;
+            const uint32_t len = (uint32_t)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)c * kTmaChunk);
+            const uint32_t slot = s0 + s * Lay::slot;
+            const uint64_t pol = ph == 0 ? keep : drop;
+            const uint32_t bytes = len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u);
+            mbar_expect_tx(full_bar(s), bytes);
+            bulk_g2s(slot + Lay::grad, grad + e, len * sizeof(GT), full_bar(s), pol);
+            bulk_g2s(slot + Lay::mq, mq + e, len, full_bar(s), pol);
+            bulk_g2s(slot + Lay::vq, vq + e, len, full_bar(s), pol);
+            if (ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, full_bar(s), drop);
+          }
+        }
+      }
+      // Every issued copy has been consumed before the consumers finish; wait
+      // for the last ones anyway so that none is in flight at exit.
+      for (int s = 0; s < kTmaSlots; ++s) {
+        if (p > (uint32_t)s) {
+          const uint32_t last = (p - 1 - s) / kTmaSlots * kTmaSlots + s;  // last position in slot s
+          mbar_wait(full_bar(s), (last / kTmaSlots) & 1, err);
+        }
+      }
+    }
+  } else {
+    // ---------------- consumers: thread `tid` owns group `tid` of each chunk
+    Consts2 c;
+    c.b1 = f2(k.b1);
+    c.omb1 = f2(k.omb1);
+    c.b2 = f2(k.b2);
+    c.omb2 = f2(k.omb2);
+    c.eps_hat = f2(k.eps_hat);
+    c.decay = f2(k.decay);
+    c.alpha = f2(k.alpha);
+    c.factor = f2(*d_factor);
+    const uint64_t drop = l2_policy_evict_first();
+    __shared__ float red[2][2][kConsumerWarps];
+    uint32_t p = 0;
+    int nb = 0;  // blocks done by this CTA
+    for (int j = cid; j < nlist; j += nclusters, ++nb) {
+      const int q = list[j];
+      const QBlock b = qb[q];
+      c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
+      c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
+      int c0, c1;
+      tma_share(b, CL, crank, c0, c1);
+      const int par = nb & 1;
+
+      // phase 1: maxima of the new moments
+      float mx = 0.0f, vx = 0.0f;
+      for (int ch = c0; ch < c1; ++ch, ++p) {
+        const int s = p % kTmaSlots;
+        mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
+        const int len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)ch * kTmaChunk);
+        if (tid * 8 < len) {
+          const unsigned char* sl = smem + s * Lay::slot;
+          Raw r;
+          r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 8 * sizeof(GT));
+          if constexpr (sizeof(GT) == 4)
+            r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 32 + 16);
+          r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + tid * 8);
+          r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + tid * 8);
+          phase1_group<GT>(c, r, mx, vx);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+      }
+      mx = warp_max(mx);
+      vx = warp_max(vx);
+      if (lane == 0) {
+        red[par][0][warp] = mx;
+        red[par][1][warp] = vx;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+      if (tid == 0) {
+        float bm = 0.0f, bv = 0.0f;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          bm = fmaxf(bm, red[par][0][w]);
+          bv = fmaxf(bv, red[par][1][w]);
+        }
+        for (int rk = 0; rk < CL; ++rk)
+          dsmem_put_arrive(smem_u32(&maxima[par * kMaxCluster + crank]), max_bar(par), rk,
+                           make_float2(bm, bv));
+      }
+      mbar_wait_cluster(max_bar(par), (nb >> 1) & 1, err);
+      float sm = 0.0f, sv = 0.0f;
+      for (int rk = 0; rk < CL; ++rk) {
+        const float2 v = maxima[par * kMaxCluster + rk];
+        sm = fmaxf(sm, v.x);
+        sv = fmaxf(sv, v.y);
+      }
+      c.im = f2(sm > 0.0f ? __fdiv_rn(127.0f, sm) : 0.0f);
+      c.iv = f2(sv > 0.0f ? __fdiv_rn(255.0f, sv) : 0.0f);
+      if (crank == 0 && tid == 0) {
+        m_scale[q] = sm;
+        v_scale[q] = sv;
+      }
+
+      // phase 2: update, requantise, write
+      for (int ch = c0; ch < c1; ++ch, ++p) {
+        const int s = p % kTmaSlots;
+        mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
+        const int len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)ch * kTmaChunk);
+        if (tid * 8 < len) {
+          const unsigned char* sl = smem + s * Lay::slot;
+          Raw r;
+          r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 8 * sizeof(GT));
+          if constexpr (sizeof(GT) == 4)
+            r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 32 + 16);
+          r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + tid * 8);
+          r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + tid * 8);
+          const uint4 pa = *reinterpret_cast<const uint4*>(sl + Lay::master + tid * 32);
+          const uint4 pb = *reinterpret_cast<const uint4*>(sl + Lay::master + tid * 32 + 16);
+          uint4 o0, o1, ob;
+          uint2 ocm, ocv;
+          phase2_group<GT>(c, r, pa, pb, o0, o1, ob, ocm, ocv);
+          const int64_t e = b.base + (int64_t)ch * kTmaChunk + tid * 8;
+          st_v4(master + e, o0, drop);
+          st_v4(master + e + 4, o1, drop);
+          st_v4(bf + e, ob, drop);
+          st_v2(mq + e, ocm, drop);
+          st_v2(vq + e, ocv, drop);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+      }
+    }
+  }
+  __syncwarp();     // the producer warp diverged (lane 0 issued the copies)
+  cluster.sync();  // no CTA leaves while a peer may still write into it
+}

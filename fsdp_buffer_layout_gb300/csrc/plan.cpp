@@ -215,8 +215,19 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
       b.ncols = (int32_t)nc;
       b.stride = (int32_t)st;
       b.tensor = t;
-      (small ? plan->small_blocks : plan->big_blocks).push_back((int32_t)plan->qblocks.size());
-      if (!small) plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
+      // Contiguous blocks that start on 16 elements and hold a multiple of 16
+      // go to the bulk-copy (TMA) kernel; the other row and tile blocks to the
+      // register kernel; element chunks to the warp kernel.
+      const bool tma = !small && nr == 1 && base % 16 == 0 && nc % 16 == 0;
+      if (small) {
+        plan->small_blocks.push_back((int32_t)plan->qblocks.size());
+      } else if (tma) {
+        plan->tma_blocks.push_back((int32_t)plan->qblocks.size());
+        plan->max_tma_elems = std::max(plan->max_tma_elems, nr * nc);
+      } else {
+        plan->big_blocks.push_back((int32_t)plan->qblocks.size());
+        plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
+      }
       plan->qblocks.push_back(b);
     };
     if (x.gran == VSF_GRAN_ELEM) {
@@ -266,6 +277,8 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
   L.qblocks = section(sizeof(vsf::QBlock) * plan->qblocks.size());
   L.big = section(sizeof(int32_t) * std::max<size_t>(1, plan->big_blocks.size()));
   L.small = section(sizeof(int32_t) * std::max<size_t>(1, plan->small_blocks.size()));
+  L.tma = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_blocks.size()));
+  L.error = section(16);
   L.spans = section(sizeof(vsf::CopySpan) * (vsf::kMaxCopyGrid + 1));
   L.partials = section(sizeof(double) * vsf::kMaxCopyGrid);
   L.bytes = (cur + 255) / 256 * 256;
@@ -343,6 +356,12 @@ vsf_status vsf_plan_rank_slices(const vsf_plan* plan, int32_t rank, int32_t capa
     ++k;
   }
   *count = k;
+  return VSF_OK;
+}
+
+vsf_status vsf_plan_device_error_offset(const vsf_plan* plan, size_t* offset) {
+  if (plan == nullptr || offset == nullptr) return fail(VSF_ERR_ARG, "NULL argument");
+  *offset = plan->layout.error;
   return VSF_OK;
 }
 

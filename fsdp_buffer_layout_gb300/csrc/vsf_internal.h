@@ -48,7 +48,8 @@ struct TensorInfo {
 struct DeviceLayout {
   size_t tensor_off = 0, tensor_numel = 0;  // int64[n] each
   size_t qblocks = 0;                       // QBlock[n_qblocks]
-  size_t big = 0, small = 0;                // int32 lists of block indices
+  size_t big = 0, small = 0, tma = 0;       // int32 lists of block indices
+  size_t error = 0;                         // uint32 device error word
   size_t spans = 0;                         // CopySpan[kMaxCopyGrid + 1]
   size_t partials = 0;                      // double[kMaxCopyGrid]
   size_t bytes = 0;
@@ -63,9 +64,11 @@ struct vsf_plan {
   double plan_seconds = 0.0;
   std::vector<vsf::TensorInfo> tensors;
   std::vector<vsf::QBlock> qblocks;
-  std::vector<int32_t> big_blocks;    // ROWS / TILE blocks: cluster kernel
+  std::vector<int32_t> big_blocks;    // ROWS / TILE blocks: register block kernel
+  std::vector<int32_t> tma_blocks;    // contiguous, 16-aligned blocks: TMA kernel
   std::vector<int32_t> small_blocks;  // ELEM chunks: warp kernel
   int64_t max_big_elems = 0;
+  int64_t max_tma_elems = 0;
   vsf::DeviceLayout layout;
 
   // Set by vsf_plan_upload.
@@ -76,6 +79,8 @@ struct vsf_plan {
   int copy_grid = 0;
   int adam_cluster = 1;
   int adam_clusters = 0;
+  int tma_cluster = 1;
+  int tma_clusters = 0;
   std::vector<unsigned char> upload_image;  // host source of the last upload copy
 };
 

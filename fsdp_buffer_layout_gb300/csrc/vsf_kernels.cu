@@ -40,7 +40,6 @@ namespace {
 
 constexpr int kCopyThreads = 256;
 constexpr int kCopyCtasPerSm = 8;
-constexpr int kAdamThreads = 512;
 constexpr int kMaxCluster = 8;
 constexpr int kSmallThreads = 256;
 
@@ -220,6 +219,7 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __rest
 }
 
 #include "adam8.cuh"
+#include "adam8_tma.cuh"
 
 // ------------------------------------------------------------------ host side
 
@@ -268,10 +268,26 @@ AdamConsts make_consts(const vsf_adam_hparams& hp, int step) {
 
 // Block-kernel variants: wide CTAs for clusters (one CTA per SM), narrower
 // ones when a CTA owns whole blocks (two or more CTAs per SM).
+#ifndef VSF_CLUSTER_THREADS
+#define VSF_CLUSTER_THREADS 512
+#define VSF_CLUSTER_MINB 1
+#define VSF_CLUSTER_U1 4
+#define VSF_CLUSTER_U2 2
+#endif
+#ifndef VSF_SOLO_THREADS
+#define VSF_SOLO_THREADS 256
+#define VSF_SOLO_MINB 2
+#define VSF_SOLO_U1 4
+#define VSF_SOLO_U2 2
+#endif
+constexpr int kClusterThreads = VSF_CLUSTER_THREADS;
+constexpr int kSoloThreads = VSF_SOLO_THREADS;
 template <typename GT>
-constexpr auto kBlockKernelCluster = adam_block_kernel<GT, 512, 1, 4, 2>;
+constexpr auto kBlockKernelCluster = adam_block_kernel<GT, VSF_CLUSTER_THREADS, VSF_CLUSTER_MINB,
+                                                       VSF_CLUSTER_U1, VSF_CLUSTER_U2>;
 template <typename GT>
-constexpr auto kBlockKernelSolo = adam_block_kernel<GT, 256, 2, 4, 2>;
+constexpr auto kBlockKernelSolo =
+    adam_block_kernel<GT, VSF_SOLO_THREADS, VSF_SOLO_MINB, VSF_SOLO_U1, VSF_SOLO_U2>;
 
 template <typename T, int kMode>
 vsf_status launch_copy(const vsf_plan* plan, const void* const* tensors, void* packed,
@@ -317,13 +333,35 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
   }
   int8_t* mq = static_cast<int8_t*>(m_state);
   uint8_t* vq = static_cast<uint8_t*>(v_state);
+  const int ntma = (int)plan->tma_blocks.size();
+  if (ntma > 0) {
+    const int CL = plan->tma_cluster;
+    const int ncl = std::min(plan->tma_clusters, ntma);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ncl * CL);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = TmaLayout<GT>::total;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(
+        &cfg, adam_tma_kernel<GT>, qb, ws_ptr<int32_t>(plan, plan->layout.tma), ntma, ncl, g,
+        d_factor, master, mq, vq, m_scale, v_scale, bf, k,
+        reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error));
+    if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (bulk-copy blocks)");
+  }
   const int nbig = (int)plan->big_blocks.size();
   if (nbig > 0) {
     const int CL = plan->adam_cluster;
     const int ncl = std::min(plan->adam_clusters, nbig);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncl * CL);
-    cfg.blockDim = dim3(CL > 1 ? 512 : 256);
+    cfg.blockDim = dim3(CL > 1 ? kClusterThreads : kSoloThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -392,13 +430,14 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     int active = 0;
     if (cand == 1) {
       int occ = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kBlockKernelSolo<uint16_t>, 256, 0);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kBlockKernelSolo<uint16_t>,
+                                                        kSoloThreads, 0);
       if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (occupancy)");
       active = std::max(1, occ) * sms;
     } else {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cand * 64);
-      cfg.blockDim = dim3(512);
+      cfg.blockDim = dim3(kClusterThreads);
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = cand;
@@ -413,6 +452,37 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     CL = cand;
     nclusters = active;
     if ((double)active * (double)plan->max_big_elems * 4.0 <= budget) break;
+  }
+
+  // Bulk-copy kernel: one CTA per SM (its ring takes ~200 KB of shared
+  // memory); the cluster size follows the same L2 budget.
+  int tma_CL = 1, tma_ncl = 1;
+  {
+    for (auto fn : {(const void*)adam_tma_kernel<uint16_t>, (const void*)adam_tma_kernel<float>}) {
+      const int bytes = fn == (const void*)adam_tma_kernel<uint16_t> ? (int)TmaLayout<uint16_t>::total
+                                                                     : (int)TmaLayout<float>::total;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (shared memory size)");
+    }
+    for (int cand = 1; cand <= kMaxCluster; cand *= 2) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cand * 64);
+      cfg.blockDim = dim3(kTmaThreads);
+      cfg.dynamicSmemBytes = TmaLayout<uint16_t>::total;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cand;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int active = 0;
+      e = cudaOccupancyMaxActiveClusters(&active, adam_tma_kernel<uint16_t>, &cfg);
+      if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (bulk-copy clusters)");
+      tma_CL = cand;
+      tma_ncl = std::max(1, active);
+      if ((double)tma_ncl * (double)plan->max_tma_elems * 4.0 <= budget) break;
+    }
   }
 
   // Host image of the device tables; it lives in the plan so that the
@@ -430,6 +500,8 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     std::memcpy(&img[L.big], plan->big_blocks.data(), 4 * plan->big_blocks.size());
   if (!plan->small_blocks.empty())
     std::memcpy(&img[L.small], plan->small_blocks.data(), 4 * plan->small_blocks.size());
+  if (!plan->tma_blocks.empty())
+    std::memcpy(&img[L.tma], plan->tma_blocks.data(), 4 * plan->tma_blocks.size());
   std::memcpy(&img[L.spans], spans.data(), sizeof(CopySpan) * spans.size());
 
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
@@ -443,6 +515,8 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   plan->copy_grid = grid;
   plan->adam_cluster = CL;
   plan->adam_clusters = std::max(1, nclusters);
+  plan->tma_cluster = tma_CL;
+  plan->tma_clusters = tma_ncl;
   plan->uploaded = true;
   return VSF_OK;
 }

@@ -105,6 +105,11 @@ class ShardStep:
         self.adam(step)
         self.unpack(params)
 
+    def device_error(self) -> int:
+        """The device error word (0 = every bounded wait succeeded)."""
+        off = V.vsf_plan_device_error_offset(self.plan)
+        return int(self.workspace[off:off + 4].view(torch.int32).item())
+
     # ---- harness helpers
     def load_master(self, t: int, values: torch.Tensor):
         o = self.offsets[t]

@@ -76,6 +76,8 @@ def lib():
             L.vsf_plan_qblocks.argtypes = [vp, vp, vp, vp, vp, vp]
             L.vsf_plan_rank_slices.restype = st
             L.vsf_plan_rank_slices.argtypes = [vp, i32, i32, P(i32), vp, vp, vp, vp, vp]
+            L.vsf_plan_device_error_offset.restype = st
+            L.vsf_plan_device_error_offset.argtypes = [vp, P(ctypes.c_size_t)]
             L.vsf_plan_workspace_bytes.restype = ctypes.c_size_t
             L.vsf_plan_workspace_bytes.argtypes = [vp]
             L.vsf_plan_upload.restype = st
@@ -162,6 +164,12 @@ def vsf_plan_rank_slices(plan: int, rank: int):
     a = [(ctypes.c_int64 * max(n, 1))() for _ in range(4)]
     _check(lib().vsf_plan_rank_slices(plan, rank, n, ctypes.byref(count), t, *a))
     return [(t[i], a[0][i], a[1][i], a[2][i], a[3][i]) for i in range(n)]
+
+
+def vsf_plan_device_error_offset(plan: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().vsf_plan_device_error_offset(plan, ctypes.byref(out)))
+    return int(out.value)
 
 
 def vsf_plan_workspace_bytes(plan: int) -> int:

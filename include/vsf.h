@@ -137,6 +137,12 @@ vsf_status vsf_plan_rank_slices(const vsf_plan* plan, int32_t rank, int32_t capa
 /* Bytes of device workspace the caller must provide to vsf_plan_upload. */
 size_t vsf_plan_workspace_bytes(const vsf_plan* plan);
 
+/* Byte offset, inside the workspace, of a 32-bit device error word (zeroed
+ * by vsf_plan_upload). A kernel sets bit 1 when one of its bounded waits
+ * runs out (the step's results are then not to be trusted); the caller reads
+ * it with an ordinary device-to-host copy after synchronising the stream. */
+vsf_status vsf_plan_device_error_offset(const vsf_plan* plan, size_t* offset);
+
 /* Copies the plan's device tables into the caller's workspace (16-byte
  * aligned, vsf_plan_workspace_bytes long) on `stream`, zeroes its scratch,
  * and binds the plan to the current CUDA device. Must precede every per-step

@@ -111,6 +111,7 @@ def run_gpu(case: Case):
             ss.adam(s)
             ss.unpack(params)
             torch.cuda.synchronize()
+            assert ss.device_error() == 0, "a bounded device wait ran out"
             factors.append(float(ss.factor[0].item()))
             norms.append(float(ss.norm[0].item()))
         def host(x):
