@@ -104,17 +104,19 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return d;
 }
 
-// Codes to exact floats: 2^23 + byte has the byte in its low mantissa bits.
+// Codes to exact floats: 2^23 + byte has the byte in its low mantissa bits,
+// and subtracting 2^23 (2^23 + 128 for the offset signed codes) is exact, so
+// the packed add here rounds nothing (and no multiply feeds it).
 __device__ __forceinline__ float2 u8pair_to_f2(uint32_t word, int first) {
   const float2 x = make_float2(__uint_as_float(__byte_perm(word, 0x4B000000u, 0x7540u | first)),
                                __uint_as_float(__byte_perm(word, 0x4B000000u, 0x7541u | first)));
-  return make_float2(__fadd_rn(x.x, -8388608.0f), __fadd_rn(x.y, -8388608.0f));
+  return __fadd2_rn(x, f2(-8388608.0f));
 }
 __device__ __forceinline__ float2 s8pair_to_f2(uint32_t word_xor80, int first) {
   const float2 x =
       make_float2(__uint_as_float(__byte_perm(word_xor80, 0x4B000000u, 0x7540u | first)),
                   __uint_as_float(__byte_perm(word_xor80, 0x4B000000u, 0x7541u | first)));
-  return make_float2(__fadd_rn(x.x, -8388736.0f), __fadd_rn(x.y, -8388736.0f));  // 2^23 + 128
+  return __fadd2_rn(x, f2(-8388736.0f));  // 2^23 + 128
 }
 
 __device__ __forceinline__ uint32_t cvt_sat_s8(float x) {

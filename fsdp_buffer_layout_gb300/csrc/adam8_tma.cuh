@@ -24,20 +24,21 @@
 // then wrong but every CTA still finishes, so no thread hangs and no CTA
 // leaves while a copy or a peer's write into it is still pending).
 
-constexpr int kTmaChunk = 4096;           // elements per chunk
-constexpr int kConsumerWarps = 16;        // 512 consumer threads: one 8-element group each
+constexpr int kConsumerWarps = VSF_TMA_WARPS;   // consumer warps per CTA
+constexpr int kTmaGroups = VSF_TMA_GROUPS;       // 8-element groups per thread and chunk
+constexpr int kTmaChunk = kTmaChunkElems;         // elements per ring chunk
 constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 template <typename GT>
 struct TmaLayout {
-  // ring depth: as many 32 KB (bf16) or 40 KB (fp32) slots as fit in 200 KB
-  static constexpr int slots = sizeof(GT) == 2 ? 6 : 5;
   static constexpr uint32_t grad = 0;
   static constexpr uint32_t mq = kTmaChunk * sizeof(GT);
   static constexpr uint32_t vq = mq + kTmaChunk;
   static constexpr uint32_t master = vq + kTmaChunk;
   static constexpr uint32_t slot = master + kTmaChunk * 4;  // bytes per slot
+  // ring depth: as many slots as fit in 200 KB, at least two
+  static constexpr int slots = (200u * 1024u / slot) < 2 ? 2 : (int)(200u * 1024u / slot);
   static constexpr uint32_t ring = slot * slots;
   // then: full[slots], empty[slots], maxbar[2] (8 B each), maxima[2][8] (float2)
   static constexpr uint32_t bars = ring;
@@ -116,12 +117,52 @@ __device__ __forceinline__ void dsmem_put_arrive(uint32_t local_slot, uint32_t l
                : "memory");
 }
 
+// One ring chunk of a block. Contiguous blocks (one row) are cut into
+// kTmaChunk-element pieces; tiles into runs of whole rows (a power-of-two row
+// length that divides the chunk), which are packed back to back in the slot.
+struct TmaChunk {
+  int64_t gstart;  // buffer element of the chunk's first element
+  int rows;        // rows in the chunk (1 for a contiguous block)
+  int row_len;     // elements per row
+  int stride;      // buffer elements between rows
+  int row_log2;    // log2(row_len) when rows > 1
+  __device__ __forceinline__ int len() const { return rows * row_len; }
+  // Buffer element of the chunk's element `i` (packed row-major order).
+  __device__ __forceinline__ int64_t at(int i) const {
+    return rows == 1 ? gstart + i
+                     : gstart + (int64_t)(i >> row_log2) * stride + (i & (row_len - 1));
+  }
+};
+
+__device__ __forceinline__ int tma_rows_per_chunk(const QBlock& b) { return kTmaChunk / b.ncols; }
+
 // Chunks [c0, c1) of block b that CTA `crank` of CL owns.
 __device__ __forceinline__ void tma_share(const QBlock& b, int CL, int crank, int& c0, int& c1) {
-  const int nch = (b.ncols + kTmaChunk - 1) / kTmaChunk;
+  const int nch = b.nrows == 1 ? (b.ncols + kTmaChunk - 1) / kTmaChunk
+                               : (b.nrows + tma_rows_per_chunk(b) - 1) / tma_rows_per_chunk(b);
   const int per = (nch + CL - 1) / CL;
   c0 = min(nch, crank * per);
   c1 = min(nch, c0 + per);
+}
+
+__device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int c) {
+  TmaChunk k;
+  if (b.nrows == 1) {
+    k.gstart = b.base + (int64_t)c * kTmaChunk;
+    k.rows = 1;
+    k.row_len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)c * kTmaChunk);
+    k.stride = 0;
+    k.row_log2 = 0;
+  } else {
+    const int rpc = tma_rows_per_chunk(b);
+    const int r0 = c * rpc;
+    k.gstart = b.base + (int64_t)r0 * b.stride;
+    k.rows = min(rpc, b.nrows - r0);
+    k.row_len = b.ncols;
+    k.stride = b.stride;
+    k.row_log2 = 31 - __clz(b.ncols);
+  }
+  return k;
 }
 
 template <typename GT>
@@ -155,35 +196,54 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
   cluster.sync();
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one lane issues every copy
-    if (lane == 0) {
-      const uint64_t keep = l2_policy_evict_last();
-      const uint64_t drop = l2_policy_evict_first();
-      uint32_t p = 0;  // position in the ring sequence
-      for (int j = cid; j < nlist; j += nclusters) {
-        const QBlock b = qb[list[j]];
-        int c0, c1;
-        tma_share(b, CL, crank, c0, c1);
-        for (int ph = 0; ph < 2; ++ph) {
-          for (int c = c0; c < c1; ++c, ++p) {
-            const int s = p % kTmaSlots;
-            const uint32_t round = p / kTmaSlots;
+    // ---------------- producer warp: lane 0 waits and posts the byte count,
+    // then the lanes issue the copies (one per array, or one per row and
+    // array for tiles).
+    const uint64_t keep = l2_policy_evict_last();
+    const uint64_t drop = l2_policy_evict_first();
+    uint32_t p = 0;  // position in the ring sequence
+    for (int j = cid; j < nlist; j += nclusters) {
+      const QBlock b = qb[list[j]];
+      int c0, c1;
+      tma_share(b, CL, crank, c0, c1);
+      for (int ph = 0; ph < 2; ++ph) {
+        for (int c = c0; c < c1; ++c, ++p) {
+          const int s = p % kTmaSlots;
+          const uint32_t round = p / kTmaSlots;
+          const TmaChunk ch = tma_chunk(b, c);
+          const uint32_t len = (uint32_t)ch.len();
+          if (lane == 0) {
             if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
-            const int64_t e = b.base + (int64_t)c * kTmaChunk;
-            const uint32_t len = (uint32_t)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)c * kTmaChunk);
-            const uint32_t slot = s0 + s * Lay::slot;
-            const uint64_t pol = ph == 0 ? keep : drop;
-            const uint32_t bytes = len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u);
-            mbar_expect_tx(full_bar(s), bytes);
-            bulk_g2s(slot + Lay::grad, grad + e, len * sizeof(GT), full_bar(s), pol);
-            bulk_g2s(slot + Lay::mq, mq + e, len, full_bar(s), pol);
-            bulk_g2s(slot + Lay::vq, vq + e, len, full_bar(s), pol);
-            if (ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, full_bar(s), drop);
+            mbar_expect_tx(full_bar(s), len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u));
           }
+          __syncwarp();
+          const uint32_t slot = s0 + s * Lay::slot;
+          const uint64_t pol = ph == 0 ? keep : drop;
+          const uint32_t fb = full_bar(s);
+          if (ch.rows == 1) {
+            const int64_t e = ch.gstart;
+            if (lane == 0) bulk_g2s(slot + Lay::grad, grad + e, len * sizeof(GT), fb, pol);
+            if (lane == 1) bulk_g2s(slot + Lay::mq, mq + e, len, fb, pol);
+            if (lane == 2) bulk_g2s(slot + Lay::vq, vq + e, len, fb, pol);
+            if (lane == 3 && ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, fb, drop);
+          } else {
+            const uint32_t rl = (uint32_t)ch.row_len;
+            for (int r = lane; r < ch.rows; r += 32) {
+              const int64_t e = ch.gstart + (int64_t)r * ch.stride;
+              const uint32_t o = (uint32_t)r * rl;
+              bulk_g2s(slot + Lay::grad + o * sizeof(GT), grad + e, rl * sizeof(GT), fb, pol);
+              bulk_g2s(slot + Lay::mq + o, mq + e, rl, fb, pol);
+              bulk_g2s(slot + Lay::vq + o, vq + e, rl, fb, pol);
+              if (ph) bulk_g2s(slot + Lay::master + o * 4u, master + e, rl * 4u, fb, drop);
+            }
+          }
+          __syncwarp();
         }
       }
-      // Every issued copy has been consumed before the consumers finish; wait
-      // for the last ones anyway so that none is in flight at exit.
+    }
+    // Every issued copy has been consumed before the consumers finish; wait
+    // for the last ones anyway so that none is in flight at exit.
+    if (lane == 0) {
       for (int s = 0; s < kTmaSlots; ++s) {
         if (p > (uint32_t)s) {
           const uint32_t last = (p - 1 - s) / kTmaSlots * kTmaSlots + s;  // last position in slot s
@@ -192,7 +252,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       }
     }
   } else {
-    // ---------------- consumers: thread `tid` owns group `tid` of each chunk
+    // ---------------- consumers: thread `tid` owns groups tid, tid + 32*W, ...
     Consts2 c;
     c.b1 = f2(k.b1);
     c.omb1 = f2(k.omb1);
@@ -217,19 +277,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
 
       // phase 1: maxima of the new moments
       float mx = 0.0f, vx = 0.0f;
-      for (int ch = c0; ch < c1; ++ch, ++p) {
+      for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const int len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)ch * kTmaChunk);
-        if (tid * 8 < len) {
-          const unsigned char* sl = smem + s * Lay::slot;
-          Raw r;
-          r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 8 * sizeof(GT));
-          if constexpr (sizeof(GT) == 4)
-            r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 32 + 16);
-          r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + tid * 8);
-          r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + tid * 8);
-          phase1_group<GT>(c, r, mx, vx);
+        const int len = tma_chunk(b, ci).len();
+        const unsigned char* sl = smem + s * Lay::slot;
+#pragma unroll
+        for (int gi = 0; gi < kTmaGroups; ++gi) {
+          const int g = tid + gi * kConsumerWarps * 32;
+          if (g * 8 < len) {
+            Raw r;
+            r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 8 * sizeof(GT));
+            if constexpr (sizeof(GT) == 4)
+              r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 32 + 16);
+            r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + g * 8);
+            r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + g * 8);
+            phase1_group<GT>(c, r, mx, vx);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
@@ -266,35 +330,40 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       }
 
       // phase 2: update, requantise, write
-      for (int ch = c0; ch < c1; ++ch, ++p) {
+      for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const int len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)ch * kTmaChunk);
-        if (tid * 8 < len) {
-          const unsigned char* sl = smem + s * Lay::slot;
-          Raw r;
-          r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 8 * sizeof(GT));
-          if constexpr (sizeof(GT) == 4)
-            r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + tid * 32 + 16);
-          r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + tid * 8);
-          r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + tid * 8);
-          const uint4 pa = *reinterpret_cast<const uint4*>(sl + Lay::master + tid * 32);
-          const uint4 pb = *reinterpret_cast<const uint4*>(sl + Lay::master + tid * 32 + 16);
-          uint4 o0, o1, ob;
-          uint2 ocm, ocv;
-          phase2_group<GT>(c, r, pa, pb, o0, o1, ob, ocm, ocv);
-          const int64_t e = b.base + (int64_t)ch * kTmaChunk + tid * 8;
-          st_v4(master + e, o0, drop);
-          st_v4(master + e + 4, o1, drop);
-          st_v4(bf + e, ob, drop);
-          st_v2(mq + e, ocm, drop);
-          st_v2(vq + e, ocv, drop);
+        const TmaChunk ch = tma_chunk(b, ci);
+        const int len = ch.len();
+        const unsigned char* sl = smem + s * Lay::slot;
+#pragma unroll
+        for (int gi = 0; gi < kTmaGroups; ++gi) {
+          const int g = tid + gi * kConsumerWarps * 32;
+          if (g * 8 < len) {
+            Raw r;
+            r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 8 * sizeof(GT));
+            if constexpr (sizeof(GT) == 4)
+              r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 32 + 16);
+            r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + g * 8);
+            r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + g * 8);
+            const uint4 pa = *reinterpret_cast<const uint4*>(sl + Lay::master + g * 32);
+            const uint4 pb = *reinterpret_cast<const uint4*>(sl + Lay::master + g * 32 + 16);
+            uint4 o0, o1, ob;
+            uint2 ocm, ocv;
+            phase2_group<GT>(c, r, pa, pb, o0, o1, ob, ocm, ocv);
+            const int64_t e = ch.at(g * 8);
+            st_v4(master + e, o0, drop);
+            st_v4(master + e + 4, o1, drop);
+            st_v4(bf + e, ob, drop);
+            st_v2(mq + e, ocm, drop);
+            st_v2(vq + e, ocv, drop);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
       }
     }
   }
-  __syncwarp();     // the producer warp diverged (lane 0 issued the copies)
+  __syncwarp();
   cluster.sync();  // no CTA leaves while a peer may still write into it
 }

@@ -218,7 +218,13 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
       // Contiguous blocks that start on 16 elements and hold a multiple of 16
       // go to the bulk-copy (TMA) kernel; the other row and tile blocks to the
       // register kernel; element chunks to the warp kernel.
-      const bool tma = !small && nr == 1 && base % 16 == 0 && nc % 16 == 0;
+      // Tiles qualify when their rows are 16-aligned, at least 512 elements
+      // long (one bulk copy per row and array: shorter rows make the copies
+      // too small to keep up) and a power-of-two length that fits a chunk.
+      const bool pow2 = nc > 0 && (nc & (nc - 1)) == 0;
+      const bool tma = !small && base % 16 == 0 && nc % 16 == 0 &&
+                       (nr == 1 || (st % 16 == 0 && pow2 && nc >= 512 &&
+                                    nc <= vsf::kTmaChunkElems));
       if (small) {
         plan->small_blocks.push_back((int32_t)plan->qblocks.size());
       } else if (tma) {

@@ -18,6 +18,16 @@ constexpr int kMaxTensors = 2048;
 // device is known.
 constexpr int kMaxCopyGrid = 4096;
 
+// Bulk-copy (TMA) AdamW kernel geometry: consumer warps per CTA, 8-element
+// groups per consumer thread, hence elements per ring chunk.
+#ifndef VSF_TMA_WARPS
+#define VSF_TMA_WARPS 16
+#endif
+#ifndef VSF_TMA_GROUPS
+#define VSF_TMA_GROUPS 2
+#endif
+constexpr int kTmaChunkElems = VSF_TMA_WARPS * 32 * 8 * VSF_TMA_GROUPS;
+
 // One quantisation block as the kernels see it: a row-major region.
 struct QBlock {
   int64_t base;    // buffer element of the first element

@@ -276,9 +276,9 @@ AdamConsts make_consts(const vsf_adam_hparams& hp, int step) {
 #endif
 #ifndef VSF_SOLO_THREADS
 #define VSF_SOLO_THREADS 256
-#define VSF_SOLO_MINB 2
-#define VSF_SOLO_U1 4
-#define VSF_SOLO_U2 2
+#define VSF_SOLO_MINB 4
+#define VSF_SOLO_U1 2
+#define VSF_SOLO_U2 1
 #endif
 constexpr int kClusterThreads = VSF_CLUSTER_THREADS;
 constexpr int kSoloThreads = VSF_SOLO_THREADS;
@@ -423,8 +423,13 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
 
   // Cluster size of the block kernel: the smallest of 1, 2, 4, 8 that keeps
   // the phase-1 bytes in flight (one block per active cluster, 4 B per
-  // element) within 64 MB of the 126 MB L2, so that phase 2's re-read hits.
-  const double budget = 64.0 * 1024 * 1024;
+  // element) within the L2 budget (128 MB of the 126 MB L2 measured best:
+  // phase 2 re-reads the newest part of each block first, and smaller
+  // clusters let every SM work), so that phase 2's re-read hits.
+#ifndef VSF_L2_BUDGET_MB
+#define VSF_L2_BUDGET_MB 128
+#endif
+  const double budget = VSF_L2_BUDGET_MB * 1024.0 * 1024.0;
   int CL = 0, nclusters = 0;
   for (int cand = 1; cand <= kMaxCluster; cand *= 2) {
     int active = 0;

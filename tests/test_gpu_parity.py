@@ -106,6 +106,15 @@ def test_large_blocks_use_clusters():
     compare(case, run_gpu(case), run_oracle(case))
 
 
+def test_wide_tiles_take_the_bulk_copy_path():
+    """Tiles of 16 x 1024 (rows long enough for per-row bulk copies) next to
+    128-column tiles and ragged ones: all bit-exact."""
+    specs = [((64, 4096), W.GRAN_TILE, 16, 1024), ((256, 512), W.GRAN_TILE, 128, 128),
+             ((40, 2048), W.GRAN_TILE, 16, 1024), ((1024,), W.GRAN_ELEM, 0, 0)]
+    case = _normal_case(specs, m=4, g=128, steps=3)
+    compare(case, run_gpu(case), run_oracle(case))
+
+
 def test_heavy_tails_student_t():
     w = W.dsv3_block()
     specs = [((512, 1024), W.GRAN_TILE, 128, 128), ((7168,), W.GRAN_ELEM, 0, 0)]
