@@ -173,7 +173,8 @@ def compare(case: Case, g: dict, o: dict, exact: bool = True):
         if math.isnan(b) or math.isinf(b):
             assert (math.isnan(a) and math.isnan(b)) or a == b, (a, b)
         else:
-            assert abs(a - b) <= 1e-12 * max(abs(b), 1e-300), (a, b)
+            n = sum(case.numels)
+            assert abs(a - b) <= max(1e-12, n * 2.0 ** -53) * max(abs(b), 1e-300), (a, b)
     check_master(g["master"], o["master"])
     if case.quantized:
         check_codes(g["m_state"], o["m_state"], "m codes")
