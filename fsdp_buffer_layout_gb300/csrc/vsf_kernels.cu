@@ -39,7 +39,10 @@ namespace vsf {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kCopyCtasPerSm = 8;
+#ifndef VSF_COPY_CTAS_PER_SM
+#define VSF_COPY_CTAS_PER_SM 8
+#endif
+constexpr int kCopyCtasPerSm = VSF_COPY_CTAS_PER_SM;
 constexpr int kMaxCluster = 8;
 constexpr int kSmallThreads = 256;
 
