@@ -43,7 +43,8 @@ struct TmaLayout {
   // then: full[slots], empty[slots], maxbar[2] (8 B each), maxima[2][8] (float2)
   static constexpr uint32_t bars = ring;
   static constexpr uint32_t maxima = bars + 8 * (2 * slots + 2);
-  static constexpr uint32_t total = maxima + 2 * kMaxCluster * 8;
+  // +128: the kernel rounds the dynamic shared memory base up to 128 bytes
+  static constexpr uint32_t total = maxima + 2 * kMaxCluster * 8 + 128;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -105,6 +106,24 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 2-D tensor copy (global -> shared) of one box at (x, y), completing on `bar`.
+__device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const void* tmap, int x, int y,
+                                             uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// Tensor maps of the tile tensors (per array: gradient, m codes, v codes,
+// master), passed as a grid constant.
+struct TileMaps {
+  CUtensorMap m[kMaxTileMaps][4];
+  int32_t tensor[kMaxTileMaps];
+  int32_t count;
+};
+
 // Remote (cluster) store of a float2 and arrive on the peer's barrier.
 __device__ __forceinline__ void dsmem_put_arrive(uint32_t local_slot, uint32_t local_bar,
                                                  uint32_t rank, float2 v) {
@@ -118,8 +137,8 @@ __device__ __forceinline__ void dsmem_put_arrive(uint32_t local_slot, uint32_t l
 }
 
 // One ring chunk of a block. Contiguous blocks (one row) are cut into
-// kTmaChunk-element pieces; tiles into runs of whole rows (a power-of-two row
-// length that divides the chunk), which are packed back to back in the slot.
+// kTmaChunk-element pieces; tiles into boxes of whole rows (a power-of-two
+// row length), which the tensor copy packs back to back in the slot.
 struct TmaChunk {
   int64_t gstart;  // buffer element of the chunk's first element
   int rows;        // rows in the chunk (1 for a contiguous block)
@@ -167,12 +186,14 @@ __device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int c) {
 
 template <typename GT>
 __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
-    const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist, int nclusters,
+    const __grid_constant__ TileMaps maps, const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist, int nclusters,
     const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
     uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k, unsigned* err) {
   using Lay = TmaLayout<GT>;
   constexpr int kTmaSlots = Lay::slots;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // tensor copies want 128-byte aligned destinations: round the base up
+  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = (int)cluster.num_blocks();
   const int crank = (int)cluster.block_rank();
@@ -196,9 +217,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
   cluster.sync();
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer warp: lane 0 waits and posts the byte count,
-    // then the lanes issue the copies (one per array, or one per row and
-    // array for tiles).
+    // ---------------- producer warp: lane 0 waits for the slot, posts the
+    // byte count and issues the copies (one 1-D bulk copy per array for a
+    // contiguous chunk, one 2-D tensor copy per array for a tile chunk).
     const uint64_t keep = l2_policy_evict_last();
     const uint64_t drop = l2_policy_evict_first();
     uint32_t p = 0;  // position in the ring sequence
@@ -206,38 +227,35 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       const QBlock b = qb[list[j]];
       int c0, c1;
       tma_share(b, CL, crank, c0, c1);
+      int mi = 0;
+      if (b.tx >= 0)
+        while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
       for (int ph = 0; ph < 2; ++ph) {
         for (int c = c0; c < c1; ++c, ++p) {
-          const int s = p % kTmaSlots;
-          const uint32_t round = p / kTmaSlots;
-          const TmaChunk ch = tma_chunk(b, c);
-          const uint32_t len = (uint32_t)ch.len();
           if (lane == 0) {
+            const int s = p % kTmaSlots;
+            const uint32_t round = p / kTmaSlots;
+            const TmaChunk ch = tma_chunk(b, c);
+            const uint32_t len = (uint32_t)ch.len();
             if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
-            mbar_expect_tx(full_bar(s), len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u));
-          }
-          __syncwarp();
-          const uint32_t slot = s0 + s * Lay::slot;
-          const uint64_t pol = ph == 0 ? keep : drop;
-          const uint32_t fb = full_bar(s);
-          if (ch.rows == 1) {
-            const int64_t e = ch.gstart;
-            if (lane == 0) bulk_g2s(slot + Lay::grad, grad + e, len * sizeof(GT), fb, pol);
-            if (lane == 1) bulk_g2s(slot + Lay::mq, mq + e, len, fb, pol);
-            if (lane == 2) bulk_g2s(slot + Lay::vq, vq + e, len, fb, pol);
-            if (lane == 3 && ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, fb, drop);
-          } else {
-            const uint32_t rl = (uint32_t)ch.row_len;
-            for (int r = lane; r < ch.rows; r += 32) {
-              const int64_t e = ch.gstart + (int64_t)r * ch.stride;
-              const uint32_t o = (uint32_t)r * rl;
-              bulk_g2s(slot + Lay::grad + o * sizeof(GT), grad + e, rl * sizeof(GT), fb, pol);
-              bulk_g2s(slot + Lay::mq + o, mq + e, rl, fb, pol);
-              bulk_g2s(slot + Lay::vq + o, vq + e, rl, fb, pol);
-              if (ph) bulk_g2s(slot + Lay::master + o * 4u, master + e, rl * 4u, fb, drop);
+            const uint32_t fb = full_bar(s);
+            mbar_expect_tx(fb, len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u));
+            const uint32_t slot = s0 + s * Lay::slot;
+            const uint64_t pol = ph == 0 ? keep : drop;
+            if (b.tx < 0) {
+              const int64_t e = ch.gstart;
+              bulk_g2s(slot + Lay::grad, grad + e, len * sizeof(GT), fb, pol);
+              bulk_g2s(slot + Lay::mq, mq + e, len, fb, pol);
+              bulk_g2s(slot + Lay::vq, vq + e, len, fb, pol);
+              if (ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, fb, drop);
+            } else {
+              const int y = b.ty + c * tma_rows_per_chunk(b);
+              tensor2d_g2s(slot + Lay::grad, &maps.m[mi][0], b.tx, y, fb, pol);
+              tensor2d_g2s(slot + Lay::mq, &maps.m[mi][1], b.tx, y, fb, pol);
+              tensor2d_g2s(slot + Lay::vq, &maps.m[mi][2], b.tx, y, fb, pol);
+              if (ph) tensor2d_g2s(slot + Lay::master, &maps.m[mi][3], b.tx, y, fb, drop);
             }
           }
-          __syncwarp();
         }
       }
     }

@@ -208,23 +208,47 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
   // Quantisation blocks, tensor order ([VSF] case study › 8-bit Adam).
   for (int t = 0; t < n; ++t) {
     const vsf::TensorInfo& x = ts[t];
-    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, bool small) {
+    // Tile tensors whose full tiles go to the bulk-copy kernel as 2-D tensor
+    // copies: tile width a power of two in [32, 256] (the copy box limit),
+    // whole boxes of rows per tile, 16-element aligned rows and offset.
+    int map = -1;
+    if (x.gran == VSF_GRAN_TILE && (int)plan->tile_maps.size() < vsf::kMaxTileMaps) {
+      const int64_t bc = x.tile_cols, br = x.block_rows;
+      const int64_t box_rows = std::min<int64_t>(br, vsf::kTmaChunkElems / std::max<int64_t>(bc, 1));
+      if (bc % 16 == 0 && bc >= 32 && bc <= 256 && (bc & (bc - 1)) == 0 && box_rows >= 1 &&
+          box_rows <= 256 &&
+          br % box_rows == 0 && x.cols % 16 == 0 && x.offset % 16 == 0 && x.cols >= bc) {
+        vsf::TileMapInfo mi;
+        mi.tensor = t;
+        mi.box_cols = (int32_t)bc;
+        mi.box_rows = (int32_t)box_rows;
+        mi.rows = x.rows;
+        mi.cols = x.cols;
+        mi.offset = x.offset;
+        map = (int)plan->tile_maps.size();
+        plan->tile_maps.push_back(mi);
+      }
+    }
+    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, bool small, int64_t r0,
+                   int64_t c0) {
       vsf::QBlock b{};
       b.base = base;
       b.nrows = (int32_t)nr;
       b.ncols = (int32_t)nc;
       b.stride = (int32_t)st;
       b.tensor = t;
-      // Contiguous blocks that start on 16 elements and hold a multiple of 16
-      // go to the bulk-copy (TMA) kernel; the other row and tile blocks to the
-      // register kernel; element chunks to the warp kernel.
-      // Tiles qualify when their rows are 16-aligned, at least 512 elements
-      // long (one bulk copy per row and array: shorter rows make the copies
-      // too small to keep up) and a power-of-two length that fits a chunk.
-      const bool pow2 = nc > 0 && (nc & (nc - 1)) == 0;
-      const bool tma = !small && base % 16 == 0 && nc % 16 == 0 &&
-                       (nr == 1 || (st % 16 == 0 && pow2 && nc >= 512 &&
-                                    nc <= vsf::kTmaChunkElems));
+      b.tx = -1;
+      b.ty = -1;
+      // Element chunks go to the warp kernel. Contiguous blocks that start
+      // on 16 elements and hold a multiple of 16, and full tiles of a mapped
+      // tile tensor, go to the bulk-copy (TMA) kernel; every other row or
+      // tile block (ragged or unaligned) to the register kernel.
+      const bool tile2d = map >= 0 && nr == x.block_rows && nc == x.tile_cols;
+      const bool tma = !small && ((nr == 1 && base % 16 == 0 && nc % 16 == 0) || tile2d);
+      if (tile2d) {
+        b.tx = (int32_t)c0;
+        b.ty = (int32_t)r0;
+      }
       if (small) {
         plan->small_blocks.push_back((int32_t)plan->qblocks.size());
       } else if (tma) {
@@ -243,7 +267,7 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
       }
       for (int64_t e = 0; e < x.numel; e += g_coll) {
         int64_t len = std::min(g_coll, x.numel - e);
-        add(x.offset + e, 1, len, len, true);
+        add(x.offset + e, 1, len, len, true, 0, e);
       }
     } else {
       const int64_t tc = x.gran == VSF_GRAN_TILE ? x.tile_cols : x.cols;
@@ -257,13 +281,17 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
               delete plan;
               return fail(VSF_ERR_OVERFLOW, "quantisation block larger than 2^31 elements");
             }
-            add(x.offset + r * x.cols, 1, nr * x.cols, nr * x.cols, false);
+            add(x.offset + r * x.cols, 1, nr * x.cols, nr * x.cols, false, r, 0);
           } else {
             if (x.cols > INT32_MAX) {
               delete plan;
               return fail(VSF_ERR_OVERFLOW, "row longer than 2^31 elements");
             }
-            add(x.offset + r * x.cols + c, nr, nc, x.cols, false);
+            if (x.rows > INT32_MAX) {
+              delete plan;
+              return fail(VSF_ERR_OVERFLOW, "more than 2^31 rows");
+            }
+            add(x.offset + r * x.cols + c, nr, nc, x.cols, false, r, c);
           }
         }
       }

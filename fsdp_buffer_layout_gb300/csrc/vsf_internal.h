@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -35,7 +36,7 @@ struct QBlock {
   int32_t ncols;   // elements per row
   int32_t stride;  // elements between row starts
   int32_t tensor;
-  int64_t pad;
+  int32_t tx, ty;  // tiles read by 2-D tensor copies: column and row in the tensor; else -1
 };
 static_assert(sizeof(QBlock) == 32, "QBlock is a 32-byte device record");
 
@@ -45,6 +46,15 @@ struct CopySpan {
   int32_t tensor;
   int32_t pad;
   int64_t elem;
+};
+
+// Tile tensors whose full tiles the bulk-copy kernel reads with 2-D tensor
+// copies (one tensor map per array and tensor, encoded per call).
+constexpr int kMaxTileMaps = 16;
+struct TileMapInfo {
+  int32_t tensor;
+  int32_t box_cols, box_rows;  // one copy = box_rows rows of box_cols elements
+  int64_t rows, cols, offset;  // the tensor's 2-D view inside the buffer
 };
 
 struct TensorInfo {
@@ -75,7 +85,8 @@ struct vsf_plan {
   std::vector<vsf::TensorInfo> tensors;
   std::vector<vsf::QBlock> qblocks;
   std::vector<int32_t> big_blocks;    // ROWS / TILE blocks: register block kernel
-  std::vector<int32_t> tma_blocks;    // contiguous, 16-aligned blocks: TMA kernel
+  std::vector<int32_t> tma_blocks;    // contiguous, 16-aligned blocks and full tiles: TMA kernel
+  std::vector<vsf::TileMapInfo> tile_maps;
   std::vector<int32_t> small_blocks;  // ELEM chunks: warp kernel
   int64_t max_big_elems = 0;
   int64_t max_tma_elems = 0;
@@ -92,6 +103,11 @@ struct vsf_plan {
   int tma_cluster = 1;
   int tma_clusters = 0;
   std::vector<unsigned char> upload_image;  // host source of the last upload copy
+  // Tensor maps of the tile tensors, encoded for the last pointers seen.
+  mutable std::mutex maps_mu;
+  mutable std::vector<unsigned char> maps_blob;  // kernel-parameter image
+  mutable const void* maps_key[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  mutable int maps_dtype = -1;
 };
 
 namespace vsf {

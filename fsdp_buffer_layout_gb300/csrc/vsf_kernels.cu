@@ -23,6 +23,8 @@
 // compiler never contracts into an FMA, so each operation rounds once in the
 // order written.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,7 +42,7 @@ namespace {
 
 constexpr int kCopyThreads = 256;
 #ifndef VSF_COPY_CTAS_PER_SM
-#define VSF_COPY_CTAS_PER_SM 8
+#define VSF_COPY_CTAS_PER_SM 16
 #endif
 constexpr int kCopyCtasPerSm = VSF_COPY_CTAS_PER_SM;
 constexpr int kMaxCluster = 8;
@@ -318,6 +320,68 @@ vsf_status launch_copy(const vsf_plan* plan, const void* const* tensors, void* p
   return e == cudaSuccess ? VSF_OK : cuda_fail(e, who);
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// The tile tensors' tensor maps for these arrays, re-encoded only when the
+// pointers or the gradient type change since the previous call.
+vsf_status tile_maps(const vsf_plan* plan, const void* grad, int grad_dtype, const void* mq,
+                     const void* vq, const void* master, TileMaps* out) {
+  std::memset(out, 0, sizeof(*out));
+  out->count = (int32_t)plan->tile_maps.size();
+  if (out->count == 0) return VSF_OK;
+  std::lock_guard<std::mutex> lock(plan->maps_mu);
+  const void* key[5] = {grad, mq, vq, master, nullptr};
+  if (plan->maps_dtype == grad_dtype && std::memcmp(plan->maps_key, key, sizeof(key)) == 0 &&
+      plan->maps_blob.size() == sizeof(TileMaps)) {
+    std::memcpy(out, plan->maps_blob.data(), sizeof(TileMaps));
+    return VSF_OK;
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return fail(VSF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const CUtensorMapDataType gtype =
+      grad_dtype == VSF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int gsize = grad_dtype == VSF_BF16 ? 2 : 4;
+  const void* arrays[4] = {grad, mq, vq, master};
+  const CUtensorMapDataType types[4] = {gtype, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                        CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                        CU_TENSOR_MAP_DATA_TYPE_FLOAT32};
+  const int sizes[4] = {gsize, 1, 1, 4};
+  for (int i = 0; i < out->count; ++i) {
+    const TileMapInfo& mi = plan->tile_maps[i];
+    out->tensor[i] = mi.tensor;
+    for (int a = 0; a < 4; ++a) {
+      cuuint64_t dims[2] = {(cuuint64_t)mi.cols, (cuuint64_t)mi.rows};
+      cuuint64_t strides[1] = {(cuuint64_t)mi.cols * sizes[a]};
+      cuuint32_t box[2] = {(cuuint32_t)mi.box_cols, (cuuint32_t)mi.box_rows};
+      cuuint32_t estr[2] = {1, 1};
+      void* addr = const_cast<char*>(static_cast<const char*>(arrays[a])) + mi.offset * sizes[a];
+      CUresult r = encode(&out->m[i][a], types[a], 2, addr, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS)
+        return fail(VSF_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    }
+  }
+  plan->maps_blob.assign(reinterpret_cast<const unsigned char*>(out),
+                         reinterpret_cast<const unsigned char*>(out) + sizeof(TileMaps));
+  std::memcpy(plan->maps_key, key, sizeof(key));
+  plan->maps_dtype = grad_dtype;
+  return VSF_OK;
+}
+
 template <typename GT>
 vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_factor,
                        float* master, void* m_state, void* v_state, float* m_scale,
@@ -352,8 +416,12 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    TileMaps maps;
+    vsf_status ms = tile_maps(plan, grad, sizeof(GT) == 2 ? VSF_BF16 : VSF_FP32, m_state, v_state,
+                              master, &maps);
+    if (ms != VSF_OK) return ms;
     cudaError_t e = cudaLaunchKernelEx(
-        &cfg, adam_tma_kernel<GT>, qb, ws_ptr<int32_t>(plan, plan->layout.tma), ntma, ncl, g,
+        &cfg, adam_tma_kernel<GT>, maps, qb, ws_ptr<int32_t>(plan, plan->layout.tma), ntma, ncl, g,
         d_factor, master, mq, vq, m_scale, v_scale, bf, k,
         reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error));
     if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (bulk-copy blocks)");

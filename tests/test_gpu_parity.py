@@ -106,11 +106,13 @@ def test_large_blocks_use_clusters():
     compare(case, run_gpu(case), run_oracle(case))
 
 
-def test_wide_tiles_take_the_bulk_copy_path():
-    """Tiles of 16 x 1024 (rows long enough for per-row bulk copies) next to
-    128-column tiles and ragged ones: all bit-exact."""
-    specs = [((64, 4096), W.GRAN_TILE, 16, 1024), ((256, 512), W.GRAN_TILE, 128, 128),
-             ((40, 2048), W.GRAN_TILE, 16, 1024), ((1024,), W.GRAN_ELEM, 0, 0)]
+def test_tiles_on_every_path():
+    """Full tiles of mapped tile tensors (2-D tensor copies: 128x128, 32x64),
+    ragged bottom tiles and tiles wider than a copy box (register kernel),
+    next to element chunks: all bit-exact."""
+    specs = [((256, 512), W.GRAN_TILE, 128, 128), ((96, 256), W.GRAN_TILE, 32, 64),
+             ((200, 384), W.GRAN_TILE, 64, 128), ((64, 4096), W.GRAN_TILE, 16, 1024),
+             ((1024,), W.GRAN_ELEM, 0, 0)]
     case = _normal_case(specs, m=4, g=128, steps=3)
     compare(case, run_gpu(case), run_oracle(case))
 
