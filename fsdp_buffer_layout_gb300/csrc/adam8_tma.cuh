@@ -40,11 +40,12 @@ struct TmaLayout {
   // ring depth: as many slots as fit in 200 KB, at least two
   static constexpr int slots = (200u * 1024u / slot) < 2 ? 2 : (int)(200u * 1024u / slot);
   static constexpr uint32_t ring = slot * slots;
-  // then: full[slots], empty[slots], maxbar[2] (8 B each), maxima[2][8] (float2)
+  // then: full[slots], empty[slots], maxbar[2] (8 B each), and the block
+  // maxima maxima[2][kMaxCluster][kMaxUnitTiles] (float2)
   static constexpr uint32_t bars = ring;
   static constexpr uint32_t maxima = bars + 8 * (2 * slots + 2);
   // +128: the kernel rounds the dynamic shared memory base up to 128 bytes
-  static constexpr uint32_t total = maxima + 2 * kMaxCluster * 8 + 128;
+  static constexpr uint32_t total = maxima + 2 * kMaxCluster * kMaxUnitTiles * 8 + 128;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -124,21 +125,26 @@ struct TileMaps {
   int32_t count;
 };
 
-// Remote (cluster) store of a float2 and arrive on the peer's barrier.
-__device__ __forceinline__ void dsmem_put_arrive(uint32_t local_slot, uint32_t local_bar,
-                                                 uint32_t rank, float2 v) {
-  uint32_t rs, rb;
+// Remote (cluster) store of a float2 into a peer's shared memory.
+__device__ __forceinline__ void dsmem_put(uint32_t local_slot, uint32_t rank, float2 v) {
+  uint32_t rs;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(local_slot), "r"(rank));
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(rs), "f"(v.x), "f"(v.y)
                : "memory");
+}
+// Arrive (release at cluster scope) on a peer's barrier: the stores before
+// it are visible to the peer's threads once they see the phase complete.
+__device__ __forceinline__ void dsmem_arrive(uint32_t local_bar, uint32_t rank) {
+  uint32_t rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb)
                : "memory");
 }
 
-// One ring chunk of a block. Contiguous blocks (one row) are cut into
-// kTmaChunk-element pieces; tiles into boxes of whole rows (a power-of-two
-// row length), which the tensor copy packs back to back in the slot.
+// One ring chunk of a work unit. Contiguous blocks (one row) are cut into
+// kTmaChunk-element pieces; a unit of k tiles into boxes of whole rows of
+// W = k * tile_cols elements (a power of two <= 256), which the tensor copy
+// packs back to back in the slot.
 struct TmaChunk {
   int64_t gstart;  // buffer element of the chunk's first element
   int rows;        // rows in the chunk (1 for a contiguous block)
@@ -153,40 +159,46 @@ struct TmaChunk {
   }
 };
 
-__device__ __forceinline__ int tma_rows_per_chunk(const QBlock& b) { return kTmaChunk / b.ncols; }
+// Unit width: the block's row length times its tiles (1 for contiguous).
+__device__ __forceinline__ int tma_width(const QBlock& b, int k) { return b.ncols * k; }
+__device__ __forceinline__ int tma_rows_per_chunk(const QBlock& b, int k) {
+  return kTmaChunk / tma_width(b, k);
+}
 
-// Chunks [c0, c1) of block b that CTA `crank` of CL owns.
-__device__ __forceinline__ void tma_share(const QBlock& b, int CL, int crank, int& c0, int& c1) {
-  const int nch = b.nrows == 1 ? (b.ncols + kTmaChunk - 1) / kTmaChunk
-                               : (b.nrows + tma_rows_per_chunk(b) - 1) / tma_rows_per_chunk(b);
+// Chunks [c0, c1) of a unit that CTA `crank` of CL owns.
+__device__ __forceinline__ void tma_share(const QBlock& b, int k, int CL, int crank, int& c0,
+                                          int& c1) {
+  const int rpc = b.nrows == 1 ? 1 : tma_rows_per_chunk(b, k);
+  const int nch = b.nrows == 1 ? (b.ncols + kTmaChunk - 1) / kTmaChunk : (b.nrows + rpc - 1) / rpc;
   const int per = (nch + CL - 1) / CL;
   c0 = min(nch, crank * per);
   c1 = min(nch, c0 + per);
 }
 
-__device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int c) {
-  TmaChunk k;
+__device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int k, int c) {
+  TmaChunk ch;
   if (b.nrows == 1) {
-    k.gstart = b.base + (int64_t)c * kTmaChunk;
-    k.rows = 1;
-    k.row_len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)c * kTmaChunk);
-    k.stride = 0;
-    k.row_log2 = 0;
+    ch.gstart = b.base + (int64_t)c * kTmaChunk;
+    ch.rows = 1;
+    ch.row_len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)c * kTmaChunk);
+    ch.stride = 0;
+    ch.row_log2 = 0;
   } else {
-    const int rpc = tma_rows_per_chunk(b);
+    const int rpc = tma_rows_per_chunk(b, k);
     const int r0 = c * rpc;
-    k.gstart = b.base + (int64_t)r0 * b.stride;
-    k.rows = min(rpc, b.nrows - r0);
-    k.row_len = b.ncols;
-    k.stride = b.stride;
-    k.row_log2 = 31 - __clz(b.ncols);
+    ch.gstart = b.base + (int64_t)r0 * b.stride;
+    ch.rows = min(rpc, b.nrows - r0);
+    ch.row_len = tma_width(b, k);
+    ch.stride = b.stride;
+    ch.row_log2 = 31 - __clz(ch.row_len);
   }
-  return k;
+  return ch;
 }
 
 template <typename GT>
 __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
-    const __grid_constant__ TileMaps maps, const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist, int nclusters,
+    const __grid_constant__ TileMaps maps, const QBlock* __restrict__ qb,
+    const int32_t* __restrict__ list, const int32_t* __restrict__ ktab, int nlist, int nclusters,
     const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
     uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k, unsigned* err) {
   using Lay = TmaLayout<GT>;
@@ -225,8 +237,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
     uint32_t p = 0;  // position in the ring sequence
     for (int j = cid; j < nlist; j += nclusters) {
       const QBlock b = qb[list[j]];
+      const int kt = ktab[j];
       int c0, c1;
-      tma_share(b, CL, crank, c0, c1);
+      tma_share(b, kt, CL, crank, c0, c1);
       int mi = 0;
       if (b.tx >= 0)
         while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
           if (lane == 0) {
             const int s = p % kTmaSlots;
             const uint32_t round = p / kTmaSlots;
-            const TmaChunk ch = tma_chunk(b, c);
+            const TmaChunk ch = tma_chunk(b, kt, c);
             const uint32_t len = (uint32_t)ch.len();
             if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
             const uint32_t fb = full_bar(s);
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
               bulk_g2s(slot + Lay::vq, vq + e, len, fb, pol);
               if (ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, fb, drop);
             } else {
-              const int y = b.ty + c * tma_rows_per_chunk(b);
+              const int y = b.ty + c * tma_rows_per_chunk(b, kt);
               tensor2d_g2s(slot + Lay::grad, &maps.m[mi][0], b.tx, y, fb, pol);
               tensor2d_g2s(slot + Lay::mq, &maps.m[mi][1], b.tx, y, fb, pol);
               tensor2d_g2s(slot + Lay::vq, &maps.m[mi][2], b.tx, y, fb, pol);
@@ -281,16 +294,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
     c.alpha = f2(k.alpha);
     c.factor = f2(*d_factor);
     const uint64_t drop = l2_policy_evict_first();
-    __shared__ float red[2][2][kConsumerWarps];
+    __shared__ float red[2][2][kConsumerWarps][kMaxUnitTiles];
     uint32_t p = 0;
-    int nb = 0;  // blocks done by this CTA
+    int nb = 0;  // units done by this CTA
     for (int j = cid; j < nlist; j += nclusters, ++nb) {
-      const int q = list[j];
-      const QBlock b = qb[q];
+      const int q0 = list[j];
+      const QBlock b = qb[q0];
+      const int kt = ktab[j];
+      // This thread's groups always sit in the same column group of a row, so
+      // in one tile of the unit: tt (0 for a contiguous block).
+      const int gpr = b.nrows == 1 ? 32 : tma_width(b, kt) >> 3;  // groups per row (<= 32)
+      const int gpt = b.nrows == 1 ? 32 : b.ncols >> 3;           // groups per tile
+      const int tt = b.nrows == 1 ? 0 : (tid % gpr) / gpt;
+      const int q = q0 + tt;
       c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
       c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
       int c0, c1;
-      tma_share(b, CL, crank, c0, c1);
+      tma_share(b, kt, CL, crank, c0, c1);
       const int par = nb & 1;
 
       // phase 1: maxima of the new moments
@@ -298,7 +318,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const int len = tma_chunk(b, ci).len();
+        const int len = tma_chunk(b, kt, ci).len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll
         for (int gi = 0; gi < kTmaGroups; ++gi) {
@@ -316,33 +336,43 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
       }
-      mx = warp_max(mx);
-      vx = warp_max(vx);
-      if (lane == 0) {
-        red[par][0][warp] = mx;
-        red[par][1][warp] = vx;
+      // Per-tile warp maxima: the lanes of one tile are runs of gpt lanes
+      // that repeat every gpr lanes.
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (o < gpt || o >= gpr) {
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          vx = fmaxf(vx, __shfl_xor_sync(0xffffffffu, vx, o));
+        }
+      }
+      if (lane < gpr && lane % gpt == 0) {
+        red[par][0][warp][lane / gpt] = mx;
+        red[par][1][warp][lane / gpt] = vx;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
       if (tid == 0) {
-        float bm = 0.0f, bv = 0.0f;
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          bm = fmaxf(bm, red[par][0][w]);
-          bv = fmaxf(bv, red[par][1][w]);
+        for (int t = 0; t < kt; ++t) {
+          float bm = 0.0f, bv = 0.0f;
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            bm = fmaxf(bm, red[par][0][w][t]);
+            bv = fmaxf(bv, red[par][1][w][t]);
+          }
+          for (int rk = 0; rk < CL; ++rk)
+            dsmem_put(smem_u32(&maxima[(par * kMaxCluster + crank) * kMaxUnitTiles + t]), rk,
+                      make_float2(bm, bv));
         }
-        for (int rk = 0; rk < CL; ++rk)
-          dsmem_put_arrive(smem_u32(&maxima[par * kMaxCluster + crank]), max_bar(par), rk,
-                           make_float2(bm, bv));
+        for (int rk = 0; rk < CL; ++rk) dsmem_arrive(max_bar(par), rk);
       }
       mbar_wait_cluster(max_bar(par), (nb >> 1) & 1, err);
       float sm = 0.0f, sv = 0.0f;
       for (int rk = 0; rk < CL; ++rk) {
-        const float2 v = maxima[par * kMaxCluster + rk];
+        const float2 v = maxima[(par * kMaxCluster + rk) * kMaxUnitTiles + tt];
         sm = fmaxf(sm, v.x);
         sv = fmaxf(sv, v.y);
       }
       c.im = f2(sm > 0.0f ? __fdiv_rn(127.0f, sm) : 0.0f);
       c.iv = f2(sv > 0.0f ? __fdiv_rn(255.0f, sv) : 0.0f);
-      if (crank == 0 && tid == 0) {
+      if (crank == 0 && tid < kt * gpt && tid % gpt == 0) {  // one thread per tile
         m_scale[q] = sm;
         v_scale[q] = sv;
       }
@@ -351,7 +381,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const TmaChunk ch = tma_chunk(b, ci);
+        const TmaChunk ch = tma_chunk(b, kt, ci);
         const int len = ch.len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll

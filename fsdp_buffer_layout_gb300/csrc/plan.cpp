@@ -209,27 +209,39 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
   for (int t = 0; t < n; ++t) {
     const vsf::TensorInfo& x = ts[t];
     // Tile tensors whose full tiles go to the bulk-copy kernel as 2-D tensor
-    // copies: tile width a power of two in [32, 256] (the copy box limit),
-    // whole boxes of rows per tile, 16-element aligned rows and offset.
+    // copies: tile width a power of two in [32, 256], k = 256 / width tiles
+    // per work unit (one copy box of 256 columns), whole boxes of rows per
+    // tile, 16-element aligned rows and offset.
     int map = -1;
+    int64_t k = 1;
     if (x.gran == VSF_GRAN_TILE && (int)plan->tile_maps.size() < vsf::kMaxTileMaps) {
       const int64_t bc = x.tile_cols, br = x.block_rows;
-      const int64_t box_rows = std::min<int64_t>(br, vsf::kTmaChunkElems / std::max<int64_t>(bc, 1));
-      if (bc % 16 == 0 && bc >= 32 && bc <= 256 && (bc & (bc - 1)) == 0 && box_rows >= 1 &&
-          box_rows <= 256 &&
-          br % box_rows == 0 && x.cols % 16 == 0 && x.offset % 16 == 0 && x.cols >= bc) {
-        vsf::TileMapInfo mi;
-        mi.tensor = t;
-        mi.box_cols = (int32_t)bc;
-        mi.box_rows = (int32_t)box_rows;
-        mi.rows = x.rows;
-        mi.cols = x.cols;
-        mi.offset = x.offset;
-        map = (int)plan->tile_maps.size();
-        plan->tile_maps.push_back(mi);
+      if (bc >= 32 && bc <= 256 && (bc & (bc - 1)) == 0) {
+        k = std::min<int64_t>(256 / bc, vsf::kMaxUnitTiles);
+        const int64_t box_cols = k * bc;
+        const int64_t box_rows = std::min<int64_t>(br, vsf::kTmaChunkElems / box_cols);
+        if (box_rows >= 1 && box_rows <= 256 && br % box_rows == 0 && x.cols % 16 == 0 &&
+            x.offset % 16 == 0 && x.cols >= box_cols) {
+          vsf::TileMapInfo mi;
+          mi.tensor = t;
+          mi.tile_cols = (int32_t)bc;
+          mi.k = (int32_t)k;
+          mi.box_cols = (int32_t)box_cols;
+          mi.box_rows = (int32_t)box_rows;
+          mi.rows = x.rows;
+          mi.cols = x.cols;
+          mi.offset = x.offset;
+          map = (int)plan->tile_maps.size();
+          plan->tile_maps.push_back(mi);
+        }
       }
     }
-    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, bool small, int64_t r0,
+    // Where a block goes: element chunks to the warp kernel; contiguous
+    // blocks that start on 16 elements and hold a multiple of 16, and full
+    // tiles grouped k at a time, to the bulk-copy (TMA) kernel; every other
+    // row or tile block (ragged, unaligned, leftover) to the register kernel.
+    enum Dest { kSmall, kTma, kTmaTile, kTmaTileMember, kRegister };
+    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, Dest dest, int64_t r0,
                    int64_t c0) {
       vsf::QBlock b{};
       b.base = base;
@@ -239,23 +251,19 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
       b.tensor = t;
       b.tx = -1;
       b.ty = -1;
-      // Element chunks go to the warp kernel. Contiguous blocks that start
-      // on 16 elements and hold a multiple of 16, and full tiles of a mapped
-      // tile tensor, go to the bulk-copy (TMA) kernel; every other row or
-      // tile block (ragged or unaligned) to the register kernel.
-      const bool tile2d = map >= 0 && nr == x.block_rows && nc == x.tile_cols;
-      const bool tma = !small && ((nr == 1 && base % 16 == 0 && nc % 16 == 0) || tile2d);
-      if (tile2d) {
+      const int32_t q = (int32_t)plan->qblocks.size();
+      if (dest == kTmaTile || dest == kTmaTileMember) {
         b.tx = (int32_t)c0;
         b.ty = (int32_t)r0;
       }
-      if (small) {
-        plan->small_blocks.push_back((int32_t)plan->qblocks.size());
-      } else if (tma) {
-        plan->tma_blocks.push_back((int32_t)plan->qblocks.size());
-        plan->max_tma_elems = std::max(plan->max_tma_elems, nr * nc);
-      } else {
-        plan->big_blocks.push_back((int32_t)plan->qblocks.size());
+      if (dest == kSmall) {
+        plan->small_blocks.push_back(q);
+      } else if (dest == kTma || dest == kTmaTile) {
+        plan->tma_blocks.push_back(q);
+        plan->tma_tiles.push_back(dest == kTmaTile ? (int32_t)k : 1);
+        plan->max_tma_elems = std::max(plan->max_tma_elems, nr * nc * (dest == kTmaTile ? k : 1));
+      } else if (dest == kRegister) {
+        plan->big_blocks.push_back(q);
         plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
       }
       plan->qblocks.push_back(b);
@@ -267,32 +275,33 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
       }
       for (int64_t e = 0; e < x.numel; e += g_coll) {
         int64_t len = std::min(g_coll, x.numel - e);
-        add(x.offset + e, 1, len, len, true, 0, e);
+        add(x.offset + e, 1, len, len, kSmall, 0, e);
       }
-    } else {
-      const int64_t tc = x.gran == VSF_GRAN_TILE ? x.tile_cols : x.cols;
+    } else if (x.gran == VSF_GRAN_ROWS) {
       for (int64_t r = 0; r < x.rows; r += x.block_rows) {
         const int64_t nr = std::min(x.block_rows, x.rows - r);
-        for (int64_t c = 0; c < x.cols; c += tc) {
+        // a whole-row block is contiguous: one row of nr*cols elements
+        if (nr * x.cols > INT32_MAX) {
+          delete plan;
+          return fail(VSF_ERR_OVERFLOW, "quantisation block larger than 2^31 elements");
+        }
+        const int64_t base = x.offset + r * x.cols, len = nr * x.cols;
+        add(base, 1, len, len, base % 16 == 0 && len % 16 == 0 ? kTma : kRegister, r, 0);
+      }
+    } else {
+      if (x.cols > INT32_MAX || x.rows > INT32_MAX) {
+        delete plan;
+        return fail(VSF_ERR_OVERFLOW, "tile tensor dimension beyond 2^31");
+      }
+      const int64_t tc = x.tile_cols;
+      for (int64_t r = 0; r < x.rows; r += x.block_rows) {
+        const int64_t nr = std::min(x.block_rows, x.rows - r);
+        const int64_t full = nr == x.block_rows ? x.cols / tc : 0;  // full tiles in the stripe
+        const int64_t grouped = map >= 0 ? full / k * k : 0;       // of them, in whole units
+        for (int64_t c = 0, i = 0; c < x.cols; c += tc, ++i) {
           const int64_t nc = std::min(tc, x.cols - c);
-          if (x.gran == VSF_GRAN_ROWS) {
-            // a whole-row block is contiguous: one row of nr*cols elements
-            if (nr * x.cols > INT32_MAX) {
-              delete plan;
-              return fail(VSF_ERR_OVERFLOW, "quantisation block larger than 2^31 elements");
-            }
-            add(x.offset + r * x.cols, 1, nr * x.cols, nr * x.cols, false, r, 0);
-          } else {
-            if (x.cols > INT32_MAX) {
-              delete plan;
-              return fail(VSF_ERR_OVERFLOW, "row longer than 2^31 elements");
-            }
-            if (x.rows > INT32_MAX) {
-              delete plan;
-              return fail(VSF_ERR_OVERFLOW, "more than 2^31 rows");
-            }
-            add(x.offset + r * x.cols + c, nr, nc, x.cols, false, r, c);
-          }
+          const Dest dest = i < grouped ? (i % k == 0 ? kTmaTile : kTmaTileMember) : kRegister;
+          add(x.offset + r * x.cols + c, nr, nc, x.cols, dest, r, c);
         }
       }
     }
@@ -312,6 +321,7 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
   L.big = section(sizeof(int32_t) * std::max<size_t>(1, plan->big_blocks.size()));
   L.small = section(sizeof(int32_t) * std::max<size_t>(1, plan->small_blocks.size()));
   L.tma = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_blocks.size()));
+  L.tma_k = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_tiles.size()));
   L.error = section(16);
   L.spans = section(sizeof(vsf::CopySpan) * (vsf::kMaxCopyGrid + 1));
   L.partials = section(sizeof(double) * vsf::kMaxCopyGrid);

@@ -50,10 +50,14 @@ struct CopySpan {
 
 // Tile tensors whose full tiles the bulk-copy kernel reads with 2-D tensor
 // copies (one tensor map per array and tensor, encoded per call).
+// A work unit of that kernel is k adjacent full tiles of one stripe, read
+// together as one box of k * tile_cols (<= 256) columns.
 constexpr int kMaxTileMaps = 16;
+constexpr int kMaxUnitTiles = 8;
 struct TileMapInfo {
   int32_t tensor;
-  int32_t box_cols, box_rows;  // one copy = box_rows rows of box_cols elements
+  int32_t tile_cols, k;        // tile width; tiles per work unit
+  int32_t box_cols, box_rows;  // one copy = box_rows rows of box_cols = k * tile_cols elements
   int64_t rows, cols, offset;  // the tensor's 2-D view inside the buffer
 };
 
@@ -69,6 +73,7 @@ struct DeviceLayout {
   size_t tensor_off = 0, tensor_numel = 0;  // int64[n] each
   size_t qblocks = 0;                       // QBlock[n_qblocks]
   size_t big = 0, small = 0, tma = 0;       // int32 lists of block indices
+  size_t tma_k = 0;                         // int32 tiles per TMA work unit
   size_t error = 0;                         // uint32 device error word
   size_t spans = 0;                         // CopySpan[kMaxCopyGrid + 1]
   size_t partials = 0;                      // double[kMaxCopyGrid]
@@ -85,7 +90,8 @@ struct vsf_plan {
   std::vector<vsf::TensorInfo> tensors;
   std::vector<vsf::QBlock> qblocks;
   std::vector<int32_t> big_blocks;    // ROWS / TILE blocks: register block kernel
-  std::vector<int32_t> tma_blocks;    // contiguous, 16-aligned blocks and full tiles: TMA kernel
+  std::vector<int32_t> tma_blocks;    // TMA kernel work units: first block of each
+  std::vector<int32_t> tma_tiles;     // tiles per unit (1 for a contiguous block)
   std::vector<vsf::TileMapInfo> tile_maps;
   std::vector<int32_t> small_blocks;  // ELEM chunks: warp kernel
   int64_t max_big_elems = 0;

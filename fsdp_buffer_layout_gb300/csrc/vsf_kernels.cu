@@ -421,7 +421,8 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
                               master, &maps);
     if (ms != VSF_OK) return ms;
     cudaError_t e = cudaLaunchKernelEx(
-        &cfg, adam_tma_kernel<GT>, maps, qb, ws_ptr<int32_t>(plan, plan->layout.tma), ntma, ncl, g,
+        &cfg, adam_tma_kernel<GT>, maps, qb, ws_ptr<int32_t>(plan, plan->layout.tma),
+        ws_ptr<int32_t>(plan, plan->layout.tma_k), ntma, ncl, g,
         d_factor, master, mq, vq, m_scale, v_scale, bf, k,
         reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error));
     if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (bulk-copy blocks)");
@@ -576,8 +577,10 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     std::memcpy(&img[L.big], plan->big_blocks.data(), 4 * plan->big_blocks.size());
   if (!plan->small_blocks.empty())
     std::memcpy(&img[L.small], plan->small_blocks.data(), 4 * plan->small_blocks.size());
-  if (!plan->tma_blocks.empty())
+  if (!plan->tma_blocks.empty()) {
     std::memcpy(&img[L.tma], plan->tma_blocks.data(), 4 * plan->tma_blocks.size());
+    std::memcpy(&img[L.tma_k], plan->tma_tiles.data(), 4 * plan->tma_tiles.size());
+  }
   std::memcpy(&img[L.spans], spans.data(), sizeof(CopySpan) * spans.size());
 
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
