@@ -36,8 +36,15 @@ METRIC = "fused shard-step HBM GB/s and params/s vs GB300 HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algorithmic_bytes(n_real: int, n_qblocks: int, grad_bytes: int = 2) -> dict:
+def algorithmic_bytes(n_real: int, n_qblocks: int, grad_bytes: int = 2,
+                      zero_copy: bool = False) -> dict:
+    """Bytes the step must move per real element. Zero-copy mode (gradients
+    and parameters are views of the packed buffers) drops copy-in and
+    copy-out; its group norm reads the packed gradient once instead."""
     adam = n_real * (grad_bytes + 1 + 1 + 4 + 1 + 1 + 4 + 2) + 16 * n_qblocks
+    if zero_copy:
+        return dict(pack=n_real * grad_bytes, adam=adam, unpack=0,
+                    step=n_real * grad_bytes + adam)
     return dict(pack=n_real * 2 * grad_bytes, adam=adam, unpack=n_real * 4,
                 step=n_real * 2 * grad_bytes + adam + n_real * 4)
 
@@ -171,7 +178,7 @@ def gpu_arm(args, rank: int, world: int):
     stream = torch.cuda.Stream(dev)
     ss = ShardStep(specs, w.m, w.g_coll, max_norm=w.max_norm, stream=stream)
     n_real, nq = ss.info.real, ss.info.n_qblocks
-    nbytes = algorithmic_bytes(n_real, nq)
+    nbytes = algorithmic_bytes(n_real, nq, zero_copy=args.zero_copy)
 
     # Per-tensor gradients and parameters, 16-byte aligned views of one buffer.
     starts, cur = [], 0
@@ -189,10 +196,16 @@ def gpu_arm(args, rank: int, world: int):
     host_norm = torch.empty(2, dtype=torch.float64).pin_memory()
     grads = [dev_g[s:s + n] for s, n in zip(starts, ss.numels)]
     params = [dev_p[s:s + n] for s, n in zip(starts, ss.numels)]
+    if args.zero_copy:
+        # gradients and parameters live in the packed buffers (address map)
+        gviews = ss.views(ss.packed_grad.view(torch.int16))
+        pviews = ss.views(ss.packed_bf16.view(torch.int16))
+        for v, g in zip(gviews, grads):
+            v.copy_(g)
     torch.cuda.synchronize(dev)
 
-    launches_per_step = 2 + 1 + (1 if any(t.gran != W.GRAN_ELEM for t in w.tensors) else 0) + \
-        (1 if any(t.gran == W.GRAN_ELEM for t in w.tensors) else 0)
+    # pack (or norm pass) + norm finalize + AdamW kernels (+ unpack)
+    launches_per_step = (2 if args.zero_copy else 3) + ss.adam_launches()
     step = 0
 
     def one_step(ev=None):
@@ -200,14 +213,18 @@ def gpu_arm(args, rank: int, world: int):
         step += 1
         if ev is not None:
             ev[0].record(stream)
-        ss.pack(grads)
-        ss.group_norm_scale()
+        if args.zero_copy:
+            ss.group_norm_scale(standalone=True)
+        else:
+            ss.pack(grads)
+            ss.group_norm_scale()
         if ev is not None:
             ev[1].record(stream)
         ss.adam(step)
         if ev is not None:
             ev[2].record(stream)
-        ss.unpack(params)
+        if not args.zero_copy:
+            ss.unpack(params)
         if ev is not None:
             ev[3].record(stream)
 
@@ -260,9 +277,17 @@ def gpu_arm(args, rank: int, world: int):
     with torch.cuda.stream(stream):
         e_start.record(stream)
         for _ in range(e2e_steps):
-            dev_g.copy_(host_g, non_blocking=True)
+            if args.zero_copy:
+                for v, s0, n in zip(gviews, starts, ss.numels):
+                    v.copy_(host_g[s0:s0 + n], non_blocking=True)
+            else:
+                dev_g.copy_(host_g, non_blocking=True)
             one_step()
-            host_p.copy_(dev_p, non_blocking=True)
+            if args.zero_copy:
+                for v, s0, n in zip(pviews, starts, ss.numels):
+                    host_p[s0:s0 + n].copy_(v, non_blocking=True)
+            else:
+                host_p.copy_(dev_p, non_blocking=True)
             host_norm.copy_(ss.norm, non_blocking=True)
         e_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -287,12 +312,15 @@ def gpu_arm(args, rank: int, world: int):
                    "bytes_per_step": nbytes["step"],
                    "l2": f"inputs larger than L2 ({nbytes['step'] / 1e9:.2f} GB per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU, m virtual ranks",
+                   "mode": "zero-copy views (no copy-in/out)" if args.zero_copy
+                   else "copy-in / copy-out",
                    "kernel_ms": {"pack+norm": round(k_pack, 5), "adam8": round(k_adam, 5),
                                  "unpack": round(k_unpack, 5)},
                    "frac_of_peak_step": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(adam_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(adam_gbs / peak, 4),
-                     "traffic": TRAFFIC.get(w.name), "kernel": "vsf_adam8_step",
+                     "traffic": TRAFFIC.get(w.name), "traffic_unit": "bytes per launch",
+                     "kernel": "vsf_adam8_step",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": round(nbytes["step"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -305,10 +333,13 @@ def gpu_arm(args, rank: int, world: int):
     return line
 
 
-# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# AdamW launch, from the ncu capture summarised in profiles/; None until taken
-# for the current kernel.
-TRAFFIC: dict = {}
+# Per-launch DRAM traffic in bytes (dram__bytes_read.sum + dram__bytes_write.sum)
+# of the AdamW bulk-copy kernel, from the ncu captures summarised in profiles/
+# (adam8_tma_*.md); a workload without a capture of the current kernel is None.
+TRAFFIC: dict = {
+    "llama_layer": 1.731780e9 + 1.547427e9,
+    "dsv3_block": 2.115067e9 + 2.040661e9,
+}
 
 
 def reference_arm(args):
@@ -346,6 +377,8 @@ def main():
     ap.add_argument("--impl", default="vsf", choices=["vsf", "reference"])
     ap.add_argument("--workload", default="llama_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--zero-copy", action="store_true",
+                    help="gradients/params as views of the packed buffers (no pack/unpack)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -348,6 +348,9 @@ vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info) {
   info->padding_ratio = 1.0 - (double)plan->real / (double)plan->total;
   info->plan_seconds = plan->plan_seconds;
   info->order_used = plan->order_used;
+  info->n_bulk_units = (int64_t)plan->tma_blocks.size();
+  info->n_register_blocks = (int64_t)plan->big_blocks.size();
+  info->n_element_chunks = (int64_t)plan->small_blocks.size();
   return VSF_OK;
 }
 
@@ -406,6 +409,18 @@ vsf_status vsf_plan_rank_slices(const vsf_plan* plan, int32_t rank, int32_t capa
 vsf_status vsf_plan_device_error_offset(const vsf_plan* plan, size_t* offset) {
   if (plan == nullptr || offset == nullptr) return fail(VSF_ERR_ARG, "NULL argument");
   *offset = plan->layout.error;
+  return VSF_OK;
+}
+
+vsf_status vsf_plan_views(const vsf_plan* plan, const void* packed, int32_t elem_bytes,
+                          void** views) {
+  if (plan == nullptr || packed == nullptr || views == nullptr)
+    return fail(VSF_ERR_ARG, "vsf_plan_views: NULL argument");
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4)
+    return fail(VSF_ERR_ARG, "vsf_plan_views: elem_bytes must be 1, 2 or 4");
+  for (int t = 0; t < plan->n; ++t)
+    views[t] = const_cast<char*>(static_cast<const char*>(packed)) +
+               plan->tensors[t].offset * (int64_t)elem_bytes;
   return VSF_OK;
 }
 

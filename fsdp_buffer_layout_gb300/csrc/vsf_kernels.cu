@@ -226,6 +226,33 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __rest
 #include "adam8.cuh"
 #include "adam8_tma.cuh"
 
+// Fused group ops over every real element of a packed buffer (all tensors
+// in one launch, over the copy spans): 0 zero, 1 scale by alpha, 2 add src.
+// fp32 arithmetic with one rounding, then the buffer's type (bf16 RNE).
+template <typename DT, typename ST, int kOp>
+__global__ void __launch_bounds__(kCopyThreads) group_op_kernel(
+    const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_numel,
+    const CopySpan* __restrict__ spans, DT* dst, const ST* __restrict__ src, float alpha) {
+  const CopySpan s0 = spans[blockIdx.x];
+  const CopySpan s1 = spans[blockIdx.x + 1];
+  for (int t = s0.tensor; t <= s1.tensor; ++t) {
+    const int64_t b = (t == s0.tensor) ? s0.elem : 0;
+    const int64_t e = (t == s1.tensor) ? s1.elem : t_numel[t];
+    const int64_t base = t_off[t];
+    for (int64_t i = b + threadIdx.x; i < e; i += kCopyThreads) {
+      const int64_t x = base + i;
+      float r = 0.0f;
+      if (kOp == 1) r = __fmul_rn(elem_f32(dst[x]), alpha);
+      if (kOp == 2) r = __fadd_rn(elem_f32(dst[x]), elem_f32(src[x]));
+      if constexpr (sizeof(DT) == 2)
+        dst[x] = (DT)bf16_bits(r);
+      else
+        dst[x] = r;
+    }
+  }
+}
+
+
 // ------------------------------------------------------------------ host side
 
 vsf_status cuda_fail(cudaError_t e, const char* what) {
@@ -675,6 +702,71 @@ vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* c
   return launch_copy<uint16_t, kUnpack>(plan, const_cast<const void* const*>(params),
                                         const_cast<uint16_t*>(packed_bf16),
                                         static_cast<cudaStream_t>(stream), "vsf_unpack");
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ fused group ops
+
+namespace vsf {
+namespace {
+
+template <typename DT, typename ST, int kOp>
+vsf_status launch_group(const vsf_plan* plan, void* dst, const void* src, float alpha,
+                        cudaStream_t st, const char* who) {
+  group_op_kernel<DT, ST, kOp><<<plan->copy_grid, kCopyThreads, 0, st>>>(
+      ws_ptr<int64_t>(plan, plan->layout.tensor_off),
+      ws_ptr<int64_t>(plan, plan->layout.tensor_numel),
+      ws_ptr<CopySpan>(plan, plan->layout.spans), static_cast<DT*>(dst),
+      static_cast<const ST*>(src), alpha);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : cuda_fail(e, who);
+}
+
+}  // namespace
+}  // namespace vsf
+
+extern "C" {
+
+vsf_status vsf_group_zero(const vsf_plan* plan, void* buf, int32_t dtype, void* stream) {
+  using namespace vsf;
+  vsf_status s = check_ready(plan, "vsf_group_zero");
+  if (s != VSF_OK) return s;
+  if (buf == nullptr) return fail(VSF_ERR_ARG, "vsf_group_zero: NULL buffer");
+  if (misaligned(buf)) return fail(VSF_ERR_ALIGN, "vsf_group_zero: alignment");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == VSF_BF16) return launch_group<uint16_t, uint16_t, 0>(plan, buf, nullptr, 0.f, st, "vsf_group_zero");
+  if (dtype == VSF_FP32) return launch_group<float, float, 0>(plan, buf, nullptr, 0.f, st, "vsf_group_zero");
+  return fail(VSF_ERR_ARG, "vsf_group_zero: dtype must be VSF_BF16 or VSF_FP32");
+}
+
+vsf_status vsf_group_scale(const vsf_plan* plan, void* buf, int32_t dtype, float alpha,
+                           void* stream) {
+  using namespace vsf;
+  vsf_status s = check_ready(plan, "vsf_group_scale");
+  if (s != VSF_OK) return s;
+  if (buf == nullptr) return fail(VSF_ERR_ARG, "vsf_group_scale: NULL buffer");
+  if (misaligned(buf)) return fail(VSF_ERR_ALIGN, "vsf_group_scale: alignment");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == VSF_BF16) return launch_group<uint16_t, uint16_t, 1>(plan, buf, nullptr, alpha, st, "vsf_group_scale");
+  if (dtype == VSF_FP32) return launch_group<float, float, 1>(plan, buf, nullptr, alpha, st, "vsf_group_scale");
+  return fail(VSF_ERR_ARG, "vsf_group_scale: dtype must be VSF_BF16 or VSF_FP32");
+}
+
+vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, const void* src,
+                         int32_t src_dtype, void* stream) {
+  using namespace vsf;
+  vsf_status s = check_ready(plan, "vsf_group_add");
+  if (s != VSF_OK) return s;
+  if (dst == nullptr || src == nullptr) return fail(VSF_ERR_ARG, "vsf_group_add: NULL buffer");
+  if (misaligned(dst) || misaligned(src)) return fail(VSF_ERR_ALIGN, "vsf_group_add: alignment");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* who = "vsf_group_add";
+  if (dst_dtype == VSF_BF16 && src_dtype == VSF_BF16) return launch_group<uint16_t, uint16_t, 2>(plan, dst, src, 0.f, st, who);
+  if (dst_dtype == VSF_FP32 && src_dtype == VSF_BF16) return launch_group<float, uint16_t, 2>(plan, dst, src, 0.f, st, who);
+  if (dst_dtype == VSF_FP32 && src_dtype == VSF_FP32) return launch_group<float, float, 2>(plan, dst, src, 0.f, st, who);
+  if (dst_dtype == VSF_BF16 && src_dtype == VSF_FP32) return launch_group<uint16_t, float, 2>(plan, dst, src, 0.f, st, who);
+  return fail(VSF_ERR_ARG, "vsf_group_add: dtypes must be VSF_BF16 or VSF_FP32");
 }
 
 }  // extern "C"

@@ -98,6 +98,28 @@ class ShardStep:
         V.vsf_unpack(self.plan, self.packed_bf16.data_ptr(), [p.data_ptr() for p in params],
                      self.stream.cuda_stream)
 
+    def adam_launches(self) -> int:
+        """Kernels one vsf_adam8_step launches for this plan (quantised mode)."""
+        i = self.info
+        return sum(1 for c in (i.n_bulk_units, i.n_register_blocks, i.n_element_chunks) if c > 0)
+
+    def views(self, buf: torch.Tensor):
+        """Per-tensor views into a packed buffer (the persistent address map):
+        writing a view writes the buffer, so pack and unpack become no-ops."""
+        ptrs = V.vsf_plan_views(self.plan, buf.data_ptr(), buf.element_size(), len(self.numels))
+        out = []
+        for p, o, n in zip(ptrs, self.offsets, self.numels):
+            v = buf[o:o + n]
+            assert v.data_ptr() == p
+            out.append(v)
+        return out
+
+    def zero_copy_step(self, step: int):
+        """One step when gradients and parameters are views of the packed
+        buffers: group norm/scale on the packed gradient, then AdamW."""
+        self.group_norm_scale(standalone=True)
+        self.adam(step)
+
     def step(self, grads, params, step: int):
         """pack -> group norm/scale -> 8-bit AdamW -> unpack."""
         self.pack(grads)

@@ -42,7 +42,9 @@ class vsf_plan_info(ctypes.Structure):
                 ("n_qblocks", ctypes.c_int64), ("n_tensors", ctypes.c_int32),
                 ("m", ctypes.c_int32), ("g_coll", ctypes.c_int64),
                 ("padding_ratio", ctypes.c_double), ("plan_seconds", ctypes.c_double),
-                ("order_used", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("order_used", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n_bulk_units", ctypes.c_int64), ("n_register_blocks", ctypes.c_int64),
+                ("n_element_chunks", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -91,6 +93,17 @@ def lib():
                                          P(vsf_adam_hparams), i32, vp]
             L.vsf_unpack.restype = st
             L.vsf_unpack.argtypes = [vp, vp, P(vp), vp]
+            L.vsf_group_zero.restype = st
+            L.vsf_group_zero.argtypes = [vp, vp, i32, vp]
+            L.vsf_group_scale.restype = st
+            L.vsf_group_scale.argtypes = [vp, vp, i32, ctypes.c_float, vp]
+            L.vsf_group_add.restype = st
+            L.vsf_group_add.argtypes = [vp, vp, i32, vp, i32, vp]
+            L.vsf_plan_views.restype = st
+            L.vsf_plan_views.argtypes = [vp, vp, i32, P(vp)]
+            L.vsf_group_norm_scale_static.restype = st
+            L.vsf_group_norm_scale_static.argtypes = [P(vp), vp, i32, i32, P(vsf_adam_hparams),
+                                                      vp, vp, vp]
             L.vsf_status_string.restype = ctypes.c_char_p
             L.vsf_status_string.argtypes = [st]
             L.vsf_last_error.restype = ctypes.c_char_p
@@ -200,6 +213,33 @@ def vsf_adam8_step(plan: int, packed_grad: int, grad_dtype: int, d_factor: int, 
 
 def vsf_unpack(plan: int, packed_bf16: int, params, stream: int) -> None:
     _check(lib().vsf_unpack(plan, packed_bf16, _ptr_array(params), stream))
+
+
+def vsf_group_zero(plan: int, buf: int, dtype: int, stream: int) -> None:
+    _check(lib().vsf_group_zero(plan, buf, dtype, stream))
+
+
+def vsf_group_scale(plan: int, buf: int, dtype: int, alpha: float, stream: int) -> None:
+    _check(lib().vsf_group_scale(plan, buf, dtype, alpha, stream))
+
+
+def vsf_group_add(plan: int, dst: int, dst_dtype: int, src: int, src_dtype: int,
+                  stream: int) -> None:
+    _check(lib().vsf_group_add(plan, dst, dst_dtype, src, src_dtype, stream))
+
+
+def vsf_plan_views(plan: int, packed: int, elem_bytes: int, n: int):
+    out = (ctypes.c_void_p * n)()
+    _check(lib().vsf_plan_views(plan, packed, elem_bytes, out))
+    return [int(x or 0) for x in out]
+
+
+def vsf_group_norm_scale_static(grads, numel, dtype: int, hp: vsf_adam_hparams, d_factor: int,
+                                d_norm, stream) -> None:
+    arr = _ptr_array(grads)
+    n = (ctypes.c_int64 * len(numel))(*[int(x) for x in numel])
+    _check(lib().vsf_group_norm_scale_static(arr, n, len(grads), dtype, ctypes.byref(hp),
+                                             d_factor, d_norm, stream))
 
 
 def vsf_status_string(status: int) -> str:

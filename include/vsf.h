@@ -97,6 +97,10 @@ typedef struct {
   double plan_seconds;   /* host time spent in vsf_plan_create */
   int32_t order_used;    /* VSF_ORDER_* actually chosen */
   int32_t reserved;
+  /* how vsf_adam8_step splits the blocks (each non-zero count is one launch):
+   * bulk-copy work units (contiguous blocks, or k full tiles), blocks of the
+   * register kernel (ragged or unaligned), element-granular chunks */
+  int64_t n_bulk_units, n_register_blocks, n_element_chunks;
 } vsf_plan_info;
 
 typedef struct vsf_plan vsf_plan; /* opaque */
@@ -133,6 +137,16 @@ vsf_status vsf_plan_qblocks(const vsf_plan* plan, int32_t* tensor, int64_t* base
 vsf_status vsf_plan_rank_slices(const vsf_plan* plan, int32_t rank, int32_t capacity,
                                 int32_t* count, int32_t* tensor, int64_t* elem_begin,
                                 int64_t* elem_end, int64_t* atom_begin, int64_t* atom_end);
+
+/* The persistent address map ([VSF] 核心方法 › Distributed Buffer: zero-copy
+ * access to every parameter's data around the collectives): views[t] =
+ * packed + offset_t * elem_bytes, for a packed buffer of 1-, 2- or 4-byte
+ * elements. A caller that lets its per-tensor gradients and parameters BE
+ * these views (zero-copy mode) skips vsf_pack and vsf_unpack: one step is
+ * then vsf_group_norm_scale on the packed gradient and vsf_adam8_step. Host
+ * pointer arithmetic only. */
+vsf_status vsf_plan_views(const vsf_plan* plan, const void* packed, int32_t elem_bytes,
+                          void** views);
 
 /* Bytes of device workspace the caller must provide to vsf_plan_upload. */
 size_t vsf_plan_workspace_bytes(const vsf_plan* plan);
@@ -199,6 +213,22 @@ vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t
  * device pointers (bf16, 16-byte aligned). */
 vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* const* params,
                       void* stream);
+
+/* Fused group ops ([VSF] 核心方法 › Distributed Buffer: the same
+ * element-wise kernel applied to every tensor of the buffer in one launch,
+ * e.g. zero_grad and gradient accumulation). They touch every real element
+ * of the m*S packed buffer(s) and never the padding. Arithmetic in fp32 with
+ * one rounding, then the destination type (bf16: round half to even).
+ *   vsf_group_zero:  buf = 0
+ *   vsf_group_scale: buf = buf * alpha
+ *   vsf_group_add:   dst = dst + src (gradient accumulation; any mix of
+ *                    VSF_BF16 / VSF_FP32 destination and source)
+ * Buffers are device pointers, 16-byte aligned, of m*S elements. */
+vsf_status vsf_group_zero(const vsf_plan* plan, void* buf, int32_t dtype, void* stream);
+vsf_status vsf_group_scale(const vsf_plan* plan, void* buf, int32_t dtype, float alpha,
+                           void* stream);
+vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, const void* src,
+                         int32_t src_dtype, void* stream);
 
 /* Group norm and scale WITHOUT any device allocation or workspace. The pages
  * have no counterpart: this entry point exists for callers that cannot

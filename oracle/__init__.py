@@ -73,6 +73,8 @@ def lib():
                                        vp, vp, vp, vp, vp, vp, dbl, dbl, dbl, dbl, dbl, c_int]
             L.orc_quantize_m.argtypes = [i64, vp, vp, vp, vp]
             L.orc_quantize_v.argtypes = [i64, vp, vp, vp, vp]
+            L.orc_group_op.restype = None
+            L.orc_group_op.argtypes = [c_int, c_int, vp, vp, vp, c_int, vp, c_int, ctypes.c_float]
             L.orc_bf16_round.restype = ctypes.c_uint16
             L.orc_bf16_round.argtypes = [ctypes.c_float]
             _lib = L
@@ -226,6 +228,15 @@ def quantize_v(x):
     s = np.zeros(1, np.float32)
     lib().orc_quantize_v(x.size, _p(x), _p(codes), _p(s), _p(deq))
     return codes, float(s[0]), deq
+
+
+def group_op(op: int, numels, offsets, dst, src=None, alpha: float = 1.0):
+    """In place on dst (uint16 bf16 bits or float32): 0 zero, 1 scale, 2 add."""
+    numel = np.array(numels, np.int64)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    lib().orc_group_op(op, len(numel), _p(numel), _p(off), _p(dst), int(dst.dtype == np.uint16),
+                       _p(src), int(src is not None and src.dtype == np.uint16), alpha)
+    return dst
 
 
 def bf16_round(x: float) -> int:

@@ -458,6 +458,35 @@ void orc_unpack(int n, void* const* tensors, const int64_t* numel, const int64_t
   }
 }
 
+// ---------------------------------------------------------------- fused group ops
+
+// One element-wise group op over every real element of a packed buffer, all
+// tensors at once ([VSF] 核心方法 › Distributed Buffer: add / scale / zero
+// applied across tensors). op 0: dst = 0; op 1: dst = dst * alpha; op 2:
+// dst = dst + src. Arithmetic in fp32, one rounding, then to the buffer type
+// (bf16 round-half-even for bf16 buffers). Padding is left as it is.
+void orc_group_op(int op, int n, const int64_t* numel, const int64_t* offsets, void* dst,
+                  int dst_bf16, const void* src, int src_bf16, float alpha) {
+  for (int t = 0; t < n; ++t) {
+    for (int64_t i = 0; i < numel[t]; ++i) {
+      const int64_t e = offsets[t] + i;
+      const float d = dst_bf16 ? bf16_value(static_cast<uint16_t*>(dst)[e])
+                               : static_cast<float*>(dst)[e];
+      float r = 0.0f;
+      if (op == 1) r = d * alpha;
+      if (op == 2) {
+        const float x = src_bf16 ? bf16_value(static_cast<const uint16_t*>(src)[e])
+                                 : static_cast<const float*>(src)[e];
+        r = d + x;
+      }
+      if (dst_bf16)
+        static_cast<uint16_t*>(dst)[e] = bf16_round(r);
+      else
+        static_cast<float*>(dst)[e] = r;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- group norm and scale
 
 // Sum of squares of every real gradient element, in fp64, tensors in order,

@@ -287,3 +287,40 @@ def test_adam_all_matches_blockwise():
                                                   m_scale=0.0, v_scale=0.0), 1, HP)
     assert np.array_equal(master[idx], one["p"]) and np.array_equal(mq[idx], one["mq"])
     assert ms[q] == one["m_scale"]
+
+
+# ---------------------------------------------------------------- fused group ops
+
+def test_group_ops_closed_forms():
+    """zero -> 0; x + (-x) -> 0; scale by 2 is exact; padding untouched."""
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal(64) * 1e-3).astype(np.float32)
+    buf = np.full(80, 7.0, np.float32)
+    buf[3:3 + 64] = x
+    oracle.group_op(1, [64], [3], buf, alpha=2.0)
+    assert np.array_equal(buf[3:67], x * np.float32(2)) and buf[0] == 7 and buf[70] == 7
+    neg = np.zeros(80, np.float32)
+    neg[3:67] = -x * 2
+    oracle.group_op(2, [64], [3], buf, neg)
+    assert not buf[3:67].any() and buf[0] == 7
+    buf[3:67] = x
+    oracle.group_op(0, [64], [3], buf)
+    assert not buf[3:67].any() and buf[67:].tolist() == [7.0] * 13
+
+
+def test_group_add_bf16_matches_numpy_and_torch_rounding():
+    """bf16 accumulation: the fp32 sum (numpy) rounded by torch's bf16 conversion."""
+    w = W.tiny()
+    a = W.grad(w, 1, 0, 0, 4096)
+    b = W.grad(w, 2, 0, 0, 4096)
+    dst = np.concatenate([np.zeros(5, np.uint16), a, np.zeros(3, np.uint16)])
+    src = np.concatenate([np.zeros(5, np.uint16), b, np.zeros(3, np.uint16)])
+    oracle.group_op(2, [4096], [5], dst, src)
+    s32 = synth.bf16_to_f32(a) + synth.bf16_to_f32(b)
+    want = torch.from_numpy(s32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(dst[5:5 + 4096], want)
+    # fp32 destination accumulating bf16: exact fp32 sums
+    acc = np.zeros(4096, np.float32)
+    oracle.group_op(2, [4096], [0], acc, a)
+    oracle.group_op(2, [4096], [0], acc, b)
+    assert np.array_equal(acc, s32)
