@@ -196,12 +196,17 @@ def gpu_arm(args, rank: int, world: int):
     host_norm = torch.empty(2, dtype=torch.float64).pin_memory()
     grads = [dev_g[s:s + n] for s, n in zip(starts, ss.numels)]
     params = [dev_p[s:s + n] for s, n in zip(starts, ss.numels)]
+    gviews = pviews = None
     if args.zero_copy:
         # gradients and parameters live in the packed buffers (address map)
         gviews = ss.views(ss.packed_grad.view(torch.int16))
         pviews = ss.views(ss.packed_bf16.view(torch.int16))
         for v, g in zip(gviews, grads):
             v.copy_(g)
+
+    def gviews_of(_buf):
+        # zero-copy mode has one packed gradient buffer: its views
+        return gviews
     torch.cuda.synchronize(dev)
 
     # pack (or norm pass) + norm finalize + AdamW kernels (+ unpack)
@@ -265,31 +270,67 @@ def gpu_arm(args, rank: int, world: int):
     k_adam = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     k_unpack = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
-    # End to end through the C ABI with host buffers: H2D of the step's
-    # gradients from pinned memory, the four calls, D2H of the parameters and
-    # of the norm, all inside the timed region.
+    # End to end through the C ABI with host buffers: every step copies its
+    # gradients in from pinned host memory and its bf16 parameters (and the
+    # norm) back out, inside the timed region. Steps are pipelined on three
+    # streams with two device buffer sets: the copy-in of step k+1 and the
+    # copy-out of step k-1 overlap the compute of step k.
     e2e_steps = max(3, min(args.steps, 100))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dev_g2 = [dev_g, torch.empty_like(dev_g)]
+    dev_p2 = [dev_p, torch.empty_like(dev_p)]
+    grads2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_g2]
+    params2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_p2]
+    host_norms = torch.empty(e2e_steps, 2, dtype=torch.float64).pin_memory()
+    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e_start.record(stream)
-        for _ in range(e2e_steps):
+    e_start.record(s_in)
+    s_out.wait_event(e_start)
+    stream.wait_event(e_start)
+    # buffer reuse distance: two device buffer sets, or the single packed
+    # buffers in zero-copy mode
+    dist_k = 1 if args.zero_copy else 2
+    for k in range(e2e_steps):
+        buf = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= dist_k:
+                s_in.wait_event(ev_done[k - dist_k])  # compute k-d has read this buffer
             if args.zero_copy:
-                for v, s0, n in zip(gviews, starts, ss.numels):
+                for v, s0, n in zip(gviews_of(buf), starts, ss.numels):
                     v.copy_(host_g[s0:s0 + n], non_blocking=True)
             else:
-                dev_g.copy_(host_g, non_blocking=True)
-            one_step()
+                dev_g2[buf].copy_(host_g, non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[k])
+            if k >= dist_k:
+                stream.wait_event(ev_out[k - dist_k])  # copy-out k-d has read this buffer
+            step += 1
+            if args.zero_copy:
+                ss.zero_copy_step(step)
+            else:
+                ss.pack(grads2[buf])
+                ss.group_norm_scale()
+                ss.adam(step)
+                ss.unpack(params2[buf])
+            host_norms[k].copy_(ss.norm, non_blocking=True)
+            ev_done[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[k])
             if args.zero_copy:
                 for v, s0, n in zip(pviews, starts, ss.numels):
                     host_p[s0:s0 + n].copy_(v, non_blocking=True)
             else:
-                host_p.copy_(dev_p, non_blocking=True)
-            host_norm.copy_(ss.norm, non_blocking=True)
-        e_end.record(stream)
+                host_p.copy_(dev_p2[buf], non_blocking=True)
+            ev_out[k].record(s_out)
+    s_out.wait_stream(stream)
+    e_end.record(s_out)
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
     if world > 1:
