@@ -100,7 +100,7 @@ std::vector<int> order_for(const std::vector<TensorInfo>& ts, int policy) {
 
 // Smallest feasible S for one order, or -1.
 int64_t scan_S(const std::vector<TensorInfo>& ts, const std::vector<int>& order, int64_t m,
-               int64_t g, int64_t real, int64_t* S_out_guard) {
+               int64_t g, int64_t real) {
   int64_t lb = round_up((real + m - 1) / m, g);
   // Everything aligned inside rank 0 always fits: an upper end for the scan.
   int64_t ub = 0;
@@ -109,13 +109,10 @@ int64_t scan_S(const std::vector<TensorInfo>& ts, const std::vector<int>& order,
   for (int64_t S = lb; S <= std::max(lb, ub); S += g) {
     if (place_all(ts, order, m, S, nullptr)) return S;
   }
-  (void)S_out_guard;
   return -1;
 }
 
 }  // namespace
-
-void set_error(const std::string& msg) { g_last_error = msg; }
 
 vsf_status fail(vsf_status s, const std::string& msg) {
   g_last_error = msg;
@@ -183,7 +180,7 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
   const int first = order == VSF_ORDER_BEST3 ? VSF_ORDER_DEFAULT : order;
   const int last = order == VSF_ORDER_BEST3 ? VSF_ORDER_SHAPE : order;
   for (int p = first; p <= last; ++p) {
-    int64_t S = vsf::scan_S(ts, vsf::order_for(ts, p), m, g_coll, real, nullptr);
+    int64_t S = vsf::scan_S(ts, vsf::order_for(ts, p), m, g_coll, real);
     if (S >= 0 && (best_S < 0 || S < best_S)) {
       best_S = S;
       used = p;

@@ -117,6 +117,5 @@ struct vsf_plan {
 };
 
 namespace vsf {
-void set_error(const std::string& msg);
 vsf_status fail(vsf_status s, const std::string& msg);
 }  // namespace vsf

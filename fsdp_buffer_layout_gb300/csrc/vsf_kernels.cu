@@ -56,13 +56,6 @@ struct TensorPtrs {
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
-__device__ __forceinline__ uint32_t f32_to_bf16(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;  // NaN -> canonical quiet NaN
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return u >> 16;
-}
-
 // Double-float accumulator of non-negative terms (Knuth's TwoSum keeps the
 // rounding error of every addition).
 struct DF {
