@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libvsf.so")
 BUILD = os.path.join(PKG, "_build")
 
-SOURCES = ["plan.cpp", "vsf_kernels.cu"]
+SOURCES = ["plan.cpp", "vsf_kernels.cu", "muon.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -61,7 +61,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, err in results:
             sys.stderr.write(err)
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-lcudart_static"]
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
+    cmd = [nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + [
+        "-lcudart_static", "-L" + cuda_lib, "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")

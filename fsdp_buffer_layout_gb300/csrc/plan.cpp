@@ -150,6 +150,8 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
       if (d.shape[k] < 1) return fail(VSF_ERR_ARG, "tensor " + std::to_string(t) + ": empty dim");
     for (int k = 0; k + 1 < d.ndim; ++k)
       if (!vsf::mul_ok(rows, d.shape[k], &rows)) return fail(VSF_ERR_OVERFLOW, "rows overflow");
+    x.ndim = d.ndim;
+    for (int k = 0; k < 8; ++k) x.shape[k] = k < d.ndim ? d.shape[k] : 1;
     x.rows = rows;
     x.cols = d.shape[d.ndim - 1];
     if (!vsf::mul_ok(x.rows, x.cols, &x.numel)) return fail(VSF_ERR_OVERFLOW, "numel overflow");

@@ -62,6 +62,8 @@ struct TileMapInfo {
 };
 
 struct TensorInfo {
+  int32_t ndim;
+  int64_t shape[8];
   int64_t rows, cols, numel;
   int32_t gran;
   int64_t block_rows, tile_cols;

@@ -98,6 +98,21 @@ class ShardStep:
         V.vsf_unpack(self.plan, self.packed_bf16.data_ptr(), [p.data_ptr() for p in params],
                      self.stream.cuda_stream)
 
+    def muon_step(self, hp=None):
+        """Distributed Muon on every matrix tensor (packed bf16 gradient in
+        self.packed_grad). Allocates the fp32 momentum buffer and the Muon
+        workspace on first use."""
+        if not hasattr(self, "momentum"):
+            with torch.cuda.device(self.device):
+                self.momentum = torch.zeros(self.info.total, dtype=torch.float32,
+                                            device=self.device)
+                self.muon_ws = torch.empty(V.vsf_muon_workspace_bytes(self.plan),
+                                           dtype=torch.uint8, device=self.device)
+        hp = V.make_muon_hparams() if hp is None else hp
+        V.vsf_muon_step(self.plan, self.packed_grad.data_ptr(), self.momentum.data_ptr(),
+                        self.master.data_ptr(), self.packed_bf16.data_ptr(), hp,
+                        self.muon_ws.data_ptr(), self.muon_ws.numel(), self.stream.cuda_stream)
+
     def adam_launches(self) -> int:
         """Kernels one vsf_adam8_step launches for this plan (quantised mode)."""
         i = self.info

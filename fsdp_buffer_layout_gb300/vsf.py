@@ -47,6 +47,13 @@ class vsf_plan_info(ctypes.Structure):
                 ("n_element_chunks", ctypes.c_int64)]
 
 
+class vsf_muon_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("momentum", ctypes.c_double),
+                ("weight_decay", ctypes.c_double), ("eps", ctypes.c_double),
+                ("ns_a", ctypes.c_double), ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
+                ("ns_steps", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -104,6 +111,13 @@ def lib():
             L.vsf_group_norm_scale_static.restype = st
             L.vsf_group_norm_scale_static.argtypes = [P(vp), vp, i32, i32, P(vsf_adam_hparams),
                                                       vp, vp, vp]
+            L.vsf_muon_select_roots.restype = st
+            L.vsf_muon_select_roots.argtypes = [vp, vp, P(ctypes.c_double)]
+            L.vsf_muon_workspace_bytes.restype = ctypes.c_size_t
+            L.vsf_muon_workspace_bytes.argtypes = [vp]
+            L.vsf_muon_step.restype = st
+            L.vsf_muon_step.argtypes = [vp, vp, vp, vp, vp, P(vsf_muon_hparams), vp,
+                                        ctypes.c_size_t, vp]
             L.vsf_status_string.restype = ctypes.c_char_p
             L.vsf_status_string.argtypes = [st]
             L.vsf_last_error.restype = ctypes.c_char_p
@@ -240,6 +254,28 @@ def vsf_group_norm_scale_static(grads, numel, dtype: int, hp: vsf_adam_hparams, 
     n = (ctypes.c_int64 * len(numel))(*[int(x) for x in numel])
     _check(lib().vsf_group_norm_scale_static(arr, n, len(grads), dtype, ctypes.byref(hp),
                                              d_factor, d_norm, stream))
+
+
+def make_muon_hparams(lr=0.02, momentum=0.95, weight_decay=0.01, eps=1e-7, ns_a=3.4445,
+                      ns_b=-4.7750, ns_c=2.0315, ns_steps=5) -> vsf_muon_hparams:
+    return vsf_muon_hparams(lr, momentum, weight_decay, eps, ns_a, ns_b, ns_c, ns_steps, 0)
+
+
+def vsf_muon_select_roots(plan: int, n: int):
+    roots = (ctypes.c_int32 * n)()
+    bal = ctypes.c_double()
+    _check(lib().vsf_muon_select_roots(plan, roots, ctypes.byref(bal)))
+    return list(roots), bal.value
+
+
+def vsf_muon_workspace_bytes(plan: int) -> int:
+    return int(lib().vsf_muon_workspace_bytes(plan))
+
+
+def vsf_muon_step(plan: int, packed_grad: int, momentum: int, master: int, packed_bf16: int,
+                  hp: vsf_muon_hparams, d_workspace: int, ws_bytes: int, stream: int) -> None:
+    _check(lib().vsf_muon_step(plan, packed_grad, momentum, master, packed_bf16, ctypes.byref(hp),
+                               d_workspace, ws_bytes, stream))
 
 
 def vsf_status_string(status: int) -> str:

@@ -230,6 +230,35 @@ vsf_status vsf_group_scale(const vsf_plan* plan, void* buf, int32_t dtype, float
 vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, const void* src,
                          int32_t src_dtype, void* stream);
 
+/* Distributed Muon ([VSF] 结构感知训练 case study › 分布式 Muon, Algorithm 2)
+ * on every matrix tensor of the plan (ndim >= 2; leading dims index a batch
+ * of matrices); 1-D tensors are left untouched.
+ *   SelectRoot: vsf_muon_select_roots gives each matrix tensor a root virtual
+ *   rank (longest-processing-time greedy over the Newton-Schulz FLOPs; -1 for
+ *   1-D tensors) and the max/mean root load.
+ *   Redistribute to the root and back is zero-copy here: a tensor is
+ *   contiguous in the buffer.
+ *   vsf_muon_step, per matrix, all in fp32 rounded once per operation except
+ *   the tensor-core products (bf16 operands, fp32 accumulation, bf16 results):
+ *     M = mu M + g;  U = g + mu M (Nesterov);
+ *     X = bf16(U * fp32(1 / (||U||_F + eps)));
+ *     ns_steps times: A = X X^T (R <= C) or X^T X (R > C); B = c A A + b A;
+ *                     X = a X + B X (R <= C) or a X + X B (R > C);
+ *     p = p (1 - lr wd) - fp32(lr sqrt(max(1, R/C))) X;  bf16 copy.
+ *   packed_grad: bf16, m*S; momentum: fp32, m*S (caller-zeroed before step
+ *   1); master: fp32; packed_bf16: out. d_workspace: vsf_muon_workspace_bytes
+ *   of caller memory (Newton-Schulz operands and the cuBLASLt workspace). */
+typedef struct {
+  double lr, momentum, weight_decay, eps, ns_a, ns_b, ns_c;
+  int32_t ns_steps, reserved;
+} vsf_muon_hparams;
+
+vsf_status vsf_muon_select_roots(const vsf_plan* plan, int32_t* root, double* load_balance);
+size_t vsf_muon_workspace_bytes(const vsf_plan* plan);
+vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
+                         float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
+                         void* d_workspace, size_t ws_bytes, void* stream);
+
 /* Group norm and scale WITHOUT any device allocation or workspace. The pages
  * have no counterpart: this entry point exists for callers that cannot
  * allocate device memory where they need the gradient norm, such as a hook

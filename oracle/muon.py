@@ -73,9 +73,11 @@ def scalar_quintic(s, steps: int = 5, coeffs=NS_COEFFS):
     return s
 
 
-def muon_matrix(g, M, p, step_hp):
+def muon_matrix(g, M, p, step_hp, exact: bool = False):
     """One Muon step on one R x C matrix. g: bf16 values (fp32 array), M:
-    fp32 momentum, p: fp32 master. Returns (M, p, bf16 bits, O)."""
+    fp32 momentum, p: fp32 master. Returns (M, p, bf16 bits, O). exact=True
+    runs the Newton-Schulz iteration without its bf16 rounding (same X0): the
+    distance between the two is the rounding noise of the bf16 iteration."""
     mu = np.float32(step_hp["momentum"])
     R, C = g.shape
     M = (mu * M + g).astype(np.float32)
@@ -84,7 +86,7 @@ def muon_matrix(g, M, p, step_hp):
     r = np.float32(1.0 / (s + step_hp["eps"]))
     X0 = bf16_from_f32((U * r).astype(np.float32)).astype(np.float64)
     O = newton_schulz(X0, step_hp["ns_steps"], (step_hp["ns_a"], step_hp["ns_b"],
-                                                step_hp["ns_c"])).astype(np.float32)
+                                                step_hp["ns_c"]), exact).astype(np.float32)
     decay = np.float32(1.0 - step_hp["lr"] * step_hp["weight_decay"])
     alpha = np.float32(step_hp["lr"] * math.sqrt(max(1.0, R / C)))
     p = (p * decay).astype(np.float32)
