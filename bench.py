@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused shard-step HBM GB/s and params/s vs GB300 HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+MUON_METRIC = "distributed Muon step Newton-Schulz TFLOP/s vs GB300 bf16 tensor roofline"
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def algorithmic_bytes(n_real: int, n_qblocks: int, grad_bytes: int = 2,
@@ -56,6 +58,30 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_peak(sustained: bool):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(path) as f:
+            return float(json.load(f)[key]), f"measured (MEASURED_PEAKS.json {key})"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+
+
+def muon_flops(w, ns_steps: int = 5) -> float:
+    """Newton-Schulz FLOPs of one Muon step over every matrix tensor of w
+    (per iteration 2 n^2 k for the Gram matrix, 2 n^3 for its square,
+    2 n^2 k for the product with X; n = min(R, C), k = max(R, C))."""
+    total = 0.0
+    for t in w.tensors:
+        if len(t.shape) < 2:
+            continue
+        *lead, R, C = t.shape
+        n, k = min(R, C), max(R, C)
+        total += float(np.prod(lead, dtype=np.float64)) * (4.0 * n * n * k + 2.0 * n ** 3)
+    return total * ns_steps
 
 
 def sample_workload(w, fraction: float):
@@ -374,6 +400,204 @@ def gpu_arm(args, rank: int, world: int):
     return line
 
 
+def muon_arm(args, rank: int, world: int):
+    """One Muon step = copy-in of the per-tensor gradients, vsf_muon_step
+    (momentum, per-matrix norm, bf16 normalisation, 5 Newton-Schulz
+    iterations of 3 GEMMs, update of master and bf16 copy), copy-out."""
+    import torch
+    import torch.distributed as dist
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    from synth import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.get(args.workload)
+    specs = [TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
+    stream = torch.cuda.Stream(dev)
+    ss = ShardStep(specs, w.m, w.g_coll, stream=stream)
+    n_real = ss.info.real
+    flops = muon_flops(w)
+    starts, cur = [], 0
+    for n in ss.numels:
+        starts.append(cur)
+        cur += (n + 7) // 8 * 8
+    host_g = torch.empty(cur, dtype=torch.int16).pin_memory()
+    hg = host_g.numpy().view(np.uint16)
+    for t, n in enumerate(ss.numels):
+        W.grad(w, 1, t, out=hg[starts[t]:starts[t] + n])
+        ss.load_master(t, torch.from_numpy(W.master_init(w, t)).to(dev))
+    dev_g = host_g.to(dev)
+    dev_p = torch.empty(cur, dtype=torch.int16, device=dev)
+    host_p = torch.empty(cur, dtype=torch.int16).pin_memory()
+    grads = [dev_g[s0:s0 + n] for s0, n in zip(starts, ss.numels)]
+    params = [dev_p[s0:s0 + n] for s0, n in zip(starts, ss.numels)]
+    n_mats = sum(1 for t in w.tensors if len(t.shape) >= 2)
+    roots, balance = ss.muon_roots()
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ss.pack(grads)
+        if ev is not None:
+            ev[1].record(stream)
+        ss.muon_step()
+        if ev is not None:
+            ev[2].record(stream)
+        ss.unpack(params)
+        if ev is not None:
+            ev[3].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    torch.cuda.synchronize(dev)
+    if ss.device_error():
+        raise RuntimeError("device error word set")
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id  # type: ignore[attr-defined]
+    except Exception:
+        bus = None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(bus)
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            one_step(evs[i])
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    k_muon = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    k_copy = statistics.mean(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs)
+
+    # End to end with host buffers: every step copies its gradients in from
+    # pinned host memory and its bf16 parameters back out, inside the timed
+    # region; copy-in of step k+1 and copy-out of step k-1 overlap the compute
+    # of step k (three streams, two device buffer sets).
+    e2e_steps = max(3, min(args.steps, 20))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dev_g2 = [dev_g, torch.empty_like(dev_g)]
+    dev_p2 = [dev_p, torch.empty_like(dev_p)]
+    grads2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_g2]
+    params2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_p2]
+    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e_start.record(s_in)
+    s_out.wait_event(e_start)
+    stream.wait_event(e_start)
+    for k in range(e2e_steps):
+        buf = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_done[k - 2])
+            dev_g2[buf].copy_(host_g, non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[k])
+            if k >= 2:
+                stream.wait_event(ev_out[k - 2])
+            ss.pack(grads2[buf])
+            ss.muon_step()
+            ss.unpack(params2[buf])
+            ev_done[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[k])
+            host_p.copy_(dev_p2[buf], non_blocking=True)
+            ev_out[k].record(s_out)
+    s_out.wait_stream(stream)
+    e_end.record(s_out)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    peak, peak_src = measured_bf16_peak(sustained=True)
+    achieved = flops / (k_muon * 1e-3) / 1e12
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    return {
+        "metric": MUON_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+        "params_per_s": round(n_real * world / (ms_step * 1e-3), 1),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "optimizer": "muon", "real_params": n_real,
+                   "matrix_tensors": n_mats, "chunks": ss.muon_chunks(), "m": w.m,
+                   "ns_steps": 5,
+                   "ns_flops_per_step": flops, "root_load_balance": round(balance, 4),
+                   "gemm": "cuBLASLt bf16 x bf16 -> bf16, fp32 accumulation, strided batch",
+                   "l2": "working set (master, momentum, Newton-Schulz buffers) larger than "
+                         "L2, no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU, m virtual ranks",
+                   "kernel_ms": {"muon_step": round(k_muon, 5),
+                                 "pack+unpack": round(k_copy, 5)}},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "vsf_muon_step (Newton-Schulz GEMM chain with its element-wise "
+                               "kernels)",
+                     "peak_source": peak_src},
+        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": int(host_g.numel() * 2),
+                "d2h_bytes_per_step": int(host_p.numel() * 2)},
+        "gpu_launches": (2 + 3 * ss.muon_chunks()) * args.steps,
+        "gpu_launches_note": "own kernels: copy-in, copy-out, and momentum, normalise and "
+                             "update per batched chunk of same-shape matrices; the 15 "
+                             "Newton-Schulz GEMMs per chunk are cuBLASLt launches, not counted",
+        "clocks": clocks,
+    }
+
+
+def muon_cpu_baseline(w, threads: int | None = None):
+    """The Muon oracle (numpy, fp64 products with bf16 rounding points) on
+    one whole matrix tensor of w, run in a child process with a fixed BLAS
+    thread count so that `cores` is the count it used."""
+    threads = threads or os.cpu_count() or 1
+    mats = [t for t in w.tensors if len(t.shape) >= 2]
+    t = min(mats, key=lambda x: math.prod(x.shape))
+    code = (
+        "import json, math, time, numpy as np\n"
+        "from oracle import muon\n"
+        f"R, C = {t.shape[-2]}, {t.shape[-1]}\n"
+        "rng = np.random.default_rng(0)\n"
+        "g = muon.bf16_from_f32((rng.standard_normal((R, C)) * 1e-3).astype(np.float32))\n"
+        "M = np.zeros((R, C), np.float32); p = np.zeros((R, C), np.float32)\n"
+        "hp = dict(lr=0.02, momentum=0.95, weight_decay=0.01, eps=1e-7, ns_steps=5,"
+        " ns_a=3.4445, ns_b=-4.7750, ns_c=2.0315)\n"
+        "t0 = time.perf_counter(); muon.muon_matrix(g, M, p, hp)\n"
+        "print(json.dumps(time.perf_counter() - t0))\n")
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads), PYTHONPATH=ROOT)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True, cwd=ROOT)
+    sec = float(out.stdout.strip().splitlines()[-1])
+    R, C = t.shape[-2], t.shape[-1]
+    n, k = min(R, C), max(R, C)
+    fl = 5 * (4.0 * n * n * k + 2.0 * n ** 3)
+    return dict(value=round(fl / sec / 1e12, 6), unit="TFLOP/s", cores=threads, kind="oracle",
+                sample=f"one Muon step of one {R}x{C} matrix ({t.name}) of {w.name}, "
+                       f"{sec:.2f} s, numpy BLAS with {threads} threads")
+
+
 # Per-launch DRAM traffic in bytes (dram__bytes_read.sum + dram__bytes_write.sum)
 # of the AdamW bulk-copy kernel, from the ncu captures summarised in profiles/
 # (adam8_tma_*.md); a workload without a capture of the current kernel is None.
@@ -410,6 +634,22 @@ def reference_arm(args):
     }
 
 
+def muon_reference_arm(args):
+    """The Muon oracle on one whole matrix per step (see muon_cpu_baseline)."""
+    from synth import workloads as W
+    w = W.get(args.workload)
+    base = muon_cpu_baseline(w)
+    return {
+        "impl": "reference", "metric": MUON_METRIC, "value": base["value"], "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": 1, "warmup": 0, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "optimizer": "muon"},
+        "cpu_baseline": base,
+        "e2e": {"value": base["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -418,6 +658,8 @@ def main():
     ap.add_argument("--impl", default="vsf", choices=["vsf", "reference"])
     ap.add_argument("--workload", default="llama_layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--optimizer", default="adam8", choices=["adam8", "muon"],
+                    help="adam8: the 8-bit AdamW shard step; muon: distributed Muon")
     ap.add_argument("--zero-copy", action="store_true",
                     help="gradients/params as views of the packed buffers (no pack/unpack)")
     args = ap.parse_args()
@@ -428,16 +670,20 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(reference_arm(args)), flush=True)
+            print(json.dumps(muon_reference_arm(args) if args.optimizer == "muon"
+                             else reference_arm(args)), flush=True)
         return
+    if args.optimizer == "muon" and args.zero_copy:
+        ap.error("--zero-copy applies to the AdamW step")
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    line = gpu_arm(args, rank, world)
+    line = (muon_arm if args.optimizer == "muon" else gpu_arm)(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             from synth import workloads as W
-            line["cpu_baseline"] = cpu_baseline(W.get(args.workload))
+            line["cpu_baseline"] = (muon_cpu_baseline if args.optimizer == "muon"
+                                    else cpu_baseline)(W.get(args.workload))
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

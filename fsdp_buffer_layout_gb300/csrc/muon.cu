@@ -14,6 +14,8 @@
 //                         accumulation), batched over a tensor's matrices;
 //   Redistribute back     zero-copy again; the element-wise update writes the
 //                         ragged shards in place.
+// Matrices of one shape from every tensor are batched into the same launches
+// (in chunks), so that many small matrices still fill the GPU.
 // Own kernels: momentum with the per-matrix Frobenius norm (double-float
 // accumulation, fixed-order fp64 reduction), the bf16 normalisation, and the
 // update of master and bf16 copy. Readings (the pages give no coefficients):
@@ -40,8 +42,15 @@ namespace vsf {
 namespace {
 
 constexpr int kMuonThreads = 256;
-constexpr int kMuonCtasPerMatrix = 64;     // norm partials per matrix
-constexpr size_t kLtWorkspace = 64u << 20;  // cuBLASLt workspace bytes
+constexpr int kMuonTargetCtas = 152 * 8;         // fills every SM of the GPU
+constexpr int kMaxChunk = 192;                    // matrices in one batched chunk
+constexpr int64_t kChunkElems = int64_t(1) << 28;  // bf16 elements of X per chunk (512 MB)
+constexpr size_t kLtWorkspace = 64u << 20;         // cuBLASLt workspace bytes
+
+// Packed-buffer offset of every matrix of one chunk (kernel parameter).
+struct MatTable {
+  int64_t off[kMaxChunk];
+};
 
 struct DFm {
   float hi = 0.0f, lo = 0.0f;
@@ -61,19 +70,67 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
-// grid (kMuonCtasPerMatrix, nmat): M = mu M + g; partial sums of U^2,
-// U = g + mu M, per CTA of each matrix.
+// Element access of the three element-wise kernels: V = 8 consecutive
+// elements per access (16-byte bf16 and 2 x 16-byte fp32 accesses; every
+// matrix offset a multiple of 8) or V = 1.
+template <int V>
+struct Vec;
+template <>
+struct Vec<1> {
+  static __device__ __forceinline__ void load_bf(const uint16_t* p, float* x) { x[0] = bf16f(*p); }
+  static __device__ __forceinline__ void load_f(const float* p, float* x) { x[0] = *p; }
+  static __device__ __forceinline__ void store_f(float* p, const float* x) { *p = x[0]; }
+  static __device__ __forceinline__ void store_bf(uint16_t* p, const float* x) { *p = to_bf16(x[0]); }
+};
+template <>
+struct Vec<8> {
+  static __device__ __forceinline__ void load_bf(const uint16_t* p, float* x) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+  static __device__ __forceinline__ void load_f(const float* p, float* x) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  static __device__ __forceinline__ void store_f(float* p, const float* x) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+  }
+  static __device__ __forceinline__ void store_bf(uint16_t* p, const float* x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      w[j] = (uint32_t)to_bf16(x[2 * j]) | ((uint32_t)to_bf16(x[2 * j + 1]) << 16);
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// grid (per, batch): M = mu M + g; partial sums of U^2, U = g + mu M, one
+// per CTA of each matrix (partials[j * per + x]).
+template <int V>
 __global__ void __launch_bounds__(kMuonThreads) muon_momentum_kernel(
-    const uint16_t* __restrict__ g, float* M, int64_t base, int64_t mat, float mu,
-    double* partials) {
-  const int64_t off = base + (int64_t)blockIdx.y * mat;
+    const uint16_t* __restrict__ g, float* M, const __grid_constant__ MatTable tab, int64_t mat,
+    float mu, double* partials) {
+  const int64_t off = tab.off[blockIdx.y];
   DFm acc;
-  for (int64_t i = (int64_t)blockIdx.x * kMuonThreads + threadIdx.x; i < mat;
-       i += (int64_t)gridDim.x * kMuonThreads) {
-    const float gi = bf16f(g[off + i]);
-    const float m = __fadd_rn(__fmul_rn(mu, M[off + i]), gi);
-    M[off + i] = m;
-    acc.add_sq(__fadd_rn(gi, __fmul_rn(mu, m)));
+  for (int64_t i = ((int64_t)blockIdx.x * kMuonThreads + threadIdx.x) * V; i < mat;
+       i += (int64_t)gridDim.x * kMuonThreads * V) {
+    float gi[V], m[V];
+    Vec<V>::load_bf(g + off + i, gi);
+    Vec<V>::load_f(M + off + i, m);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      m[j] = __fadd_rn(__fmul_rn(mu, m[j]), gi[j]);
+      acc.add_sq(__fadd_rn(gi[j], __fmul_rn(mu, m[j])));
+    }
+    Vec<V>::store_f(M + off + i, m);
   }
   __shared__ double red[kMuonThreads / 32];
   double v = isinf(acc.hi) ? (double)acc.hi : (double)acc.hi + (double)acc.lo;
@@ -87,38 +144,60 @@ __global__ void __launch_bounds__(kMuonThreads) muon_momentum_kernel(
   }
 }
 
-// One thread per matrix: r = fp32(1 / (sqrt(sum) + eps)).
-__global__ void muon_scale_kernel(const double* __restrict__ partials, int per, int nmat,
-                                  double eps, float* r) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= nmat) return;
-  double s = 0.0;
-  for (int i = 0; i < per; ++i) s += partials[(int64_t)e * per + i];
-  r[e] = __double2float_rn(1.0 / (sqrt(s) + eps));
-}
-
-// X0 = bf16(U * r), U = g + mu M (the momentum already updated).
+// X0 = bf16(U * r), U = g + mu M (the momentum already updated), r =
+// fp32(1 / (sqrt(sum of the matrix's partials) + eps)); every CTA of a matrix
+// reduces the same partials in the same fixed order, so all agree on r. X
+// holds the chunk's matrices back to back.
+template <int V>
 __global__ void __launch_bounds__(kMuonThreads) muon_normalize_kernel(
-    const uint16_t* __restrict__ g, const float* __restrict__ M, int64_t base, int64_t mat,
-    float mu, const float* __restrict__ r, uint16_t* X) {
-  const int64_t off = (int64_t)blockIdx.y * mat;
-  const float re = r[blockIdx.y];
-  for (int64_t i = (int64_t)blockIdx.x * kMuonThreads + threadIdx.x; i < mat;
-       i += (int64_t)gridDim.x * kMuonThreads) {
-    const float u = __fadd_rn(bf16f(g[base + off + i]), __fmul_rn(mu, M[base + off + i]));
-    X[off + i] = to_bf16(__fmul_rn(u, re));
+    const uint16_t* __restrict__ g, const float* __restrict__ M, const __grid_constant__ MatTable tab,
+    int64_t mat, float mu, const double* __restrict__ partials, double eps, uint16_t* X) {
+  __shared__ double red[kMuonThreads / 32];
+  __shared__ float r_s;
+  {
+    const double* p = partials + (int64_t)blockIdx.y * gridDim.x;
+    double v = 0.0;
+    for (unsigned i = threadIdx.x; i < gridDim.x; i += kMuonThreads) v += p[i];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double s = 0.0;
+      for (int w = 0; w < kMuonThreads / 32; ++w) s += red[w];
+      r_s = __double2float_rn(1.0 / (sqrt(s) + eps));
+    }
+    __syncthreads();
+  }
+  const float re = r_s;
+  const int64_t off = tab.off[blockIdx.y];
+  uint16_t* x = X + (int64_t)blockIdx.y * mat;
+  for (int64_t i = ((int64_t)blockIdx.x * kMuonThreads + threadIdx.x) * V; i < mat;
+       i += (int64_t)gridDim.x * kMuonThreads * V) {
+    float gi[V], m[V], u[V];
+    Vec<V>::load_bf(g + off + i, gi);
+    Vec<V>::load_f(M + off + i, m);
+#pragma unroll
+    for (int j = 0; j < V; ++j) u[j] = __fmul_rn(__fadd_rn(gi[j], __fmul_rn(mu, m[j])), re);
+    Vec<V>::store_bf(x + i, u);
   }
 }
 
 // p = p * decay - alpha * O; bf16 copy.
+template <int V>
 __global__ void __launch_bounds__(kMuonThreads) muon_update_kernel(
-    const uint16_t* __restrict__ O, float* master, uint16_t* bf, int64_t base, int64_t n,
-    float decay, float alpha) {
-  for (int64_t i = (int64_t)blockIdx.x * kMuonThreads + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * kMuonThreads) {
-    const float p = __fsub_rn(__fmul_rn(master[base + i], decay), __fmul_rn(alpha, bf16f(O[i])));
-    master[base + i] = p;
-    bf[base + i] = to_bf16(p);
+    const uint16_t* __restrict__ O, float* master, uint16_t* bf, const __grid_constant__ MatTable tab,
+    int64_t mat, float decay, float alpha) {
+  const int64_t off = tab.off[blockIdx.y];
+  const uint16_t* o = O + (int64_t)blockIdx.y * mat;
+  for (int64_t i = ((int64_t)blockIdx.x * kMuonThreads + threadIdx.x) * V; i < mat;
+       i += (int64_t)gridDim.x * kMuonThreads * V) {
+    float ov[V], p[V];
+    Vec<V>::load_bf(o + i, ov);
+    Vec<V>::load_f(master + off + i, p);
+#pragma unroll
+    for (int j = 0; j < V; ++j) p[j] = __fsub_rn(__fmul_rn(p[j], decay), __fmul_rn(alpha, ov[j]));
+    Vec<V>::store_f(master + off + i, p);
+    Vec<V>::store_bf(bf + off + i, p);
   }
 }
 
@@ -147,17 +226,63 @@ double ns_flops(const MuonMatrix& mm) {
   return (double)mm.batch * (4.0 * n * n * k + 2.0 * n * n * n);
 }
 
+// Matrices of one shape, batched through the same launches: every matrix of
+// every tensor of that shape, in tensor order, cut into chunks of at most
+// kMaxChunk matrices and kChunkElems elements.
+struct MuonChunk {
+  int64_t R, C, batch;
+  std::vector<int64_t> off;  // packed offset of each matrix
+};
+
+std::vector<MuonChunk> muon_chunks(const vsf_plan* plan) {
+  std::vector<std::pair<int64_t, int64_t>> shapes;
+  std::vector<std::vector<int64_t>> offs;
+  for (const MuonMatrix& mm : muon_matrices(plan)) {
+    size_t s = 0;
+    while (s < shapes.size() && shapes[s] != std::make_pair(mm.R, mm.C)) ++s;
+    if (s == shapes.size()) {
+      shapes.push_back({mm.R, mm.C});
+      offs.emplace_back();
+    }
+    const int64_t base = plan->tensors[mm.tensor].offset;
+    for (int64_t e = 0; e < mm.batch; ++e) offs[s].push_back(base + e * mm.R * mm.C);
+  }
+  std::vector<MuonChunk> out;
+  for (size_t s = 0; s < shapes.size(); ++s) {
+    const int64_t mat = shapes[s].first * shapes[s].second;
+    const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(kMaxChunk, kChunkElems / mat));
+    for (size_t i = 0; i < offs[s].size(); i += (size_t)cap) {
+      MuonChunk c;
+      c.R = shapes[s].first;
+      c.C = shapes[s].second;
+      const size_t end = std::min(offs[s].size(), i + (size_t)cap);
+      c.off.assign(offs[s].begin() + i, offs[s].begin() + end);
+      c.batch = (int64_t)c.off.size();
+      out.push_back(std::move(c));
+    }
+  }
+  return out;
+}
+
+// CTAs per matrix for the element-wise kernels: enough to fill the GPU,
+// at least 4 elements per thread.
+int muon_per(int64_t batch, int64_t mat) {
+  const int64_t want = (kMuonTargetCtas + batch - 1) / batch;
+  const int64_t most = std::max<int64_t>(1, mat / (8 * kMuonThreads));
+  return (int)std::max<int64_t>(1, std::min(want, most));
+}
+
 struct MuonLayout {
-  size_t lt = 0, partials = 0, r = 0, x = 0, xn = 0, a = 0, b = 0, bytes = 0;
+  size_t lt = 0, partials = 0, x = 0, xn = 0, a = 0, b = 0, bytes = 0;
 };
 
 MuonLayout muon_layout(const vsf_plan* plan) {
-  int64_t max_elems = 0, max_sq = 0, max_batch = 0;
-  for (const MuonMatrix& mm : muon_matrices(plan)) {
-    const int64_t n = std::min(mm.R, mm.C);
-    max_elems = std::max(max_elems, mm.batch * mm.R * mm.C);
-    max_sq = std::max(max_sq, mm.batch * n * n);
-    max_batch = std::max(max_batch, mm.batch);
+  int64_t max_elems = 0, max_sq = 0, max_part = 0;
+  for (const MuonChunk& c : muon_chunks(plan)) {
+    const int64_t n = std::min(c.R, c.C);
+    max_elems = std::max(max_elems, c.batch * c.R * c.C);
+    max_sq = std::max(max_sq, c.batch * n * n);
+    max_part = std::max(max_part, c.batch * muon_per(c.batch, c.R * c.C));
   }
   MuonLayout L;
   size_t cur = 0;
@@ -167,8 +292,7 @@ MuonLayout muon_layout(const vsf_plan* plan) {
     return at;
   };
   L.lt = section(kLtWorkspace);
-  L.partials = section(sizeof(double) * std::max<int64_t>(1, max_batch) * kMuonCtasPerMatrix);
-  L.r = section(sizeof(float) * std::max<int64_t>(1, max_batch));
+  L.partials = section(sizeof(double) * std::max<int64_t>(1, max_part));
   L.x = section(2 * std::max<int64_t>(1, max_elems));
   L.xn = section(2 * std::max<int64_t>(1, max_elems));
   L.a = section(2 * std::max<int64_t>(1, max_sq));
@@ -305,6 +429,10 @@ size_t vsf_muon_workspace_bytes(const vsf_plan* plan) {
   return plan == nullptr ? 0 : muon_layout(plan).bytes;
 }
 
+int32_t vsf_muon_chunk_count(const vsf_plan* plan) {
+  return plan == nullptr ? 0 : (int32_t)muon_chunks(plan).size();
+}
+
 vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream) {
@@ -322,7 +450,6 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
   double* partials = reinterpret_cast<double*>(ws + L.partials);
-  float* r = reinterpret_cast<float*>(ws + L.r);
   uint16_t* X = reinterpret_cast<uint16_t*>(ws + L.x);
   uint16_t* Xn = reinterpret_cast<uint16_t*>(ws + L.xn);
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
@@ -332,52 +459,63 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
   const float decay = (float)(1.0 - hp->lr * hp->weight_decay);
   const float na = (float)hp->ns_a, nb = (float)hp->ns_b, nc = (float)hp->ns_c;
 
-  for (const MuonMatrix& mm : muon_matrices(plan)) {
-    const int64_t base = plan->tensors[mm.tensor].offset;
-    const int64_t mat = mm.R * mm.C;
-    if (mm.batch > 65535) return fail(VSF_ERR_ARG, "vsf_muon_step: more than 65535 matrices in a tensor");
-    const dim3 grid(kMuonCtasPerMatrix, (unsigned)mm.batch);
-    muon_momentum_kernel<<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, base, mat, mu,
-                                                        partials);
-    muon_scale_kernel<<<(unsigned)((mm.batch + 127) / 128), 128, 0, st>>>(
-        partials, kMuonCtasPerMatrix, (int)mm.batch, hp->eps, r);
-    muon_normalize_kernel<<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, base, mat, mu, r,
-                                                         X);
+  for (const MuonChunk& c : muon_chunks(plan)) {
+    MatTable tab;
+    for (int64_t j = 0; j < c.batch; ++j) tab.off[j] = c.off[(size_t)j];
+    const int64_t mat = c.R * c.C;
+    const int per = muon_per(c.batch, mat);
+    const dim3 grid((unsigned)per, (unsigned)c.batch);
+    // 8-wide accesses when every matrix of the chunk starts on 8 elements
+    bool vec = mat % 8 == 0;
+    for (int64_t j = 0; j < c.batch; ++j) vec = vec && c.off[(size_t)j] % 8 == 0;
+    if (vec) {
+      muon_momentum_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                             partials);
+      muon_normalize_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                              partials, hp->eps, X);
+    } else {
+      muon_momentum_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                             partials);
+      muon_normalize_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                              partials, hp->eps, X);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
     // Newton-Schulz, column-major view of the row-major R x C matrices: Xc is
     // C x R with leading dimension C.
-    const bool tall = mm.R > mm.C;
-    const int64_t n = std::min(mm.R, mm.C), sx = mat, sa = n * n;
+    const bool tall = c.R > c.C;
+    const int64_t n = std::min(c.R, c.C), sx = mat, sa = n * n;
     for (int it = 0; it < hp->ns_steps; ++it) {
       vsf_status s;
       // A (n x n) = X X^T (wide) or X^T X (tall)
       if (!tall)
-        s = lt_gemm(true, false, n, n, mm.C, X, mm.C, sx, X, mm.C, sx, 1.0f, 0.0f, A, A, n, sa,
-                    mm.batch, lt, st);
+        s = lt_gemm(true, false, n, n, c.C, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f, A, A, n, sa,
+                    c.batch, lt, st);
       else
-        s = lt_gemm(false, true, n, n, mm.R, X, mm.C, sx, X, mm.C, sx, 1.0f, 0.0f, A, A, n, sa,
-                    mm.batch, lt, st);
+        s = lt_gemm(false, true, n, n, c.R, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f, A, A, n, sa,
+                    c.batch, lt, st);
       if (s != VSF_OK) return s;
       // B = c A A + b A
-      s = lt_gemm(false, false, n, n, n, A, n, sa, A, n, sa, nc, nb, A, B, n, sa, mm.batch, lt, st);
+      s = lt_gemm(false, false, n, n, n, A, n, sa, A, n, sa, nc, nb, A, B, n, sa, c.batch, lt, st);
       if (s != VSF_OK) return s;
       // X' = a X + B X (wide) or a X + X B (tall), column-major Xc' = a Xc +
       // Xc B (wide) or a Xc + B Xc (tall)
       if (!tall)
-        s = lt_gemm(false, false, mm.C, mm.R, mm.R, X, mm.C, sx, B, n, sa, 1.0f, na, X, Xn, mm.C,
-                    sx, mm.batch, lt, st);
+        s = lt_gemm(false, false, c.C, c.R, c.R, X, c.C, sx, B, n, sa, 1.0f, na, X, Xn, c.C, sx,
+                    c.batch, lt, st);
       else
-        s = lt_gemm(false, false, mm.C, mm.R, mm.C, B, n, sa, X, mm.C, sx, 1.0f, na, X, Xn, mm.C,
-                    sx, mm.batch, lt, st);
+        s = lt_gemm(false, false, c.C, c.R, c.C, B, n, sa, X, c.C, sx, 1.0f, na, X, Xn, c.C, sx,
+                    c.batch, lt, st);
       if (s != VSF_OK) return s;
       std::swap(X, Xn);
     }
-    const float alpha = (float)(hp->lr * std::sqrt(std::max(1.0, (double)mm.R / (double)mm.C)));
-    const int64_t total = mm.batch * mat;
-    const unsigned ugrid = (unsigned)std::min<int64_t>(4096, (total + kMuonThreads - 1) / kMuonThreads);
-    muon_update_kernel<<<ugrid, kMuonThreads, 0, st>>>(X, master, packed_bf16, base, total, decay,
-                                                       alpha);
+    const float alpha = (float)(hp->lr * std::sqrt(std::max(1.0, (double)c.R / (double)c.C)));
+    if (vec)
+      muon_update_kernel<8><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
+                                                           alpha);
+    else
+      muon_update_kernel<1><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
+                                                           alpha);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
   }

@@ -113,6 +113,14 @@ class ShardStep:
                         self.master.data_ptr(), self.packed_bf16.data_ptr(), hp,
                         self.muon_ws.data_ptr(), self.muon_ws.numel(), self.stream.cuda_stream)
 
+    def muon_roots(self):
+        """SelectRoot: (root rank per tensor, -1 for 1-D; max/mean load)."""
+        return V.vsf_muon_select_roots(self.plan, len(self.specs))
+
+    def muon_chunks(self) -> int:
+        """Batched chunks of same-shape matrices one Muon step runs."""
+        return V.vsf_muon_chunk_count(self.plan)
+
     def adam_launches(self) -> int:
         """Kernels one vsf_adam8_step launches for this plan (quantised mode)."""
         i = self.info

@@ -115,6 +115,8 @@ def lib():
             L.vsf_muon_select_roots.argtypes = [vp, vp, P(ctypes.c_double)]
             L.vsf_muon_workspace_bytes.restype = ctypes.c_size_t
             L.vsf_muon_workspace_bytes.argtypes = [vp]
+            L.vsf_muon_chunk_count.restype = ctypes.c_int32
+            L.vsf_muon_chunk_count.argtypes = [vp]
             L.vsf_muon_step.restype = st
             L.vsf_muon_step.argtypes = [vp, vp, vp, vp, vp, P(vsf_muon_hparams), vp,
                                         ctypes.c_size_t, vp]
@@ -270,6 +272,10 @@ def vsf_muon_select_roots(plan: int, n: int):
 
 def vsf_muon_workspace_bytes(plan: int) -> int:
     return int(lib().vsf_muon_workspace_bytes(plan))
+
+
+def vsf_muon_chunk_count(plan: int) -> int:
+    return int(lib().vsf_muon_chunk_count(plan))
 
 
 def vsf_muon_step(plan: int, packed_grad: int, momentum: int, master: int, packed_bf16: int,

@@ -247,7 +247,12 @@ vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, con
  *     p = p (1 - lr wd) - fp32(lr sqrt(max(1, R/C))) X;  bf16 copy.
  *   packed_grad: bf16, m*S; momentum: fp32, m*S (caller-zeroed before step
  *   1); master: fp32; packed_bf16: out. d_workspace: vsf_muon_workspace_bytes
- *   of caller memory (Newton-Schulz operands and the cuBLASLt workspace). */
+ *   of caller memory (Newton-Schulz operands and the cuBLASLt workspace).
+ *   Matrices of one shape, across tensors, run batched: vsf_muon_chunk_count
+ *   gives the number of batches (each: 3 own kernels and 3 * ns_steps
+ *   cuBLASLt GEMMs); 0 for a NULL plan. Errors: VSF_ERR_ARG (NULL, small
+ *   workspace, ns_steps < 0), VSF_ERR_ALIGN (a pointer not 16-byte aligned),
+ *   VSF_ERR_STATE (plan not uploaded), VSF_ERR_CUDA (launch or cuBLASLt). */
 typedef struct {
   double lr, momentum, weight_decay, eps, ns_a, ns_b, ns_c;
   int32_t ns_steps, reserved;
@@ -255,6 +260,7 @@ typedef struct {
 
 vsf_status vsf_muon_select_roots(const vsf_plan* plan, int32_t* root, double* load_balance);
 size_t vsf_muon_workspace_bytes(const vsf_plan* plan);
+int32_t vsf_muon_chunk_count(const vsf_plan* plan);
 vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream);

@@ -74,6 +74,13 @@ def _run(specs, m, g_coll, steps):
     [((256, 512), W.GRAN_ROWS, 32, 0), ((512,), W.GRAN_ELEM, 0, 0)],
     [((512, 256), W.GRAN_ROWS, 32, 0)],
     [((384, 384), W.GRAN_TILE, 128, 128), ((4, 128, 256), W.GRAN_ROWS, 64, 0)],
+    # one shape across tensors (one batched chunk), another shape between them
+    [((128, 256), W.GRAN_ROWS, 32, 0), ((96, 64), W.GRAN_ROWS, 32, 0),
+     ((2, 128, 256), W.GRAN_ROWS, 64, 0), ((128, 256), W.GRAN_ROWS, 128, 0), ((7,), W.GRAN_ELEM, 0, 0)],
+    # 63-element matrices: offsets off the 8-element grid (scalar kernels)
+    [((5, 9, 7), W.GRAN_ROWS, 5, 0), ((24, 40), W.GRAN_ROWS, 8, 0)],
+    # more matrices of one shape than one chunk holds (192)
+    [((200, 16, 32), W.GRAN_ROWS, 16, 0), ((3, 32, 16), W.GRAN_ROWS, 32, 0)],
 ])
 def test_muon_matches_oracle(specs):
     ss, state, masters = _run(specs, 4, 128, steps=3)
