@@ -19,7 +19,7 @@
 // (release at cluster scope); consumers wait on their own barrier (acquire).
 // Slots and barriers alternate between two sets by block parity.
 //
-// Every wait is bounded: after kWaitLimit polls it sets bit 1 of the device
+// Every wait is bounded: after 2 s it sets bit 1 of the device
 // error word and carries on as if the wait had succeeded (the results are
 // then wrong but every CTA still finishes, so no thread hangs and no CTA
 // leaves while a copy or a peer's write into it is still pending).
@@ -28,7 +28,8 @@ constexpr int kConsumerWarps = VSF_TMA_WARPS;   // consumer warps per CTA
 constexpr int kTmaGroups = VSF_TMA_GROUPS;       // 8-element groups per thread and chunk
 constexpr int kTmaChunk = kTmaChunkElems;         // elements per ring chunk
 constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kSuspendNs = 1u << 20;        // sleep limit of one barrier test
+constexpr uint64_t kWaitNs = 2000000000ull;       // bound of one wait: 2 s
 
 template <typename GT>
 struct TmaLayout {
@@ -56,36 +57,63 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-// Bounded wait for the phase of the given parity; returns false on timeout.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One potentially blocking test of the phase with the given parity: the
+// thread may sleep until the phase completes or kSuspendNs pass, so a
+// waiting warp issues a few instructions per wait instead of spinning.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of the given parity; returns false after
+// kWaitNs of wall-clock time (global timer), having set bit 1 of the error
+// word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try(bar, parity)) {
+    if (global_ns() - t0 > kWaitNs) {
+      atomicOr(err, 2u);
+      return false;
+    }
   }
-  atomicOr(err, 2u);
-  return false;
+  return true;
 }
 
 // The same at cluster scope (acquire), for barriers that peers arrive on.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
+  if (mbar_try_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_cluster(bar, parity)) {
+    if (global_ns() - t0 > kWaitNs) {
+      atomicOr(err, 2u);
+      return false;
+    }
   }
-  atomicOr(err, 2u);
-  return false;
+  return true;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
