@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kSmallThreads) adam_small_kernel(
 // fp32 moments (no quantisation): element-wise over the copy spans.
 template <typename GT>
 __global__ void __launch_bounds__(kCopyThreads) adam_fp32_kernel(
-    const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_numel,
+    const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_lo, const int64_t* __restrict__ t_hi,
     const CopySpan* __restrict__ spans, const GT* __restrict__ grad,
     const float* __restrict__ d_factor, float* master, float* m_state, float* v_state,
     uint16_t* bf, AdamConsts k) {
@@ -592,8 +592,8 @@ __global__ void __launch_bounds__(kCopyThreads) adam_fp32_kernel(
   c.dm = f2(1.0f);
   c.dv = f2(1.0f);
   for (int t = s0.tensor; t <= s1.tensor; ++t) {
-    const int64_t b = (t == s0.tensor) ? s0.elem : 0;
-    const int64_t e = (t == s1.tensor) ? s1.elem : t_numel[t];
+    const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
+    const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
     const int64_t base = t_off[t];
     for (int64_t i = b + threadIdx.x; i < e; i += kCopyThreads) {
       const int64_t x = base + i;

@@ -440,6 +440,8 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
       packed_bf16 == nullptr || hp == nullptr || d_workspace == nullptr)
     return fail(VSF_ERR_ARG, "vsf_muon_step: NULL argument");
   if (!plan->uploaded) return fail(VSF_ERR_STATE, "vsf_muon_step: plan not uploaded");
+  if (plan->rank_begin != 0 || plan->rank_end != plan->m)
+    return fail(VSF_ERR_STATE, "vsf_muon_step: Newton-Schulz needs whole matrices (unrestricted plan)");
   const MuonLayout L = muon_layout(plan);
   if (ws_bytes < L.bytes) return fail(VSF_ERR_ARG, "vsf_muon_step: workspace too small");
   for (const void* p : {(const void*)packed_grad, (const void*)momentum, (const void*)master,

@@ -119,6 +119,160 @@ vsf_status fail(vsf_status s, const std::string& msg) {
   return s;
 }
 
+// Quantisation-block tables, tile maps and the workspace layout for the rank
+// window [r0, r1). Only blocks inside the window are listed (no block
+// crosses a rank boundary: RaggedShard's Non-Sharded Block rule for row and
+// tile atoms; element chunks start on g_coll multiples, as do offsets and
+// S). Buffer elements are counted from the window start r0 * S.
+vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
+  const int n = plan->n;
+  const int64_t g_coll = plan->g_coll;
+  const int64_t wlo = (int64_t)r0 * plan->S, whi = (int64_t)r1 * plan->S;
+  plan->rank_begin = r0;
+  plan->rank_end = r1;
+  plan->total = whi - wlo;
+  plan->qblocks.clear();
+  plan->big_blocks.clear();
+  plan->tma_blocks.clear();
+  plan->tma_tiles.clear();
+  plan->tile_maps.clear();
+  plan->small_blocks.clear();
+  plan->max_big_elems = 0;
+  plan->max_tma_elems = 0;
+  std::vector<TensorInfo>& ts = plan->tensors;
+  int64_t real = 0;
+  for (TensorInfo& x : ts) {
+    x.lo = std::min(x.numel, std::max<int64_t>(0, wlo - x.offset));
+    x.hi = std::max(x.lo, std::min(x.numel, whi - x.offset));
+    real += x.hi - x.lo;
+  }
+  plan->real = real;
+
+  // Quantisation blocks, tensor order ([VSF] case study › 8-bit Adam).
+  for (int t = 0; t < n; ++t) {
+    const TensorInfo& x = ts[t];
+    if (x.lo >= x.hi) continue;  // no element inside the window
+    const int64_t off = x.offset - wlo;  // window element of the tensor's element 0
+    // Rows inside the window: whole stripes for row and tile atoms.
+    const int64_t row_lo = x.lo / x.cols, row_hi = x.hi / x.cols;
+    // Tile tensors whose full tiles go to the bulk-copy kernel as 2-D tensor
+    // copies: tile width a power of two in [32, 256], k = 256 / width tiles
+    // per work unit (one copy box of 256 columns), whole boxes of rows per
+    // tile, 16-element aligned rows and window offset.
+    int map = -1;
+    int64_t k = 1;
+    if (x.gran == VSF_GRAN_TILE && (int)plan->tile_maps.size() < kMaxTileMaps) {
+      const int64_t bc = x.tile_cols, br = x.block_rows;
+      if (bc >= 32 && bc <= 256 && (bc & (bc - 1)) == 0) {
+        k = std::min<int64_t>(256 / bc, kMaxUnitTiles);
+        const int64_t box_cols = k * bc;
+        const int64_t box_rows = std::min<int64_t>(br, kTmaChunkElems / box_cols);
+        const int64_t map_off = off + row_lo * x.cols;
+        if (box_rows >= 1 && box_rows <= 256 && br % box_rows == 0 && x.cols % 16 == 0 &&
+            map_off % 16 == 0 && x.cols >= box_cols) {
+          TileMapInfo mi;
+          mi.tensor = t;
+          mi.tile_cols = (int32_t)bc;
+          mi.k = (int32_t)k;
+          mi.box_cols = (int32_t)box_cols;
+          mi.box_rows = (int32_t)box_rows;
+          mi.rows = row_hi - row_lo;
+          mi.cols = x.cols;
+          mi.offset = map_off;
+          map = (int)plan->tile_maps.size();
+          plan->tile_maps.push_back(mi);
+        }
+      }
+    }
+    // Where a block goes: element chunks to the warp kernel; contiguous
+    // blocks that start on 16 elements and hold a multiple of 16, and full
+    // tiles grouped k at a time, to the bulk-copy (TMA) kernel; every other
+    // row or tile block (ragged, unaligned, leftover) to the register kernel.
+    enum Dest { kSmall, kTma, kTmaTile, kTmaTileMember, kRegister };
+    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, Dest dest, int64_t r,
+                   int64_t c) {
+      QBlock b{};
+      b.base = base;
+      b.nrows = (int32_t)nr;
+      b.ncols = (int32_t)nc;
+      b.stride = (int32_t)st;
+      b.tensor = t;
+      b.tx = -1;
+      b.ty = -1;
+      const int32_t q = (int32_t)plan->qblocks.size();
+      if (dest == kTmaTile || dest == kTmaTileMember) {
+        b.tx = (int32_t)c;
+        b.ty = (int32_t)(r - row_lo);  // row inside the tile map
+      }
+      if (dest == kSmall) {
+        plan->small_blocks.push_back(q);
+      } else if (dest == kTma || dest == kTmaTile) {
+        plan->tma_blocks.push_back(q);
+        plan->tma_tiles.push_back(dest == kTmaTile ? (int32_t)k : 1);
+        plan->max_tma_elems = std::max(plan->max_tma_elems, nr * nc * (dest == kTmaTile ? k : 1));
+      } else if (dest == kRegister) {
+        plan->big_blocks.push_back(q);
+        plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
+      }
+      plan->qblocks.push_back(b);
+    };
+    if (x.gran == VSF_GRAN_ELEM) {
+      if (g_coll > INT32_MAX) return fail(VSF_ERR_OVERFLOW, "g_coll too large for element-granular blocks");
+      for (int64_t e = x.lo; e < x.hi; e += g_coll) {
+        const int64_t len = std::min(g_coll, x.numel - e);
+        add(off + e, 1, len, len, kSmall, 0, e);
+      }
+    } else if (x.gran == VSF_GRAN_ROWS) {
+      for (int64_t r = row_lo; r < row_hi; r += x.block_rows) {
+        const int64_t nr = std::min(x.block_rows, x.rows - r);
+        // a whole-row block is contiguous: one row of nr*cols elements
+        if (nr * x.cols > INT32_MAX)
+          return fail(VSF_ERR_OVERFLOW, "quantisation block larger than 2^31 elements");
+        const int64_t base = off + r * x.cols, len = nr * x.cols;
+        add(base, 1, len, len, base % 16 == 0 && len % 16 == 0 ? kTma : kRegister, r, 0);
+      }
+    } else {
+      if (x.cols > INT32_MAX || x.rows > INT32_MAX)
+        return fail(VSF_ERR_OVERFLOW, "tile tensor dimension beyond 2^31");
+      const int64_t tc = x.tile_cols;
+      for (int64_t r = row_lo; r < row_hi; r += x.block_rows) {
+        const int64_t nr = std::min(x.block_rows, x.rows - r);
+        const int64_t full = nr == x.block_rows ? x.cols / tc : 0;  // full tiles in the stripe
+        const int64_t grouped = map >= 0 ? full / k * k : 0;       // of them, in whole units
+        for (int64_t c = 0, i = 0; c < x.cols; c += tc, ++i) {
+          const int64_t nc = std::min(tc, x.cols - c);
+          const Dest dest = i < grouped ? (i % k == 0 ? kTmaTile : kTmaTileMember) : kRegister;
+          add(off + r * x.cols + c, nr, nc, x.cols, dest, r, c);
+        }
+      }
+    }
+  }
+
+  // Device workspace layout (256-byte aligned sections).
+  DeviceLayout& L = plan->layout;
+  L = DeviceLayout();
+  size_t cur = 0;
+  auto section = [&](size_t bytes) {
+    size_t at = (cur + 255) / 256 * 256;
+    cur = at + bytes;
+    return at;
+  };
+  L.tensor_off = section(sizeof(int64_t) * n);
+  L.tensor_lo = section(sizeof(int64_t) * n);
+  L.tensor_hi = section(sizeof(int64_t) * n);
+  L.qblocks = section(sizeof(QBlock) * plan->qblocks.size());
+  L.big = section(sizeof(int32_t) * std::max<size_t>(1, plan->big_blocks.size()));
+  L.small = section(sizeof(int32_t) * std::max<size_t>(1, plan->small_blocks.size()));
+  L.tma = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_blocks.size()));
+  L.tma_k = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_tiles.size()));
+  L.error = section(16);
+  L.spans = section(sizeof(CopySpan) * (kMaxCopyGrid + 1));
+  L.partials = section(sizeof(double) * kMaxCopyGrid);
+  L.bytes = (cur + 255) / 256 * 256;
+  return VSF_OK;
+}
+
+
 const char* last_error() { return g_last_error.c_str(); }
 
 }  // namespace vsf
@@ -198,138 +352,26 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
   plan->m = m;
   plan->g_coll = g_coll;
   plan->S = best_S;
-  plan->total = (int64_t)m * best_S;
-  plan->real = real;
   plan->order_used = used;
   for (int t = 0; t < n; ++t) ts[t].offset = offsets[t];
   plan->tensors = ts;
-
-  // Quantisation blocks, tensor order ([VSF] case study › 8-bit Adam).
-  for (int t = 0; t < n; ++t) {
-    const vsf::TensorInfo& x = ts[t];
-    // Tile tensors whose full tiles go to the bulk-copy kernel as 2-D tensor
-    // copies: tile width a power of two in [32, 256], k = 256 / width tiles
-    // per work unit (one copy box of 256 columns), whole boxes of rows per
-    // tile, 16-element aligned rows and offset.
-    int map = -1;
-    int64_t k = 1;
-    if (x.gran == VSF_GRAN_TILE && (int)plan->tile_maps.size() < vsf::kMaxTileMaps) {
-      const int64_t bc = x.tile_cols, br = x.block_rows;
-      if (bc >= 32 && bc <= 256 && (bc & (bc - 1)) == 0) {
-        k = std::min<int64_t>(256 / bc, vsf::kMaxUnitTiles);
-        const int64_t box_cols = k * bc;
-        const int64_t box_rows = std::min<int64_t>(br, vsf::kTmaChunkElems / box_cols);
-        if (box_rows >= 1 && box_rows <= 256 && br % box_rows == 0 && x.cols % 16 == 0 &&
-            x.offset % 16 == 0 && x.cols >= box_cols) {
-          vsf::TileMapInfo mi;
-          mi.tensor = t;
-          mi.tile_cols = (int32_t)bc;
-          mi.k = (int32_t)k;
-          mi.box_cols = (int32_t)box_cols;
-          mi.box_rows = (int32_t)box_rows;
-          mi.rows = x.rows;
-          mi.cols = x.cols;
-          mi.offset = x.offset;
-          map = (int)plan->tile_maps.size();
-          plan->tile_maps.push_back(mi);
-        }
-      }
-    }
-    // Where a block goes: element chunks to the warp kernel; contiguous
-    // blocks that start on 16 elements and hold a multiple of 16, and full
-    // tiles grouped k at a time, to the bulk-copy (TMA) kernel; every other
-    // row or tile block (ragged, unaligned, leftover) to the register kernel.
-    enum Dest { kSmall, kTma, kTmaTile, kTmaTileMember, kRegister };
-    auto add = [&](int64_t base, int64_t nr, int64_t nc, int64_t st, Dest dest, int64_t r0,
-                   int64_t c0) {
-      vsf::QBlock b{};
-      b.base = base;
-      b.nrows = (int32_t)nr;
-      b.ncols = (int32_t)nc;
-      b.stride = (int32_t)st;
-      b.tensor = t;
-      b.tx = -1;
-      b.ty = -1;
-      const int32_t q = (int32_t)plan->qblocks.size();
-      if (dest == kTmaTile || dest == kTmaTileMember) {
-        b.tx = (int32_t)c0;
-        b.ty = (int32_t)r0;
-      }
-      if (dest == kSmall) {
-        plan->small_blocks.push_back(q);
-      } else if (dest == kTma || dest == kTmaTile) {
-        plan->tma_blocks.push_back(q);
-        plan->tma_tiles.push_back(dest == kTmaTile ? (int32_t)k : 1);
-        plan->max_tma_elems = std::max(plan->max_tma_elems, nr * nc * (dest == kTmaTile ? k : 1));
-      } else if (dest == kRegister) {
-        plan->big_blocks.push_back(q);
-        plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
-      }
-      plan->qblocks.push_back(b);
-    };
-    if (x.gran == VSF_GRAN_ELEM) {
-      if (g_coll > INT32_MAX) {
-        delete plan;
-        return fail(VSF_ERR_OVERFLOW, "g_coll too large for element-granular blocks");
-      }
-      for (int64_t e = 0; e < x.numel; e += g_coll) {
-        int64_t len = std::min(g_coll, x.numel - e);
-        add(x.offset + e, 1, len, len, kSmall, 0, e);
-      }
-    } else if (x.gran == VSF_GRAN_ROWS) {
-      for (int64_t r = 0; r < x.rows; r += x.block_rows) {
-        const int64_t nr = std::min(x.block_rows, x.rows - r);
-        // a whole-row block is contiguous: one row of nr*cols elements
-        if (nr * x.cols > INT32_MAX) {
-          delete plan;
-          return fail(VSF_ERR_OVERFLOW, "quantisation block larger than 2^31 elements");
-        }
-        const int64_t base = x.offset + r * x.cols, len = nr * x.cols;
-        add(base, 1, len, len, base % 16 == 0 && len % 16 == 0 ? kTma : kRegister, r, 0);
-      }
-    } else {
-      if (x.cols > INT32_MAX || x.rows > INT32_MAX) {
-        delete plan;
-        return fail(VSF_ERR_OVERFLOW, "tile tensor dimension beyond 2^31");
-      }
-      const int64_t tc = x.tile_cols;
-      for (int64_t r = 0; r < x.rows; r += x.block_rows) {
-        const int64_t nr = std::min(x.block_rows, x.rows - r);
-        const int64_t full = nr == x.block_rows ? x.cols / tc : 0;  // full tiles in the stripe
-        const int64_t grouped = map >= 0 ? full / k * k : 0;       // of them, in whole units
-        for (int64_t c = 0, i = 0; c < x.cols; c += tc, ++i) {
-          const int64_t nc = std::min(tc, x.cols - c);
-          const Dest dest = i < grouped ? (i % k == 0 ? kTmaTile : kTmaTileMember) : kRegister;
-          add(x.offset + r * x.cols + c, nr, nc, x.cols, dest, r, c);
-        }
-      }
-    }
+  const vsf_status st = vsf::build_tables(plan, 0, m);
+  if (st != VSF_OK) {
+    delete plan;
+    return st;
   }
-
-  // Device workspace layout (16-byte aligned sections).
-  vsf::DeviceLayout& L = plan->layout;
-  size_t cur = 0;
-  auto section = [&](size_t bytes) {
-    size_t at = (cur + 255) / 256 * 256;
-    cur = at + bytes;
-    return at;
-  };
-  L.tensor_off = section(sizeof(int64_t) * n);
-  L.tensor_numel = section(sizeof(int64_t) * n);
-  L.qblocks = section(sizeof(vsf::QBlock) * plan->qblocks.size());
-  L.big = section(sizeof(int32_t) * std::max<size_t>(1, plan->big_blocks.size()));
-  L.small = section(sizeof(int32_t) * std::max<size_t>(1, plan->small_blocks.size()));
-  L.tma = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_blocks.size()));
-  L.tma_k = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_tiles.size()));
-  L.error = section(16);
-  L.spans = section(sizeof(vsf::CopySpan) * (vsf::kMaxCopyGrid + 1));
-  L.partials = section(sizeof(double) * vsf::kMaxCopyGrid);
-  L.bytes = (cur + 255) / 256 * 256;
-
   plan->plan_seconds =
       std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
   *out = plan;
   return VSF_OK;
+}
+
+vsf_status vsf_plan_restrict(vsf_plan* plan, int32_t rank_begin, int32_t rank_end) {
+  if (plan == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_restrict: NULL plan");
+  if (plan->uploaded) return fail(VSF_ERR_STATE, "vsf_plan_restrict: plan already uploaded");
+  if (rank_begin < 0 || rank_end > plan->m || rank_begin >= rank_end)
+    return fail(VSF_ERR_ARG, "vsf_plan_restrict: need 0 <= rank_begin < rank_end <= m");
+  return vsf::build_tables(plan, rank_begin, rank_end);
 }
 
 void vsf_plan_destroy(vsf_plan* plan) { delete plan; }
@@ -350,6 +392,8 @@ vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info) {
   info->n_bulk_units = (int64_t)plan->tma_blocks.size();
   info->n_register_blocks = (int64_t)plan->big_blocks.size();
   info->n_element_chunks = (int64_t)plan->small_blocks.size();
+  info->rank_begin = plan->rank_begin;
+  info->rank_end = plan->rank_end;
   return VSF_OK;
 }
 
@@ -417,6 +461,8 @@ vsf_status vsf_plan_views(const vsf_plan* plan, const void* packed, int32_t elem
     return fail(VSF_ERR_ARG, "vsf_plan_views: NULL argument");
   if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4)
     return fail(VSF_ERR_ARG, "vsf_plan_views: elem_bytes must be 1, 2 or 4");
+  if (plan->rank_begin != 0 || plan->rank_end != plan->m)
+    return fail(VSF_ERR_STATE, "vsf_plan_views: whole tensors live only in an unrestricted plan");
   for (int t = 0; t < plan->n; ++t)
     views[t] = const_cast<char*>(static_cast<const char*>(packed)) +
                plan->tensors[t].offset * (int64_t)elem_bytes;

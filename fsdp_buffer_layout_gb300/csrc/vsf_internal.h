@@ -40,8 +40,8 @@ struct QBlock {
 };
 static_assert(sizeof(QBlock) == 32, "QBlock is a 32-byte device record");
 
-// Where one CTA of the copy grid starts in the concatenation of all real
-// elements (tensor order).
+// Where one CTA of the copy grid starts in the concatenation of the real
+// elements the plan covers (tensor order; each tensor's [lo, hi) range).
 struct CopySpan {
   int32_t tensor;
   int32_t pad;
@@ -58,7 +58,7 @@ struct TileMapInfo {
   int32_t tensor;
   int32_t tile_cols, k;        // tile width; tiles per work unit
   int32_t box_cols, box_rows;  // one copy = box_rows rows of box_cols = k * tile_cols elements
-  int64_t rows, cols, offset;  // the tensor's 2-D view inside the buffer
+  int64_t rows, cols, offset;  // the 2-D view (rows inside the plan's window) in the buffer
 };
 
 struct TensorInfo {
@@ -68,11 +68,13 @@ struct TensorInfo {
   int32_t gran;
   int64_t block_rows, tile_cols;
   int64_t atom, align;
-  int64_t offset;
+  int64_t offset;  // global buffer element of the tensor's first element
+  int64_t lo, hi;  // the tensor's elements inside the plan's rank window
 };
 
 struct DeviceLayout {
-  size_t tensor_off = 0, tensor_numel = 0;  // int64[n] each
+  size_t tensor_off = 0;                    // int64[n]: offset minus the window start
+  size_t tensor_lo = 0, tensor_hi = 0;      // int64[n]: element range inside the window
   size_t qblocks = 0;                       // QBlock[n_qblocks]
   size_t big = 0, small = 0, tma = 0;       // int32 lists of block indices
   size_t tma_k = 0;                         // int32 tiles per TMA work unit
@@ -86,8 +88,11 @@ struct DeviceLayout {
 
 struct vsf_plan {
   int32_t n = 0, m = 0;
-  int64_t g_coll = 0, S = 0, total = 0, real = 0;
+  int64_t g_coll = 0, S = 0, total = 0, real = 0;  // total, real: inside the rank window
   int32_t order_used = 0;
+  // Rank window [rank_begin, rank_end): buffers passed to the per-step calls
+  // hold elements [rank_begin * S, rank_end * S) of the planned buffer.
+  int32_t rank_begin = 0, rank_end = 0;
   double plan_seconds = 0.0;
   std::vector<vsf::TensorInfo> tensors;
   std::vector<vsf::QBlock> qblocks;
@@ -120,4 +125,5 @@ struct vsf_plan {
 
 namespace vsf {
 vsf_status fail(vsf_status s, const std::string& msg);
+vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1);
 }  // namespace vsf

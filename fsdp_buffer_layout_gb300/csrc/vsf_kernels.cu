@@ -130,7 +130,7 @@ __device__ __forceinline__ float elem_f32(float f) { return f; }
 template <typename T, int kMode>
 __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
                                                             const int64_t* __restrict__ t_off,
-                                                            const int64_t* __restrict__ t_numel,
+                                                            const int64_t* __restrict__ t_lo, const int64_t* __restrict__ t_hi,
                                                             const CopySpan* __restrict__ spans,
                                                             T* packed, double* partials) {
   constexpr int V = 16 / sizeof(T);
@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
   const CopySpan s1 = spans[blockIdx.x + 1];
   DF acc;
   for (int t = s0.tensor; t <= s1.tensor; ++t) {
-    const int64_t b = (t == s0.tensor) ? s0.elem : 0;
-    const int64_t e = (t == s1.tensor) ? s1.elem : t_numel[t];
+    const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
+    const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
     if (b >= e) continue;
     T* pk = packed + t_off[t];
     T* tp = const_cast<T*>(static_cast<const T*>(ptrs.p[t]));
@@ -192,9 +192,9 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
 
 // One CTA: fixed-order fp64 sum of the per-CTA partials, then the group
 // scale factor (clip and 1/world).
-__global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __restrict__ partials,
-                                                            int n, int world, double max_norm,
-                                                            float* d_factor, double* d_norm) {
+// Fixed-order fp64 sum of n partials by one CTA of 256 threads; the result
+// is valid in thread 0.
+__device__ __forceinline__ double reduce_partials(const double* __restrict__ partials, int n) {
   __shared__ double red[256];
   double s = 0.0;
   for (int i = threadIdx.x; i < n; i += 256) s += partials[i];
@@ -204,16 +204,39 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __rest
     if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    const double norm = sqrt(red[0]) / (double)world;
-    double c = 1.0;
-    if (isfinite(max_norm) && max_norm > 0.0) {
-      const double r = max_norm / (norm + 1e-6);
-      if (r < 1.0) c = r;
-    }
-    *d_factor = __double2float_rn(c / (double)world);
-    if (d_norm) *d_norm = norm;
+  return red[0];
+}
+
+// norm = sqrt(sum of squares) / world; clip c = min(1, max_norm / (norm +
+// 1e-6)) when max_norm is finite and positive; factor = fp32(c / world).
+__device__ __forceinline__ void norm_factor(double sumsq, int world, double max_norm,
+                                            float* d_factor, double* d_norm) {
+  const double norm = sqrt(sumsq) / (double)world;
+  double c = 1.0;
+  if (isfinite(max_norm) && max_norm > 0.0) {
+    const double r = max_norm / (norm + 1e-6);
+    if (r < 1.0) c = r;
   }
+  *d_factor = __double2float_rn(c / (double)world);
+  if (d_norm) *d_norm = norm;
+}
+
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __restrict__ partials,
+                                                            int n, int world, double max_norm,
+                                                            float* d_factor, double* d_norm) {
+  const double s = reduce_partials(partials, n);
+  if (threadIdx.x == 0) norm_factor(s, world, max_norm, d_factor, d_norm);
+}
+
+__global__ void __launch_bounds__(256) sumsq_kernel(const double* __restrict__ partials, int n,
+                                                    double* d_sumsq) {
+  const double s = reduce_partials(partials, n);
+  if (threadIdx.x == 0) *d_sumsq = s;
+}
+
+__global__ void factor_kernel(const double* __restrict__ d_sumsq, int world, double max_norm,
+                              float* d_factor, double* d_norm) {
+  norm_factor(*d_sumsq, world, max_norm, d_factor, d_norm);
 }
 
 #include "adam8.cuh"
@@ -224,13 +247,13 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const double* __rest
 // fp32 arithmetic with one rounding, then the buffer's type (bf16 RNE).
 template <typename DT, typename ST, int kOp>
 __global__ void __launch_bounds__(kCopyThreads) group_op_kernel(
-    const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_numel,
+    const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_lo, const int64_t* __restrict__ t_hi,
     const CopySpan* __restrict__ spans, DT* dst, const ST* __restrict__ src, float alpha) {
   const CopySpan s0 = spans[blockIdx.x];
   const CopySpan s1 = spans[blockIdx.x + 1];
   for (int t = s0.tensor; t <= s1.tensor; ++t) {
-    const int64_t b = (t == s0.tensor) ? s0.elem : 0;
-    const int64_t e = (t == s1.tensor) ? s1.elem : t_numel[t];
+    const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
+    const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
     const int64_t base = t_off[t];
     for (int64_t i = b + threadIdx.x; i < e; i += kCopyThreads) {
       const int64_t x = base + i;
@@ -333,7 +356,8 @@ vsf_status launch_copy(const vsf_plan* plan, const void* const* tensors, void* p
   }
   copy_kernel<T, kMode><<<plan->copy_grid, kCopyThreads, 0, st>>>(
       ptrs, ws_ptr<int64_t>(plan, plan->layout.tensor_off),
-      ws_ptr<int64_t>(plan, plan->layout.tensor_numel),
+      ws_ptr<int64_t>(plan, plan->layout.tensor_lo),
+      ws_ptr<int64_t>(plan, plan->layout.tensor_hi),
       ws_ptr<CopySpan>(plan, plan->layout.spans), static_cast<T*>(packed),
       reinterpret_cast<double*>(plan->d_ws + plan->layout.partials));
   cudaError_t e = cudaGetLastError();
@@ -412,7 +436,8 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
   if (!quantized) {
     adam_fp32_kernel<GT><<<plan->copy_grid, kCopyThreads, 0, st>>>(
         ws_ptr<int64_t>(plan, plan->layout.tensor_off),
-        ws_ptr<int64_t>(plan, plan->layout.tensor_numel),
+        ws_ptr<int64_t>(plan, plan->layout.tensor_lo),
+      ws_ptr<int64_t>(plan, plan->layout.tensor_hi),
         ws_ptr<CopySpan>(plan, plan->layout.spans), g, d_factor, master,
         static_cast<float*>(m_state), static_cast<float*>(v_state), bf, k);
     cudaError_t e = cudaGetLastError();
@@ -496,12 +521,14 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload");
 
-  // Copy grid: equal spans of the real elements, cut on 8-element multiples.
+  // Copy grid: equal spans of the real elements inside the rank window
+  // (each tensor's [lo, hi)), cut on 8-element multiples.
   const int grid = std::max(1, std::min(kMaxCopyGrid, sms * kCopyCtasPerSm));
   std::vector<CopySpan> spans(grid + 1);
   {
     std::vector<int64_t> starts(plan->n + 1, 0);
-    for (int t = 0; t < plan->n; ++t) starts[t + 1] = starts[t] + plan->tensors[t].numel;
+    for (int t = 0; t < plan->n; ++t)
+      starts[t + 1] = starts[t] + (plan->tensors[t].hi - plan->tensors[t].lo);
     int t = 0;
     for (int c = 0; c <= grid; ++c) {
       int64_t pos = (c == grid) ? plan->real : (plan->real / grid * c) / 8 * 8;
@@ -509,7 +536,7 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
       if (c == grid) t = plan->n - 1;
       spans[c].tensor = t;
       spans[c].pad = 0;
-      spans[c].elem = pos - starts[t];
+      spans[c].elem = plan->tensors[t].lo + (pos - starts[t]);
     }
   }
 
@@ -588,8 +615,10 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   img.assign(plan->layout.spans + sizeof(CopySpan) * (grid + 1), 0);
   const DeviceLayout& L = plan->layout;
   for (int t = 0; t < plan->n; ++t) {
-    std::memcpy(&img[L.tensor_off + 8 * t], &plan->tensors[t].offset, 8);
-    std::memcpy(&img[L.tensor_numel + 8 * t], &plan->tensors[t].numel, 8);
+    const int64_t off = plan->tensors[t].offset - (int64_t)plan->rank_begin * plan->S;
+    std::memcpy(&img[L.tensor_off + 8 * t], &off, 8);
+    std::memcpy(&img[L.tensor_lo + 8 * t], &plan->tensors[t].lo, 8);
+    std::memcpy(&img[L.tensor_hi + 8 * t], &plan->tensors[t].hi, 8);
   }
   if (!plan->qblocks.empty())
     std::memcpy(&img[L.qblocks], plan->qblocks.data(), sizeof(QBlock) * plan->qblocks.size());
@@ -637,6 +666,10 @@ vsf_status vsf_group_norm_scale(const vsf_plan* plan, const void* packed_grad, i
                                 void* stream) {
   vsf_status s = check_ready(plan, "vsf_group_norm_scale");
   if (s != VSF_OK) return s;
+  if (plan->rank_begin != 0 || plan->rank_end != plan->m)
+    return fail(VSF_ERR_STATE,
+                "vsf_group_norm_scale: the plan covers a rank window; use vsf_group_sumsq, "
+                "sum across windows, then vsf_group_scale_from_sumsq");
   if (hp == nullptr || d_factor == nullptr) return fail(VSF_ERR_ARG, "vsf_group_norm_scale: NULL");
   if (hp->world < 1) return fail(VSF_ERR_ARG, "vsf_group_norm_scale: world must be >= 1");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -657,6 +690,41 @@ vsf_status vsf_group_norm_scale(const vsf_plan* plan, const void* packed_grad, i
       hp->world, hp->max_norm, d_factor, d_norm);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_group_norm_scale");
+}
+
+vsf_status vsf_group_sumsq(const vsf_plan* plan, const void* packed_grad, int32_t dtype,
+                           double* d_sumsq, void* stream) {
+  vsf_status s = check_ready(plan, "vsf_group_sumsq");
+  if (s != VSF_OK) return s;
+  if (d_sumsq == nullptr) return fail(VSF_ERR_ARG, "vsf_group_sumsq: NULL d_sumsq");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (packed_grad != nullptr) {
+    if (misaligned(packed_grad)) return fail(VSF_ERR_ALIGN, "vsf_group_sumsq: alignment");
+    if (dtype == VSF_BF16)
+      s = launch_copy<uint16_t, kNormOnly>(plan, nullptr, const_cast<void*>(packed_grad), st,
+                                           "vsf_group_sumsq");
+    else if (dtype == VSF_FP32)
+      s = launch_copy<float, kNormOnly>(plan, nullptr, const_cast<void*>(packed_grad), st,
+                                        "vsf_group_sumsq");
+    else
+      return fail(VSF_ERR_ARG, "vsf_group_sumsq: dtype must be VSF_BF16 or VSF_FP32");
+    if (s != VSF_OK) return s;
+  }
+  sumsq_kernel<<<1, 256, 0, st>>>(reinterpret_cast<const double*>(plan->d_ws + plan->layout.partials),
+                                  plan->copy_grid, d_sumsq);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_group_sumsq");
+}
+
+vsf_status vsf_group_scale_from_sumsq(const double* d_sumsq, const vsf_adam_hparams* hp,
+                                      float* d_factor, double* d_norm, void* stream) {
+  if (d_sumsq == nullptr || hp == nullptr || d_factor == nullptr)
+    return fail(VSF_ERR_ARG, "vsf_group_scale_from_sumsq: NULL argument");
+  if (hp->world < 1) return fail(VSF_ERR_ARG, "vsf_group_scale_from_sumsq: world must be >= 1");
+  factor_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(d_sumsq, hp->world, hp->max_norm,
+                                                                 d_factor, d_norm);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_group_scale_from_sumsq");
 }
 
 vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t grad_dtype,
@@ -709,7 +777,8 @@ vsf_status launch_group(const vsf_plan* plan, void* dst, const void* src, float 
                         cudaStream_t st, const char* who) {
   group_op_kernel<DT, ST, kOp><<<plan->copy_grid, kCopyThreads, 0, st>>>(
       ws_ptr<int64_t>(plan, plan->layout.tensor_off),
-      ws_ptr<int64_t>(plan, plan->layout.tensor_numel),
+      ws_ptr<int64_t>(plan, plan->layout.tensor_lo),
+      ws_ptr<int64_t>(plan, plan->layout.tensor_hi),
       ws_ptr<CopySpan>(plan, plan->layout.spans), static_cast<DT*>(dst),
       static_cast<const ST*>(src), alpha);
   cudaError_t e = cudaGetLastError();

@@ -23,6 +23,10 @@ class TensorSpec:
 class ShardStep:
     """One DBuffer of m virtual ranks on the current CUDA device.
 
+    With ranks=(r0, r1) the plan is restricted to virtual ranks [r0, r1): the
+    packed buffers hold that window only ((r1 - r0) * S elements) and the
+    norm is split (group_sumsq, an all-reduce by the caller, scale_from_sumsq).
+
     Buffers (m*S elements each unless noted): packed_grad (bf16 or fp32),
     master (fp32), m_state / v_state (int8 / uint8 codes, or fp32 when
     quantized=False), m_scale / v_scale (fp32, one per quantisation block),
@@ -32,13 +36,16 @@ class ShardStep:
     def __init__(self, specs, m: int, g_coll: int, *, order: int = V.VSF_ORDER_DEFAULT,
                  grad_dtype: int = V.VSF_BF16, quantized: bool = True, lr=1e-3, beta1=0.9,
                  beta2=0.999, eps=1e-8, weight_decay=0.01, max_norm=float("inf"),
-                 world: int | None = None, device=None, stream: torch.cuda.Stream | None = None):
+                 world: int | None = None, device=None, stream: torch.cuda.Stream | None = None,
+                 ranks: tuple[int, int] | None = None):
         self.specs = list(specs)
         self.m, self.g_coll = m, g_coll
         self.grad_dtype = grad_dtype
         self.quantized = quantized
         descs = [V.make_desc(s.shape, s.gran, s.block_rows, s.tile_cols) for s in self.specs]
         self.plan = V.vsf_plan_create(descs, m, g_coll, order)
+        if ranks is not None:  # this process owns virtual ranks [r0, r1) only
+            V.vsf_plan_restrict(self.plan, int(ranks[0]), int(ranks[1]))
         self.info = V.vsf_plan_get_info(self.plan)
         self.offsets = V.vsf_plan_offsets(self.plan, len(self.specs))
         self.numels = [int(torch.Size(s.shape).numel()) for s in self.specs]
@@ -63,6 +70,7 @@ class ShardStep:
             self.packed_bf16 = torch.zeros(total, dtype=torch.bfloat16, device=dev)
             self.factor = torch.zeros(4, dtype=torch.float32, device=dev)
             self.norm = torch.zeros(2, dtype=torch.float64, device=dev)
+            self.sumsq = torch.zeros(2, dtype=torch.float64, device=dev)
             V.vsf_plan_upload(self.plan, self.workspace.data_ptr(), self.workspace.numel(),
                               self.stream.cuda_stream)
 
@@ -86,6 +94,16 @@ class ShardStep:
         V.vsf_group_norm_scale(self.plan, self.packed_grad.data_ptr() if standalone else None,
                                self.grad_dtype, self.hp, self.factor.data_ptr(),
                                self.norm.data_ptr(), self.stream.cuda_stream)
+
+    def group_sumsq(self, standalone: bool = False):
+        """This window's fp64 sum of squares into self.sumsq[0] (device)."""
+        V.vsf_group_sumsq(self.plan, self.packed_grad.data_ptr() if standalone else None,
+                          self.grad_dtype, self.sumsq.data_ptr(), self.stream.cuda_stream)
+
+    def scale_from_sumsq(self, total: torch.Tensor):
+        """Factor and norm from the sum of squares over every window (device fp64)."""
+        V.vsf_group_scale_from_sumsq(total.data_ptr(), self.hp, self.factor.data_ptr(),
+                                     self.norm.data_ptr(), self.stream.cuda_stream)
 
     def adam(self, step: int):
         V.vsf_adam8_step(self.plan, self.packed_grad.data_ptr(), self.grad_dtype,

@@ -44,7 +44,8 @@ class vsf_plan_info(ctypes.Structure):
                 ("padding_ratio", ctypes.c_double), ("plan_seconds", ctypes.c_double),
                 ("order_used", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("n_bulk_units", ctypes.c_int64), ("n_register_blocks", ctypes.c_int64),
-                ("n_element_chunks", ctypes.c_int64)]
+                ("n_element_chunks", ctypes.c_int64), ("rank_begin", ctypes.c_int32),
+                ("rank_end", ctypes.c_int32)]
 
 
 class vsf_muon_hparams(ctypes.Structure):
@@ -93,6 +94,12 @@ def lib():
             L.vsf_plan_upload.argtypes = [vp, vp, ctypes.c_size_t, vp]
             L.vsf_pack.restype = st
             L.vsf_pack.argtypes = [vp, P(vp), i32, vp, vp]
+            L.vsf_plan_restrict.restype = st
+            L.vsf_plan_restrict.argtypes = [vp, i32, i32]
+            L.vsf_group_sumsq.restype = st
+            L.vsf_group_sumsq.argtypes = [vp, vp, i32, vp, vp]
+            L.vsf_group_scale_from_sumsq.restype = st
+            L.vsf_group_scale_from_sumsq.argtypes = [vp, P(vsf_adam_hparams), vp, vp, vp]
             L.vsf_group_norm_scale.restype = st
             L.vsf_group_norm_scale.argtypes = [vp, vp, i32, P(vsf_adam_hparams), vp, vp, vp]
             L.vsf_adam8_step.restype = st
@@ -163,6 +170,19 @@ def vsf_plan_create(descs, m: int, g_coll: int, order: int = VSF_ORDER_DEFAULT) 
 
 def vsf_plan_destroy(plan: int) -> None:
     lib().vsf_plan_destroy(plan)
+
+
+def vsf_plan_restrict(plan: int, rank_begin: int, rank_end: int) -> None:
+    _check(lib().vsf_plan_restrict(plan, rank_begin, rank_end))
+
+
+def vsf_group_sumsq(plan: int, packed_grad, dtype: int, d_sumsq: int, stream: int) -> None:
+    _check(lib().vsf_group_sumsq(plan, packed_grad, dtype, d_sumsq, stream))
+
+
+def vsf_group_scale_from_sumsq(d_sumsq: int, hp: vsf_adam_hparams, d_factor: int, d_norm,
+                               stream: int) -> None:
+    _check(lib().vsf_group_scale_from_sumsq(d_sumsq, ctypes.byref(hp), d_factor, d_norm, stream))
 
 
 def vsf_plan_get_info(plan: int) -> vsf_plan_info:

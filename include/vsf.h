@@ -88,9 +88,9 @@ typedef struct {
 
 typedef struct {
   int64_t S;             /* uniform per-rank size in elements */
-  int64_t total;         /* m * S, elements of every packed buffer */
-  int64_t real;          /* real (non-padding) elements */
-  int64_t n_qblocks;     /* quantisation blocks = entries of m_scale / v_scale */
+  int64_t total;         /* elements of every packed buffer: (rank_end - rank_begin) * S */
+  int64_t real;          /* real (non-padding) elements inside the rank window */
+  int64_t n_qblocks;     /* quantisation blocks in the window = entries of m_scale / v_scale */
   int32_t n_tensors, m;
   int64_t g_coll;
   double padding_ratio;  /* 1 - real / total */
@@ -101,6 +101,7 @@ typedef struct {
    * bulk-copy work units (contiguous blocks, or k full tiles), blocks of the
    * register kernel (ragged or unaligned), element-granular chunks */
   int64_t n_bulk_units, n_register_blocks, n_element_chunks;
+  int32_t rank_begin, rank_end; /* the plan's rank window (0, m unless restricted) */
 } vsf_plan_info;
 
 typedef struct vsf_plan vsf_plan; /* opaque */
@@ -117,6 +118,28 @@ vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, i
                            int32_t order, vsf_plan** out);
 void vsf_plan_destroy(vsf_plan* plan);
 
+/* Restricts a plan, before vsf_plan_upload, to the virtual ranks
+ * [rank_begin, rank_end): the part of the DBuffer one process owns ([VSF]
+ * 核心方法 › RaggedShard and Distributed Buffer: each rank holds its own
+ * slice; no quantisation block crosses a rank boundary, so every block lies
+ * in one window). The layout (S, offsets) is unchanged. Afterwards:
+ *   - every packed buffer passed to a per-step call holds the window, i.e.
+ *     elements [rank_begin*S, rank_end*S) of the planned buffer, indexed from
+ *     0 (total = (rank_end - rank_begin) * S);
+ *   - vsf_pack / vsf_unpack / group ops touch only the window's elements
+ *     (per-tensor tensors stay whole: element i of tensor t is copied when
+ *     offset_t + i falls in the window);
+ *   - the quantisation-block table, n_qblocks and the scale arrays cover the
+ *     window's blocks only, with bases counted from the window start;
+ *   - the gradient norm needs every window: vsf_group_sumsq gives this
+ *     window's sum of squares, the caller adds the windows' sums (an
+ *     all-reduce of one fp64 value), and vsf_group_scale_from_sumsq turns the
+ *     total into the factor. vsf_group_norm_scale, vsf_plan_views and
+ *     vsf_muon_step need whole tensors and return VSF_ERR_STATE.
+ * Calling it again replaces the window. Errors: VSF_ERR_ARG (NULL plan, not
+ * 0 <= rank_begin < rank_end <= m), VSF_ERR_STATE (already uploaded). */
+vsf_status vsf_plan_restrict(vsf_plan* plan, int32_t rank_begin, int32_t rank_end);
+
 vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info);
 
 /* Per-tensor element offsets into the m*S buffer; offsets has n entries. */
@@ -124,8 +147,9 @@ vsf_status vsf_plan_offsets(const vsf_plan* plan, int64_t* offsets);
 
 /* Quantisation-block table, in tensor order then stripe, then tile: block q
  * is the row-major region of nrows rows x ncols elements starting at buffer
- * element base[q], rows `stride` elements apart, of tensor tensor[q]. Arrays
- * have n_qblocks entries (any may be NULL). */
+ * element base[q] (counted from the rank window's start), rows `stride`
+ * elements apart, of tensor tensor[q]. Arrays have n_qblocks entries (any
+ * may be NULL). */
 vsf_status vsf_plan_qblocks(const vsf_plan* plan, int32_t* tensor, int64_t* base, int64_t* nrows,
                             int64_t* ncols, int64_t* stride);
 
@@ -180,10 +204,24 @@ vsf_status vsf_pack(const vsf_plan* plan, const void* const* grads, int32_t dtyp
  * else 1; writes *d_factor = fp32(c / world) and *d_norm = norm (both device
  * pointers; d_norm may be NULL). With packed_grad == NULL the partial sums
  * left by the last vsf_pack on this plan are used; otherwise they are
- * recomputed from packed_grad (element type dtype). */
+ * recomputed from packed_grad (element type dtype). A plan restricted to a
+ * rank window gets VSF_ERR_STATE: its norm needs the other windows. */
 vsf_status vsf_group_norm_scale(const vsf_plan* plan, const void* packed_grad, int32_t dtype,
                                 const vsf_adam_hparams* hp, float* d_factor, double* d_norm,
                                 void* stream);
+
+/* The same norm split at its one cross-rank exchange, for plans restricted
+ * to a rank window (vsf_plan_restrict). vsf_group_sumsq writes the window's
+ * fp64 sum of g^2 to *d_sumsq (device), from the last vsf_pack's partials
+ * (packed_grad == NULL) or from packed_grad. vsf_group_scale_from_sumsq takes
+ * the total over all windows (device fp64; the caller's all-reduce) and
+ * writes *d_factor and *d_norm exactly as vsf_group_norm_scale does; it needs
+ * no plan. Errors: VSF_ERR_ARG (NULL, world < 1, bad dtype), VSF_ERR_ALIGN,
+ * VSF_ERR_STATE (plan not uploaded), VSF_ERR_CUDA. */
+vsf_status vsf_group_sumsq(const vsf_plan* plan, const void* packed_grad, int32_t dtype,
+                           double* d_sumsq, void* stream);
+vsf_status vsf_group_scale_from_sumsq(const double* d_sumsq, const vsf_adam_hparams* hp,
+                                      float* d_factor, double* d_norm, void* stream);
 
 /* Block-wise 8-bit AdamW on every virtual rank's RaggedShard slice ([VSF]
  * case study › 8-bit Adam; blocks never cross a rank, so every scale is

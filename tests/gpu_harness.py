@@ -133,6 +133,94 @@ def run_gpu(case: Case):
         ss.close()
 
 
+def run_gpu_windows(case: Case, windows):
+    """The same steps with the DBuffer split into rank windows [r0, r1), one
+    ShardStep per window (as separate processes would hold them), run one
+    after another on one GPU. The norm's one exchange is the sum of the
+    windows' fp64 sums of squares (on the device). Results are stitched into
+    whole-buffer arrays: buffers by window, scales through the block table."""
+    from fsdp_buffer_layout_gb300 import vsf as V
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    specs = [TensorSpec(tuple(s[0]), s[1], s[2], s[3]) for s in case.specs]
+    sss = []
+    try:
+        for r0, r1 in windows:
+            sss.append(ShardStep(specs, case.m, case.g_coll, grad_dtype=case.grad_dtype,
+                                 quantized=case.quantized, max_norm=case.max_norm,
+                                 world=case.world, ranks=(r0, r1)))
+        dev = sss[0].device
+        S, offs = sss[0].info.S, sss[0].offsets
+        for ss, (r0, r1) in zip(sss, windows):
+            lo, hi = r0 * S, r1 * S
+            for t in range(len(specs)):
+                m, o = case.masters(t), offs[t]
+                a, b = max(lo, o), min(hi, o + m.size)
+                if a < b:
+                    ss.master[a - lo:b - lo].copy_(torch.from_numpy(m[a - o:b - o]).to(dev))
+        gdt = torch.int16 if case.grad_dtype == 0 else torch.float32
+        grads = [torch.empty(n, dtype=gdt, device=dev) for n in case.numels]
+        params = [torch.empty(n, dtype=torch.int16, device=dev) for n in case.numels]
+        factors, norms = [], []
+        for s in range(1, case.steps + 1):
+            for t, g in enumerate(grads):
+                h = case.grads(s, t)
+                g.copy_(torch.from_numpy(h.view(np.int16) if case.grad_dtype == 0 else h))
+            for ss in sss:
+                ss.pack(grads)
+                ss.group_sumsq(standalone=case.standalone_norm)
+            total = sss[0].sumsq[:1].clone()
+            for ss in sss[1:]:
+                total += ss.sumsq[:1]
+            for ss in sss:
+                ss.scale_from_sumsq(total)
+                ss.adam(s)
+                ss.unpack(params)
+            torch.cuda.synchronize()
+            for ss in sss:
+                assert ss.device_error() == 0, "a bounded device wait ran out"
+                assert float(ss.factor[0].item()) == float(sss[0].factor[0].item())
+            factors.append(float(sss[0].factor[0].item()))
+            norms.append(float(sss[0].norm[0].item()))
+
+        def host(x):
+            if x.dtype == torch.bfloat16:
+                x = x.view(torch.int16)
+            return x.cpu().numpy()
+
+        total_elems = case.m * S
+        out = dict(S=S, offsets=np.array(offs), factors=factors, norms=norms,
+                   params=[host(p).view(np.uint16) for p in params])
+        for k in ("packed_grad", "master", "m_state", "v_state", "packed_bf16"):
+            parts = [host(getattr(ss, k)) for ss in sss]
+            whole = np.zeros(total_elems, dtype=parts[0].dtype)
+            for part, (r0, r1) in zip(parts, windows):
+                whole[r0 * S:r1 * S] = part
+            out[k] = whole
+        out["packed_bf16"] = out["packed_bf16"].view(np.uint16)
+        if case.grad_dtype == 0:
+            out["packed_grad"] = out["packed_grad"].view(np.uint16)
+        # scales: window block (tensor, base + r0*S) -> the whole plan's block index
+        whole_plan = V.vsf_plan_create([V.make_desc(*s) for s in case.specs], case.m, case.g_coll)
+        try:
+            nq = V.vsf_plan_get_info(whole_plan).n_qblocks
+            qb = V.vsf_plan_qblocks(whole_plan, nq)
+        finally:
+            V.vsf_plan_destroy(whole_plan)
+        index = {(qb["tensor"][q], qb["base"][q]): q for q in range(nq)}
+        for k in ("m_scale", "v_scale"):
+            whole = np.zeros(nq, np.float32)
+            for ss, (r0, r1) in zip(sss, windows):
+                lq = V.vsf_plan_qblocks(ss.plan, ss.info.n_qblocks)
+                vals = host(getattr(ss, k))
+                for q in range(ss.info.n_qblocks):
+                    whole[index[(lq["tensor"][q], lq["base"][q] + r0 * S)]] = vals[q]
+            out[k] = whole
+        return out
+    finally:
+        for ss in sss:
+            ss.close()
+
+
 def check_master(got, want, rtol=MASTER_RTOL):
     got = got.astype(np.float64)
     want = want.astype(np.float64)

@@ -42,15 +42,22 @@ def _worker(rank, world, port, max_norm, out):
             for r in range(rank * per, (rank + 1) * per):
                 for (t, e0, e1, _, _) in V.vsf_plan_rank_slices(plan, r):
                     pieces.append(np.ascontiguousarray(W.grad(w, 1, t)[e0:e1]))
+            # this process's own plan: restricted to its window of ranks
+            V.vsf_plan_restrict(plan, rank * per, (rank + 1) * per)
+            mine = V.vsf_plan_get_info(plan)
         finally:
             V.vsf_plan_destroy(plan)
+        counts = torch.tensor([mine.real, mine.n_qblocks, sum(p.size for p in pieces)],
+                              dtype=torch.int64)
+        assert counts[0] == counts[2]  # the window's real elements are its slices
+        dist.all_reduce(counts)
         local = oracle.sumsq(pieces) if pieces else 0.0
         total = torch.tensor([local], dtype=torch.float64)
         dist.all_reduce(total)
         factor, norm = oracle.factor(float(total.item()), w.m, max_norm)
         t = torch.tensor([1.0 + rank], dtype=torch.float64)  # a per-rank "time"
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        out[rank] = (factor, norm, float(t.item()), len(pieces))
+        out[rank] = (factor, norm, float(t.item()), len(pieces), int(counts[0]), int(counts[1]))
     finally:
         dist.destroy_process_group()
 
@@ -62,6 +69,13 @@ def test_two_rank_norm_matches_single_process(max_norm):
     w = W.tiny()
     whole = [W.grad(w, 1, t) for t in range(len(w.tensors))]
     want_f, want_n = oracle.factor(oracle.sumsq(whole), w.m, max_norm)
+    from fsdp_buffer_layout_gb300 import vsf as V
+    plan = V.vsf_plan_create([V.make_desc(t.shape, t.gran, t.block_rows, t.tile_cols)
+                              for t in w.tensors], w.m, w.g_coll)
+    try:
+        info = V.vsf_plan_get_info(plan)
+    finally:
+        V.vsf_plan_destroy(plan)
     ctx = mp.get_context("spawn")
     with ctx.Manager() as man:
         out = man.dict()
@@ -75,8 +89,9 @@ def test_two_rank_norm_matches_single_process(max_norm):
         res = dict(out)
     assert set(res) == {0, 1}
     for rank in (0, 1):
-        f, n, tmax, npieces = res[rank]
+        f, n, tmax, npieces, real, nq = res[rank]
         assert npieces > 0
+        assert (real, nq) == (info.real, info.n_qblocks)  # the windows partition the plan
         assert abs(n - want_n) <= 1e-12 * want_n
         if math.isinf(max_norm):
             assert f == want_f == np.float32(0.25)
