@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kSmallThreads) adam_small_kernel(
     const QBlock* __restrict__ qb, const int32_t* __restrict__ list, int nlist,
     const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
     uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k) {
+  // The bulk-copy kernel, launched next with programmatic serialization,
+  // touches other blocks only: let it start at once.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * (kSmallThreads / 32) + (threadIdx.x >> 5);
   if (j >= nlist) return;

@@ -442,4 +442,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
   }
   __syncwarp();
   cluster.sync();  // no CTA leaves while a peer may still write into it
+  // When launched alongside the element-chunk kernel (programmatic
+  // serialization), finish only after it, so that later launches on the
+  // stream see both kernels' writes. Returns at once otherwise.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }

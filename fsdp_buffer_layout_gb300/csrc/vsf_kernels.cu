@@ -445,6 +445,17 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
   }
   int8_t* mq = static_cast<int8_t*>(m_state);
   uint8_t* vq = static_cast<uint8_t*>(v_state);
+  // Element chunks first: a short kernel that lets the bulk-copy kernel start
+  // while it runs (the two touch disjoint blocks).
+  const int nsmall = (int)plan->small_blocks.size();
+  if (nsmall > 0) {
+    const int per = kSmallThreads / 32;
+    adam_small_kernel<GT><<<(nsmall + per - 1) / per, kSmallThreads, 0, st>>>(
+        qb, ws_ptr<int32_t>(plan, plan->layout.small), nsmall, g, d_factor, master, mq, vq,
+        m_scale, v_scale, bf, k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (element chunks)");
+  }
   const int ntma = (int)plan->tma_blocks.size();
   if (ntma > 0) {
     const int CL = plan->tma_cluster;
@@ -454,13 +465,16 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
     cfg.blockDim = dim3(kTmaThreads);
     cfg.dynamicSmemBytes = TmaLayout<GT>::total;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic serialization only right behind the element-chunk kernel
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = nsmall > 0 ? 2 : 1;
     TileMaps maps;
     vsf_status ms = tile_maps(plan, grad, sizeof(GT) == 2 ? VSF_BF16 : VSF_FP32, m_state, v_state,
                               master, &maps);
@@ -491,15 +505,6 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
                                        qb, ws_ptr<int32_t>(plan, plan->layout.big), nbig, ncl, g,
                                        d_factor, master, mq, vq, m_scale, v_scale, bf, k);
     if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (blocks)");
-  }
-  const int nsmall = (int)plan->small_blocks.size();
-  if (nsmall > 0) {
-    const int per = kSmallThreads / 32;
-    adam_small_kernel<GT><<<(nsmall + per - 1) / per, kSmallThreads, 0, st>>>(
-        qb, ws_ptr<int32_t>(plan, plan->layout.small), nsmall, g, d_factor, master, mq, vq,
-        m_scale, v_scale, bf, k);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (element chunks)");
   }
   return VSF_OK;
 }
