@@ -119,6 +119,40 @@ vsf_status fail(vsf_status s, const std::string& msg) {
   return s;
 }
 
+// Host-side check of the tables every kernel trusts: tensors inside the
+// buffer and disjoint; each tensor's blocks inside its elements of the rank
+// window (counted from the window start) and covering them exactly once.
+vsf_status check_tables(const vsf_plan& plan) {
+  const std::vector<TensorInfo>& ts = plan.tensors;
+  std::vector<int> by_offset(ts.size());
+  std::iota(by_offset.begin(), by_offset.end(), 0);
+  std::sort(by_offset.begin(), by_offset.end(),
+            [&](int a, int b) { return ts[a].offset < ts[b].offset; });
+  int64_t end = 0;
+  for (int t : by_offset) {
+    if (ts[t].offset < end) return fail(VSF_ERR_STATE, "layout check: tensors overlap");
+    end = ts[t].offset + ts[t].numel;
+  }
+  if (end > (int64_t)plan.m * plan.S) return fail(VSF_ERR_STATE, "layout check: past m * S");
+  const int64_t wlo = (int64_t)plan.rank_begin * plan.S;
+  std::vector<int64_t> covered(ts.size(), 0);
+  for (const QBlock& b : plan.qblocks) {
+    if (b.tensor < 0 || b.tensor >= (int)ts.size() || b.nrows < 1 || b.ncols < 1 ||
+        (b.nrows > 1 && b.stride < b.ncols))
+      return fail(VSF_ERR_STATE, "layout check: malformed block");
+    const TensorInfo& x = ts[b.tensor];
+    const int64_t first = b.base + wlo - x.offset;  // tensor element of the block start
+    const int64_t last = first + (int64_t)(b.nrows - 1) * b.stride + b.ncols;  // one past
+    if (first < x.lo || last > x.hi)
+      return fail(VSF_ERR_STATE, "layout check: block outside its tensor's window");
+    covered[b.tensor] += (int64_t)b.nrows * b.ncols;
+  }
+  for (size_t t = 0; t < ts.size(); ++t)
+    if (covered[t] != ts[t].hi - ts[t].lo)
+      return fail(VSF_ERR_STATE, "layout check: blocks do not cover tensor " + std::to_string(t));
+  return VSF_OK;
+}
+
 // Quantisation-block tables, tile maps and the workspace layout for the rank
 // window [r0, r1). Only blocks inside the window are listed (no block
 // crosses a rank boundary: RaggedShard's Non-Sharded Block rule for row and
@@ -247,6 +281,9 @@ vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
       }
     }
   }
+
+  const vsf_status checked = check_tables(*plan);
+  if (checked != VSF_OK) return checked;
 
   // Device workspace layout (256-byte aligned sections).
   DeviceLayout& L = plan->layout;

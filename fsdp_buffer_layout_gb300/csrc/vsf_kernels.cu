@@ -45,6 +45,10 @@ constexpr int kCopyThreads = 256;
 #define VSF_COPY_CTAS_PER_SM 16
 #endif
 constexpr int kCopyCtasPerSm = VSF_COPY_CTAS_PER_SM;
+#ifndef VSF_COPY_UNROLL
+#define VSF_COPY_UNROLL 8
+#endif
+constexpr int kCopyUnroll = VSF_COPY_UNROLL;  // 16-byte loads in flight per thread
 constexpr int kMaxCluster = 8;
 constexpr int kSmallThreads = 256;
 
@@ -154,12 +158,12 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
       const uint4* s = reinterpret_cast<const uint4*>(src + b);
       uint4* d = reinterpret_cast<uint4*>(dst + b);
       int64_t k = threadIdx.x;
-      for (; k + 3 * kCopyThreads < nvec; k += 4 * kCopyThreads) {
-        uint4 r[4];
+      for (; k + (kCopyUnroll - 1) * kCopyThreads < nvec; k += kCopyUnroll * kCopyThreads) {
+        uint4 r[kCopyUnroll];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) r[u] = ld_stream(s + k + u * kCopyThreads);
+        for (int u = 0; u < kCopyUnroll; ++u) r[u] = ld_stream(s + k + u * kCopyThreads);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kCopyUnroll; ++u) {
           if (kMode != kUnpack) sq_vec<T>(acc, r[u]);
           if (kMode != kNormOnly) st_stream(d + k + u * kCopyThreads, r[u]);
         }
@@ -545,7 +549,8 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     }
   }
 
-  // Cluster size of the block kernel: the smallest of 1, 2, 4, 8 that keeps
+  // Cluster size of the block kernel: the smallest of 1, 2, 4, 8 (3 and 6
+  // split a block's chunks unevenly and measured slower) that keeps
   // the phase-1 bytes in flight (one block per active cluster, 4 B per
   // element) within the L2 budget (128 MB of the 126 MB L2 measured best:
   // phase 2 re-reads the newest part of each block first, and smaller

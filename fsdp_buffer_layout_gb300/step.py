@@ -173,6 +173,30 @@ class ShardStep:
         off = V.vsf_plan_device_error_offset(self.plan)
         return int(self.workspace[off:off + 4].view(torch.int32).item())
 
+    # ---- checkpoint / resume: the optimizer state is the caller's buffers
+    STATE = ("master", "m_state", "v_state", "m_scale", "v_scale", "packed_bf16")
+
+    def state_dict(self) -> dict:
+        """Host copies of the optimizer state of this DBuffer (or rank window),
+        with the plan's identity (S, offsets, rank window) to check on load."""
+        torch.cuda.current_stream(self.device).wait_stream(self.stream)
+        out = {k: getattr(self, k).detach().to("cpu", copy=True) for k in self.STATE}
+        out["plan"] = dict(S=int(self.info.S), offsets=list(self.offsets),
+                           ranks=(int(self.info.rank_begin), int(self.info.rank_end)),
+                           quantized=bool(self.quantized))
+        return out
+
+    def load_state_dict(self, sd: dict) -> None:
+        """Restores a state_dict taken from a ShardStep with the same plan."""
+        want = dict(S=int(self.info.S), offsets=list(self.offsets),
+                    ranks=(int(self.info.rank_begin), int(self.info.rank_end)),
+                    quantized=bool(self.quantized))
+        if sd["plan"] != want:
+            raise ValueError(f"state_dict was taken under another plan: {sd['plan']} != {want}")
+        with torch.cuda.stream(self.stream):
+            for k in self.STATE:
+                getattr(self, k).copy_(sd[k], non_blocking=False)
+
     # ---- harness helpers
     def load_master(self, t: int, values: torch.Tensor):
         o = self.offsets[t]
