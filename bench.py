@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused shard-step HBM GB/s and params/s vs GB300 HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # HBM3e specification figure the measured copy is set against
 MUON_METRIC = "distributed Muon step Newton-Schulz TFLOP/s vs GB300 bf16 tensor roofline"
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -141,7 +142,11 @@ def cpu_baseline(w, target_s: float = 12.0):
     sw = sample_workload(w, frac)
     t_step, n, nq = oracle_steps(sw, steps)
     b = algorithmic_bytes(n, nq)
-    return dict(value=round(b["step"] / t_step / 1e9, 4), unit="GB/s",
+    import oracle
+    t0 = time.perf_counter()
+    oracle.plan(oracle.Desc.from_workload(w), w.m, w.g_coll)  # the whole workload's layout
+    plan_s = time.perf_counter() - t0
+    return dict(value=round(b["step"] / t_step / 1e9, 4), unit="GB/s", plan_seconds=round(plan_s, 6),
                 params_per_s=round(n / t_step, 1), cores=1, kind="oracle",
                 sample=f"{w.name} with every tensor cut to {frac:.4f} of its rows "
                        f"({n} real elements, {nq} quantisation blocks), {steps} full steps, "
@@ -383,7 +388,9 @@ def gpu_arm(args, rank: int, world: int):
                    else "copy-in / copy-out",
                    "kernel_ms": {"pack+norm": round(k_pack, 5), "adam8": round(k_adam, 5),
                                  "unpack": round(k_unpack, 5)},
-                   "frac_of_peak_step": round(value / world / peak, 4)},
+                   "frac_of_peak_step": round(value / world / peak, 4),
+                   "frac_of_nominal_8tbs_step": round(value / world / NOMINAL_HBM_GBS, 4),
+                   "plan_seconds": round(ss.info.plan_seconds, 6)},
         "roofline": {"bound": "hbm", "achieved": round(adam_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(adam_gbs / peak, 4),
                      "traffic": TRAFFIC.get(w.name), "traffic_unit": "bytes per launch",
