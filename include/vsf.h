@@ -27,7 +27,9 @@
  *     VSF_ERR_CUDA.
  *   - Buffers indexed by "buffer element" hold m*S elements (see
  *     vsf_plan_info.total); virtual rank r owns elements [r*S, (r+1)*S).
- *     Padding elements are never read or written by the per-step calls.
+ *     A plan restricted to ranks [r0, r1) (vsf_plan_restrict) uses buffers
+ *     of (r1 - r0)*S elements holding [r0*S, r1*S). Padding elements are
+ *     never read or written by the per-step calls.
  */
 #ifndef VSF_H
 #define VSF_H
