@@ -46,6 +46,7 @@ constexpr int kMuonTargetCtas = 152 * 8;         // fills every SM of the GPU
 constexpr int kMaxChunk = 192;                    // matrices in one batched chunk
 constexpr int64_t kChunkElems = int64_t(1) << 28;  // bf16 elements of X per chunk (512 MB)
 constexpr size_t kLtWorkspace = 64u << 20;         // cuBLASLt workspace bytes
+constexpr int64_t kSymBlockMin = 1024;             // n from which symmetric products use 2x2 blocks
 
 // Packed-buffer offset of every matrix of one chunk (kernel parameter).
 struct MatTable {
@@ -198,6 +199,47 @@ __global__ void __launch_bounds__(kMuonThreads) muon_update_kernel(
     for (int j = 0; j < V; ++j) p[j] = __fsub_rn(__fmul_rn(p[j], decay), __fmul_rn(alpha, ov[j]));
     Vec<V>::store_f(master + off + i, p);
     Vec<V>::store_bf(bf + off + i, p);
+  }
+}
+
+// Symmetric products computed by 2x2 blocks: the (1,0) block is the
+// transpose of the (0,1) block. A is row-major n x n, h = n / 2 (h and n
+// multiples of 8, so rows start on 16 bytes). One CTA (8 warps) per 64 x 64
+// tile and matrix: rows of the source tile are read as 32-bit bf16 pairs
+// (coalesced), kept in shared memory (rows padded to 33 words), and each
+// output word pairs the same column of two adjacent source rows; output rows
+// are written as 32-bit words (coalesced). Grid (ceil(h/64), ceil(h/64),
+// batch).
+__global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int64_t h, int64_t sa) {
+  __shared__ uint32_t tile[64][33];
+  uint16_t* M = A + (int64_t)blockIdx.z * sa;
+  const int64_t i0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // source block (0,1): rows i0 + r, columns h + j0 + 2 lane (+1)
+  for (int r = warp; r < 64; r += 8) {
+    const int64_t i = i0 + r, j = j0 + 2 * lane;
+    uint32_t w = 0;
+    if (i < h && j + 1 < h) {
+      w = *reinterpret_cast<const uint32_t*>(M + i * n + h + j);
+    } else if (i < h && j < h) {
+      w = M[i * n + h + j];
+    }
+    tile[r][lane] = w;
+  }
+  __syncthreads();
+  // destination block (1,0): row h + j0 + c holds source column j0 + c;
+  // its word `lane` holds source rows i0 + 2 lane and i0 + 2 lane + 1
+  for (int c = warp; c < 64; c += 8) {
+    const int64_t orow = j0 + c, ocol = i0 + 2 * lane;
+    if (orow >= h || ocol >= h) continue;
+    const uint32_t a = tile[2 * lane][c >> 1], b = tile[2 * lane + 1][c >> 1];
+    const uint32_t lo = (c & 1) ? (a >> 16) : (a & 0xffffu);
+    const uint32_t hi = (c & 1) ? (b >> 16) : (b & 0xffffu);
+    uint16_t* dst = M + (h + orow) * n + ocol;
+    if (ocol + 1 < h)
+      *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);
+    else
+      *dst = (uint16_t)lo;
   }
 }
 
@@ -487,18 +529,41 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
     // C x R with leading dimension C.
     const bool tall = c.R > c.C;
     const int64_t n = std::min(c.R, c.C), sx = mat, sa = n * n;
+    // The two symmetric products (the Gram matrix and c A A + b A) by 2x2
+    // blocks when n is large: the diagonal blocks and the (0,1) block, then
+    // (1,0) as its transpose; 3/4 of the FLOPs, and exactly symmetric
+    // results. Column-major operand views of the row-major buffers.
+    const bool blocked = n >= kSymBlockMin && n % 16 == 0;
+    const int64_t h = blocked ? n / 2 : n;
+    auto mirror = [&](uint16_t* M) {
+      const unsigned t = (unsigned)((h + 63) / 64);
+      mirror_kernel<<<dim3(t, t, (unsigned)c.batch), 256, 0, st>>>(M, n, h, sa);
+      const cudaError_t e2 = cudaGetLastError();
+      return e2 == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e2));
+    };
+    const int64_t blocks[3][2] = {{0, 0}, {h, h}, {0, h}};  // (I0, J0) of each computed block
+    const int nblocks = blocked ? 3 : 1;
     for (int it = 0; it < hp->ns_steps; ++it) {
-      vsf_status s;
-      // A (n x n) = X X^T (wide) or X^T X (tall)
-      if (!tall)
-        s = lt_gemm(true, false, n, n, c.C, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f, A, A, n, sa,
-                    c.batch, lt, st);
-      else
-        s = lt_gemm(false, true, n, n, c.R, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f, A, A, n, sa,
-                    c.batch, lt, st);
+      vsf_status s = VSF_OK;
+      // A (n x n) = X X^T (wide) or X^T X (tall); block (I, J) at A + I0 n + J0
+      for (int q = 0; q < nblocks && s == VSF_OK; ++q) {
+        const int64_t I0 = blocks[q][0], J0 = blocks[q][1];
+        if (!tall)
+          s = lt_gemm(true, false, h, h, c.C, X + J0 * c.C, c.C, sx, X + I0 * c.C, c.C, sx, 1.0f,
+                      0.0f, A + I0 * n + J0, A + I0 * n + J0, n, sa, c.batch, lt, st);
+        else
+          s = lt_gemm(false, true, h, h, c.R, X + J0, c.C, sx, X + I0, c.C, sx, 1.0f, 0.0f,
+                      A + I0 * n + J0, A + I0 * n + J0, n, sa, c.batch, lt, st);
+      }
+      if (s == VSF_OK && blocked) s = mirror(A);
       if (s != VSF_OK) return s;
-      // B = c A A + b A
-      s = lt_gemm(false, false, n, n, n, A, n, sa, A, n, sa, nc, nb, A, B, n, sa, c.batch, lt, st);
+      // B = c A A + b A (A symmetric: block (I, J) = c A[J rows] A[I cols] + b A_IJ)
+      for (int q = 0; q < nblocks && s == VSF_OK; ++q) {
+        const int64_t I0 = blocks[q][0], J0 = blocks[q][1];
+        s = lt_gemm(false, false, h, h, n, A + J0, n, sa, A + I0 * n, n, sa, nc, nb,
+                    A + I0 * n + J0, B + I0 * n + J0, n, sa, c.batch, lt, st);
+      }
+      if (s == VSF_OK && blocked) s = mirror(B);
       if (s != VSF_OK) return s;
       // X' = a X + B X (wide) or a X + X B (tall), column-major Xc' = a Xc +
       // Xc B (wide) or a Xc + B Xc (tall)

@@ -79,6 +79,9 @@ def _run(specs, m, g_coll, steps):
      ((2, 128, 256), W.GRAN_ROWS, 64, 0), ((128, 256), W.GRAN_ROWS, 128, 0), ((7,), W.GRAN_ELEM, 0, 0)],
     # 63-element matrices: offsets off the 8-element grid (scalar kernels)
     [((5, 9, 7), W.GRAN_ROWS, 5, 0), ((24, 40), W.GRAN_ROWS, 8, 0)],
+    # n >= 1024: the symmetric products by 2x2 blocks (wide, tall, batched)
+    [((1024, 1536), W.GRAN_ROWS, 32, 0), ((2048, 1024), W.GRAN_ROWS, 64, 0)],
+    [((2, 1024, 1024), W.GRAN_ROWS, 128, 0)],
     # more matrices of one shape than one chunk holds (192)
     [((200, 16, 32), W.GRAN_ROWS, 16, 0), ((3, 32, 16), W.GRAN_ROWS, 32, 0)],
 ])
@@ -123,7 +126,8 @@ def test_muon_output_is_orthogonal_band():
         ss.close()
 
 
-@pytest.mark.parametrize("shape", [(256, 512), (512, 256), (3, 128, 192)])
+@pytest.mark.parametrize("shape", [(256, 512), (512, 256), (3, 128, 192), (1024, 2048),
+                                   (2048, 1024)])
 def test_muon_update_one_step(shape):
     """Step 1: the update O recovered from the master, (p0 decay - p1) / alpha,
     against the oracle's O. Both are bf16 roundings of the same exact
