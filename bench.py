@@ -36,6 +36,10 @@ METRIC = "fused shard-step HBM GB/s and params/s vs GB300 HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0  # HBM3e specification figure the measured copy is set against
 MUON_METRIC = "distributed Muon step Newton-Schulz TFLOP/s vs GB300 bf16 tensor roofline"
+GROUP_METRIC = "fused DBuffer group ops (zero, scale, add) HBM GB/s vs GB300 HBM roofline"
+# algorithmic bytes per real element of each group op, in step order
+GROUP_OPS = (("zero bf16", 2), ("scale bf16", 4), ("add bf16 += bf16", 6),
+             ("add fp32 += bf16", 10))
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -585,6 +589,156 @@ def muon_arm(args, rank: int, world: int):
     }
 
 
+def group_ops_arm(args, rank: int, world: int):
+    """One step = the four fused group ops over every real element of the
+    DBuffer: zero and scale of the packed bf16 gradient, bf16 += bf16 (a
+    second micro-batch's gradient) and fp32 += bf16 (gradient accumulation
+    into an fp32 buffer), each one launch over all tensors."""
+    import torch
+    import torch.distributed as dist
+    from fsdp_buffer_layout_gb300 import vsf as V
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    from synth import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.get(args.workload)
+    stream = torch.cuda.Stream(dev)
+    ss = ShardStep([TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors],
+                   w.m, w.g_coll, stream=stream)
+    n_real, total = ss.info.real, ss.info.total
+    g = ss.packed_grad
+    g2 = torch.zeros_like(g)
+    acc = torch.zeros(total, dtype=torch.float32, device=dev)
+    for t in range(len(w.tensors)):  # real elements: a seeded gradient in both bf16 buffers
+        o, n = ss.offsets[t], ss.numels[t]
+        x = torch.from_numpy(W.grad(w, 1, t).view(np.int16)).to(dev)
+        g.view(torch.int16)[o:o + n].copy_(x)
+        g2.view(torch.int16)[o:o + n].copy_(x)
+    st = stream.cuda_stream
+    ops = [lambda: V.vsf_group_zero(ss.plan, g.data_ptr(), V.VSF_BF16, st),
+           lambda: V.vsf_group_scale(ss.plan, g2.data_ptr(), V.VSF_BF16, 0.5, st),
+           lambda: V.vsf_group_add(ss.plan, g.data_ptr(), V.VSF_BF16, g2.data_ptr(), V.VSF_BF16,
+                                   st),
+           lambda: V.vsf_group_add(ss.plan, acc.data_ptr(), V.VSF_FP32, g2.data_ptr(), V.VSF_BF16,
+                                   st)]
+    nbytes = [n_real * b for _, b in GROUP_OPS]
+
+    def one_step(ev=None):
+        for i, op in enumerate(ops):
+            if ev is not None:
+                ev[i].record(stream)
+            op()
+        if ev is not None:
+            ev[len(ops)].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id  # type: ignore[attr-defined]
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus)
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            one_step(evs[i])
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    op_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(len(ops))]
+
+    # end to end: each step copies a micro-batch gradient in from pinned host
+    # memory into the packed buffer, accumulates it into the fp32 buffer and
+    # reads one accumulated value back
+    host_g = g2.view(torch.int16).cpu().pin_memory()
+    host_out = torch.empty(1, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(e2e_steps):
+            g2.view(torch.int16).copy_(host_g, non_blocking=True)
+            ops[3]()
+            host_out.copy_(acc[:1], non_blocking=True)
+        e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+
+    peak, peak_kind = measured_peak()
+    gbs = [b / (ms * 1e-3) / 1e9 for b, ms in zip(nbytes, op_ms)]
+    value = sum(nbytes) * world / (ms_step * 1e-3) / 1e9
+    return {
+        "metric": GROUP_METRIC, "value": round(value, 2), "unit": "GB/s",
+        "params_per_s": round(n_real * world / (ms_step * 1e-3), 1),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "ops": {name: {"ms": round(ms, 5), "GB/s": round(x, 1),
+                                                      "frac": round(x / peak, 4),
+                                                      "bytes_per_elem": b}
+                                               for (name, b), ms, x in zip(GROUP_OPS, op_ms, gbs)},
+                   "real_params": n_real, "m": w.m, "g_coll": w.g_coll,
+                   "l2": "buffers larger than L2, no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU, m virtual ranks"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs[3], 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs[3] / peak, 4), "traffic": None,
+                     "kernel": "vsf_group_add (fp32 += bf16)",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(nbytes[3] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "workload": "H2D of one bf16 gradient, "
+                "fp32 accumulate, D2H of one value",
+                "h2d_bytes_per_step": int(host_g.numel() * 2), "d2h_bytes_per_step": 4},
+        "gpu_launches": len(ops) * args.steps,
+        "clocks": clocks,
+    }
+
+
+def group_ops_cpu_baseline(w, target_s: float = 6.0):
+    """The oracle's group add (fp32 += bf16, single thread) on the workload's
+    layout with every tensor cut to a fraction of its rows: a probe sizes the
+    sample to about target_s seconds."""
+    import oracle
+    from synth import workloads as W
+
+    def timed(frac):
+        sw = sample_workload(w, frac)
+        d = oracle.Desc.from_workload(sw)
+        S, off = oracle.plan(d, sw.m, sw.g_coll)
+        numels = [t.numel for t in sw.tensors]
+        src = oracle.pack([W.grad(sw, 1, t) for t in range(d.n)], off, sw.m * S)
+        dst = np.zeros(sw.m * S, np.float32)
+        t0 = time.perf_counter()
+        oracle.group_op(2, numels, off, dst, src)
+        return time.perf_counter() - t0, sum(numels)
+
+    sec, n = timed(min(1.0, 1e6 / w.numel))
+    frac = min(1.0, target_s / (sec / n) / w.numel)
+    sec, n = timed(frac)
+    return dict(value=round(n * 10 / sec / 1e9, 4), unit="GB/s", cores=1, kind="oracle",
+                sample=f"add fp32 += bf16 over {w.name} cut to {frac:.4f} of its rows ({n} real "
+                       f"elements, {sec:.1f} s), single thread; host has {os.cpu_count()} cores")
+
+
 def muon_cpu_baseline(w, threads: int | None = None):
     """The Muon oracle (numpy, fp64 products with bf16 rounding points) on
     one whole matrix tensor of w, run in a child process with a fixed BLAS
@@ -678,6 +832,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--optimizer", default="adam8", choices=["adam8", "muon"],
                     help="adam8: the 8-bit AdamW shard step; muon: distributed Muon")
+    ap.add_argument("--group-ops", action="store_true",
+                    help="time the fused DBuffer group ops (zero, scale, add) instead")
     ap.add_argument("--zero-copy", action="store_true",
                     help="gradients/params as views of the packed buffers (no pack/unpack)")
     args = ap.parse_args()
@@ -696,9 +852,13 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    line = (muon_arm if args.optimizer == "muon" else gpu_arm)(args, rank, world)
+    arm = group_ops_arm if args.group_ops else muon_arm if args.optimizer == "muon" else gpu_arm
+    line = arm(args, rank, world)
     if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.group_ops:
+            from synth import workloads as W
+            line["cpu_baseline"] = group_ops_cpu_baseline(W.get(args.workload))
+        elif world == 1 and not args.no_cpu_baseline:
             from synth import workloads as W
             line["cpu_baseline"] = (muon_cpu_baseline if args.optimizer == "muon"
                                     else cpu_baseline)(W.get(args.workload))

@@ -14,6 +14,9 @@
 //                         Adam): one HBM pass per block, the block's new
 //                         absmax reduced across a thread-block cluster;
 //   vsf_unpack            copy-out of the bf16 parameters.
+// For a plan restricted to a rank window, the norm is split at its one
+// cross-rank exchange: vsf_group_sumsq (this window's sum of squares) and
+// vsf_group_scale_from_sumsq (the factor from the caller's total).
 // Nothing here is a dense contraction: the kernels are HBM-bound streams
 // (128-bit loads and stores, streaming cache hints, warp-shuffle reductions).
 //
@@ -250,28 +253,69 @@ __global__ void factor_kernel(const double* __restrict__ d_sumsq, int world, dou
 // in one launch, over the copy spans): 0 zero, 1 scale by alpha, 2 add src.
 // fp32 arithmetic with one rounding, then the buffer's type (bf16 RNE).
 template <typename DT, typename ST, int kOp>
+__device__ __forceinline__ DT group_elem(DT d, ST x, float alpha) {
+  float r = 0.0f;
+  if (kOp == 1) r = __fmul_rn(elem_f32(d), alpha);
+  if (kOp == 2) r = __fadd_rn(elem_f32(d), elem_f32(x));
+  if constexpr (sizeof(DT) == 2)
+    return (DT)bf16_bits(r);
+  else
+    return r;
+}
+
+// E consecutive elements of a buffer, read and written as one vector access
+// of E * sizeof(T) bytes (16 or 8), aligned to that size.
+template <typename T, int E>
+struct Group {
+  static constexpr int kWords = E * (int)sizeof(T) / 4;
+  alignas(16) T v[E];
+  __device__ __forceinline__ void load(const T* p) {
+    if constexpr (kWords == 4)
+      *reinterpret_cast<uint4*>(v) = ld_stream(p);
+    else
+      *reinterpret_cast<uint2*>(v) = __ldcs(reinterpret_cast<const uint2*>(p));
+  }
+  __device__ __forceinline__ void store(T* p) const {
+    if constexpr (kWords == 4)
+      st_stream(p, *reinterpret_cast<const uint4*>(v));
+    else
+      __stcs(reinterpret_cast<uint2*>(p), *reinterpret_cast<const uint2*>(v));
+  }
+};
+
+template <typename DT, typename ST, int kOp>
 __global__ void __launch_bounds__(kCopyThreads) group_op_kernel(
     const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_lo, const int64_t* __restrict__ t_hi,
     const CopySpan* __restrict__ spans, DT* dst, const ST* __restrict__ src, float alpha) {
+  // elements per vector group: 16 bytes of the wider type (8 bf16, 4 fp32)
+  constexpr int E = 16 / (sizeof(DT) > sizeof(ST) ? sizeof(DT) : sizeof(ST));
   const CopySpan s0 = spans[blockIdx.x];
   const CopySpan s1 = spans[blockIdx.x + 1];
   for (int t = s0.tensor; t <= s1.tensor; ++t) {
     const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
     const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
+    if (b >= e) continue;
     const int64_t base = t_off[t];
-    for (int64_t i = b + threadIdx.x; i < e; i += kCopyThreads) {
-      const int64_t x = base + i;
-      float r = 0.0f;
-      if (kOp == 1) r = __fmul_rn(elem_f32(dst[x]), alpha);
-      if (kOp == 2) r = __fadd_rn(elem_f32(dst[x]), elem_f32(src[x]));
-      if constexpr (sizeof(DT) == 2)
-        dst[x] = (DT)bf16_bits(r);
-      else
-        dst[x] = r;
+    // buffer elements [x0, x1): scalar up to a multiple of E, then groups of
+    // E (vector-aligned in both buffers), then the scalar tail
+    const int64_t x0 = base + b, x1 = base + e;
+    const int64_t v0 = min64(x1, (x0 + E - 1) / E * E), v1 = v0 + (x1 - v0) / E * E;
+    for (int64_t x = x0 + threadIdx.x; x < v0; x += kCopyThreads)
+      dst[x] = group_elem<DT, ST, kOp>(dst[x], kOp == 2 ? src[x] : ST(0), alpha);
+    for (int64_t x = v0 + E * (int64_t)threadIdx.x; x < v1; x += E * kCopyThreads) {
+      Group<DT, E> d;
+      Group<ST, E> y;
+      if (kOp != 0) d.load(dst + x);
+      if (kOp == 2) y.load(src + x);
+#pragma unroll
+      for (int k = 0; k < E; ++k)
+        d.v[k] = group_elem<DT, ST, kOp>(kOp != 0 ? d.v[k] : DT(0), kOp == 2 ? y.v[k] : ST(0), alpha);
+      d.store(dst + x);
     }
+    for (int64_t x = v1 + threadIdx.x; x < x1; x += kCopyThreads)
+      dst[x] = group_elem<DT, ST, kOp>(dst[x], kOp == 2 ? src[x] : ST(0), alpha);
   }
 }
-
 
 // ------------------------------------------------------------------ host side
 
