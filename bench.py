@@ -806,6 +806,22 @@ def reference_arm(args):
     }
 
 
+def group_ops_reference_arm(args):
+    """The oracle's group add (fp32 += bf16) on a bounded sample per step."""
+    from synth import workloads as W
+    w = W.get(args.workload)
+    base = group_ops_cpu_baseline(w)
+    return {
+        "impl": "reference", "metric": GROUP_METRIC, "value": base["value"], "unit": "GB/s",
+        "n_gpus": 1, "steps": 1, "warmup": 0, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "ops": "add fp32 += bf16"},
+        "cpu_baseline": base,
+        "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def muon_reference_arm(args):
     """The Muon oracle on one whole matrix per step (see muon_cpu_baseline)."""
     from synth import workloads as W
@@ -844,8 +860,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(muon_reference_arm(args) if args.optimizer == "muon"
-                             else reference_arm(args)), flush=True)
+            arm = (group_ops_reference_arm if args.group_ops else
+                   muon_reference_arm if args.optimizer == "muon" else reference_arm)
+            print(json.dumps(arm(args)), flush=True)
         return
     if args.optimizer == "muon" and args.zero_copy:
         ap.error("--zero-copy applies to the AdamW step")
