@@ -76,13 +76,16 @@ struct DF {
   }
 };
 
-// x*x into the accumulator, exactly for bf16 inputs (16 significant bits)
-// and with the FMA-recovered product error for fp32 inputs.
+// x*x into the accumulator, with the FMA-recovered product error (fp32
+// inputs).
 __device__ __forceinline__ void acc_sq(DF& a, float x) {
   const float p = __fmul_rn(x, x);
   a.add(p);
   a.lo = __fadd_rn(a.lo, __fmaf_rn(x, x, -p));
 }
+// The same for a bf16 value: its square has at most 16 significant bits and
+// is exact in fp32, so there is no product error to recover.
+__device__ __forceinline__ void acc_sq_exact(DF& a, float x) { a.add(__fmul_rn(x, x)); }
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
@@ -114,8 +117,8 @@ __device__ __forceinline__ void sq_vec<uint16_t>(DF& acc, uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    acc_sq(acc, bf16_to_f32(w[i] & 0xffffu));
-    acc_sq(acc, bf16_to_f32(w[i] >> 16));
+    acc_sq_exact(acc, bf16_to_f32(w[i] & 0xffffu));
+    acc_sq_exact(acc, bf16_to_f32(w[i] >> 16));
   }
 }
 
