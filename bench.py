@@ -75,7 +75,20 @@ def measured_bf16_peak(sustained: bool):
         return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
 
 
-SYM_BLOCK_MIN = 1024  # n from which libvsf computes the two symmetric products by 2x2 blocks
+SYM_BLOCK_MIN = 1024  # libvsf splits a symmetric product's diagonal block of this size or more
+
+
+def sym_fraction(n: int) -> float:
+    """Share of a symmetric n x n product's FLOPs that libvsf's blocking
+    executes: a diagonal block splits into two halves plus their off-diagonal
+    block (mirrored) when it is >= 1024 at the top and >= 2048 one level down."""
+    def cost(size, level):
+        lim = SYM_BLOCK_MIN if level == 0 else 2 * SYM_BLOCK_MIN
+        if level < 2 and size >= lim and size % 16 == 0:
+            h = size // 2
+            return 2 * cost(h, level + 1) + h * h
+        return size * size
+    return cost(n, 0) / float(n * n)
 
 
 def muon_flops(w, ns_steps: int = 5, executed: bool = False) -> float:
@@ -83,14 +96,14 @@ def muon_flops(w, ns_steps: int = 5, executed: bool = False) -> float:
     By the definition, per iteration: 2 n^2 k for the Gram matrix, 2 n^3 for
     its square, 2 n^2 k for the product with X (n = min(R, C), k = max(R, C)).
     executed=True counts what the tensor cores run: libvsf computes the two
-    symmetric products by 2x2 blocks (3 of the 4 blocks) once n >= 1024."""
+    symmetric products by blocks (sym_fraction of their FLOPs)."""
     total = 0.0
     for t in w.tensors:
         if len(t.shape) < 2:
             continue
         *lead, R, C = t.shape
         n, k = min(R, C), max(R, C)
-        sym = 0.75 if executed and n >= SYM_BLOCK_MIN and n % 16 == 0 else 1.0
+        sym = sym_fraction(n) if executed else 1.0
         per = sym * (2.0 * n * n * k + 2.0 * n ** 3) + 2.0 * n * n * k
         total += float(np.prod(lead, dtype=np.float64)) * per
     return total * ns_steps
@@ -574,7 +587,7 @@ def muon_arm(args, rank: int, world: int):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": "vsf_muon_step (Newton-Schulz GEMM chain with its element-wise "
                                "kernels)",
-                     "flops": "executed by the tensor cores (symmetric products by 2x2 "
+                     "flops": "executed by the tensor cores (symmetric products by "
                               "blocks); value counts the definition's full products",
                      "peak_source": peak_src},
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

@@ -46,7 +46,11 @@ constexpr int kMuonTargetCtas = 152 * 8;         // fills every SM of the GPU
 constexpr int kMaxChunk = 192;                    // matrices in one batched chunk
 constexpr int64_t kChunkElems = int64_t(1) << 28;  // bf16 elements of X per chunk (512 MB)
 constexpr size_t kLtWorkspace = 64u << 20;         // cuBLASLt workspace bytes
-constexpr int64_t kSymBlockMin = 1024;             // n from which symmetric products use 2x2 blocks
+constexpr int64_t kSymBlockMin = 1024;             // n from which symmetric products use blocks
+#ifndef VSF_SYM_LEVELS
+#define VSF_SYM_LEVELS 2
+#endif
+constexpr int kSymLevels = VSF_SYM_LEVELS;         // levels of splitting (a lower one needs 2048)
 
 // Packed-buffer offset of every matrix of one chunk (kernel parameter).
 struct MatTable {
@@ -202,16 +206,19 @@ __global__ void __launch_bounds__(kMuonThreads) muon_update_kernel(
   }
 }
 
-// Symmetric products computed by 2x2 blocks: the (1,0) block is the
-// transpose of the (0,1) block. A is row-major n x n, h = n / 2 (h and n
-// multiples of 8, so rows start on 16 bytes). One CTA (8 warps) per 64 x 64
+// Symmetric products computed by blocks: an off-diagonal block below the
+// diagonal is the transpose of its mirror above it. A is row-major n x n;
+// the block's size h and offsets bi, bj are multiples of 8 (rows start on
+// 16 bytes). One CTA (8 warps) per 64 x 64
 // tile and matrix: rows of the source tile are read as 32-bit bf16 pairs
 // (coalesced), kept in shared memory (rows padded to 33 words), and each
 // output word pairs the same column of two adjacent source rows; output rows
 // are written as 32-bit words (coalesced). Grid (ceil(h/64), ceil(h/64),
 // batch).
-__global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int64_t h, int64_t sa) {
+__global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int64_t bi, int64_t bj,
+                                                     int64_t h, int64_t sa) {
   __shared__ uint32_t tile[64][33];
+  // the h x h block at rows bi, columns bj, mirrored to rows bj, columns bi
   uint16_t* M = A + (int64_t)blockIdx.z * sa;
   const int64_t i0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -220,9 +227,9 @@ __global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int
     const int64_t i = i0 + r, j = j0 + 2 * lane;
     uint32_t w = 0;
     if (i < h && j + 1 < h) {
-      w = *reinterpret_cast<const uint32_t*>(M + i * n + h + j);
+      w = *reinterpret_cast<const uint32_t*>(M + (bi + i) * n + bj + j);
     } else if (i < h && j < h) {
-      w = M[i * n + h + j];
+      w = M[(bi + i) * n + bj + j];
     }
     tile[r][lane] = w;
   }
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int
     const uint32_t a = tile[2 * lane][c >> 1], b = tile[2 * lane + 1][c >> 1];
     const uint32_t lo = (c & 1) ? (a >> 16) : (a & 0xffffu);
     const uint32_t hi = (c & 1) ? (b >> 16) : (b & 0xffffu);
-    uint16_t* dst = M + (h + orow) * n + ocol;
+    uint16_t* dst = M + (bj + orow) * n + bi + ocol;
     if (ocol + 1 < h)
       *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);
     else
@@ -529,41 +536,63 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
     // C x R with leading dimension C.
     const bool tall = c.R > c.C;
     const int64_t n = std::min(c.R, c.C), sx = mat, sa = n * n;
-    // The two symmetric products (the Gram matrix and c A A + b A) by 2x2
-    // blocks when n is large: the diagonal blocks and the (0,1) block, then
-    // (1,0) as its transpose; 3/4 of the FLOPs, and exactly symmetric
-    // results. Column-major operand views of the row-major buffers.
-    const bool blocked = n >= kSymBlockMin && n % 16 == 0;
-    const int64_t h = blocked ? n / 2 : n;
-    auto mirror = [&](uint16_t* M) {
-      const unsigned t = (unsigned)((h + 63) / 64);
-      mirror_kernel<<<dim3(t, t, (unsigned)c.batch), 256, 0, st>>>(M, n, h, sa);
+    // The two symmetric products (the Gram matrix and c A A + b A) by blocks:
+    // a diagonal block of size s >= 1024 (2048 below the top level) splits
+    // into two diagonal halves and their off-diagonal block, whose mirror is
+    // its transpose. One level costs 3/4 of the FLOPs, two levels 5/8; the
+    // results are exactly symmetric. Column-major operand views of the
+    // row-major buffers.
+    struct Blk {
+      int64_t i0, j0, size;
+    };
+    std::vector<Blk> gemm_blocks, mirrors;
+    {
+      std::vector<std::pair<Blk, int>> todo = {{{0, 0, n}, 0}};
+      while (!todo.empty()) {
+        const Blk b = todo.back().first;
+        const int level = todo.back().second;
+        todo.pop_back();
+        const int64_t smin = level == 0 ? kSymBlockMin : 2 * kSymBlockMin;
+        if (level < kSymLevels && b.size >= smin && b.size % 16 == 0) {
+          const int64_t h2 = b.size / 2;
+          todo.push_back({{b.i0, b.i0, h2}, level + 1});
+          todo.push_back({{b.i0 + h2, b.i0 + h2, h2}, level + 1});
+          gemm_blocks.push_back({b.i0, b.i0 + h2, h2});
+          mirrors.push_back({b.i0, b.i0 + h2, h2});
+        } else {
+          gemm_blocks.push_back(b);
+        }
+      }
+    }
+    auto mirror_all = [&](uint16_t* M) {
+      for (const Blk& b : mirrors) {
+        const unsigned t = (unsigned)((b.size + 63) / 64);
+        mirror_kernel<<<dim3(t, t, (unsigned)c.batch), 256, 0, st>>>(M, n, b.i0, b.j0, b.size, sa);
+      }
       const cudaError_t e2 = cudaGetLastError();
       return e2 == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e2));
     };
-    const int64_t blocks[3][2] = {{0, 0}, {h, h}, {0, h}};  // (I0, J0) of each computed block
-    const int nblocks = blocked ? 3 : 1;
     for (int it = 0; it < hp->ns_steps; ++it) {
       vsf_status s = VSF_OK;
       // A (n x n) = X X^T (wide) or X^T X (tall); block (I, J) at A + I0 n + J0
-      for (int q = 0; q < nblocks && s == VSF_OK; ++q) {
-        const int64_t I0 = blocks[q][0], J0 = blocks[q][1];
+      for (size_t q = 0; q < gemm_blocks.size() && s == VSF_OK; ++q) {
+        const int64_t I0 = gemm_blocks[q].i0, J0 = gemm_blocks[q].j0, hs = gemm_blocks[q].size;
         if (!tall)
-          s = lt_gemm(true, false, h, h, c.C, X + J0 * c.C, c.C, sx, X + I0 * c.C, c.C, sx, 1.0f,
+          s = lt_gemm(true, false, hs, hs, c.C, X + J0 * c.C, c.C, sx, X + I0 * c.C, c.C, sx, 1.0f,
                       0.0f, A + I0 * n + J0, A + I0 * n + J0, n, sa, c.batch, lt, st);
         else
-          s = lt_gemm(false, true, h, h, c.R, X + J0, c.C, sx, X + I0, c.C, sx, 1.0f, 0.0f,
+          s = lt_gemm(false, true, hs, hs, c.R, X + J0, c.C, sx, X + I0, c.C, sx, 1.0f, 0.0f,
                       A + I0 * n + J0, A + I0 * n + J0, n, sa, c.batch, lt, st);
       }
-      if (s == VSF_OK && blocked) s = mirror(A);
+      if (s == VSF_OK && !mirrors.empty()) s = mirror_all(A);
       if (s != VSF_OK) return s;
       // B = c A A + b A (A symmetric: block (I, J) = c A[J rows] A[I cols] + b A_IJ)
-      for (int q = 0; q < nblocks && s == VSF_OK; ++q) {
-        const int64_t I0 = blocks[q][0], J0 = blocks[q][1];
-        s = lt_gemm(false, false, h, h, n, A + J0, n, sa, A + I0 * n, n, sa, nc, nb,
+      for (size_t q = 0; q < gemm_blocks.size() && s == VSF_OK; ++q) {
+        const int64_t I0 = gemm_blocks[q].i0, J0 = gemm_blocks[q].j0, hs = gemm_blocks[q].size;
+        s = lt_gemm(false, false, hs, hs, n, A + J0, n, sa, A + I0 * n, n, sa, nc, nb,
                     A + I0 * n + J0, B + I0 * n + J0, n, sa, c.batch, lt, st);
       }
-      if (s == VSF_OK && blocked) s = mirror(B);
+      if (s == VSF_OK && !mirrors.empty()) s = mirror_all(B);
       if (s != VSF_OK) return s;
       // X' = a X + B X (wide) or a X + X B (tall), column-major Xc' = a Xc +
       // Xc B (wide) or a Xc + B Xc (tall)

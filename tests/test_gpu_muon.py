@@ -127,13 +127,14 @@ def test_muon_output_is_orthogonal_band():
 
 
 @pytest.mark.parametrize("shape", [(256, 512), (512, 256), (3, 128, 192), (1024, 2048),
-                                   (2048, 1024)])
+                                   (2048, 1024), (4096, 4096)])
 def test_muon_update_one_step(shape):
     """Step 1: the update O recovered from the master, (p0 decay - p1) / alpha,
     against the oracle's O. Both are bf16 roundings of the same exact
     Newton-Schulz iteration, so by the triangle inequality they lie within
     twice the oracle's own distance d from exact arithmetic (the oracle run
-    with exact=True), in Frobenius norm and element by element."""
+    with exact=True), in Frobenius norm and element by element. Shapes from
+    1024 take the blocked symmetric products, 4096 x 4096 two levels of them."""
     ss, state, masters = _run([(shape, W.GRAN_ROWS, 64, 0)], 2, 128, steps=1)
     try:
         n = ss.numels[0]
