@@ -378,18 +378,24 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
         red[par][1][warp][lane / gpt] = vx;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-      if (tid == 0) {
+      if (warp == 0) {
+        // the CTA's maxima, one warp entry per lane; lane r then writes them
+        // into cluster rank r and arrives there (release covers its stores)
         for (int t = 0; t < kt; ++t) {
-          float bm = 0.0f, bv = 0.0f;
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            bm = fmaxf(bm, red[par][0][w][t]);
-            bv = fmaxf(bv, red[par][1][w][t]);
+          float bm = lane < kConsumerWarps ? red[par][0][lane][t] : 0.0f;
+          float bv = lane < kConsumerWarps ? red[par][1][lane][t] : 0.0f;
+          bm = fmaxf(bm, 0.0f);
+          bv = fmaxf(bv, 0.0f);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, o));
           }
-          for (int rk = 0; rk < CL; ++rk)
-            dsmem_put(smem_u32(&maxima[(par * kMaxCluster + crank) * kMaxUnitTiles + t]), rk,
+          if (lane < CL)
+            dsmem_put(smem_u32(&maxima[(par * kMaxCluster + crank) * kMaxUnitTiles + t]), lane,
                       make_float2(bm, bv));
         }
-        for (int rk = 0; rk < CL; ++rk) dsmem_arrive(max_bar(par), rk);
+        if (lane < CL) dsmem_arrive(max_bar(par), lane);
       }
       mbar_wait_cluster(max_bar(par), (nb >> 1) & 1, err);
       float sm = 0.0f, sv = 0.0f;
