@@ -208,21 +208,33 @@ __global__ void __launch_bounds__(kMuonThreads) muon_update_kernel(
 
 // Symmetric products computed by blocks: an off-diagonal block below the
 // diagonal is the transpose of its mirror above it. A is row-major n x n;
-// the block's size h and offsets bi, bj are multiples of 8 (rows start on
-// 16 bytes). One CTA (8 warps) per 64 x 64
-// tile and matrix: rows of the source tile are read as 32-bit bf16 pairs
-// (coalesced), kept in shared memory (rows padded to 33 words), and each
-// output word pairs the same column of two adjacent source rows; output rows
-// are written as 32-bit words (coalesced). Grid (ceil(h/64), ceil(h/64),
-// batch).
-__global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int64_t bi, int64_t bj,
-                                                     int64_t h, int64_t sa) {
+// block sizes and offsets are multiples of 8 (rows start on 16 bytes).
+// One launch mirrors every block of one product: the grid's x index runs
+// over the 64 x 64 tiles of all blocks in turn (tile_begin holds each block's
+// first tile), y over the matrices of the chunk. One CTA (8 warps) per tile:
+// rows of the source tile are read as 32-bit bf16 pairs (coalesced), kept in
+// shared memory (rows padded to 33 words), and each output word pairs the
+// same column of two adjacent source rows; output rows are written as
+// 32-bit words (coalesced).
+constexpr int kMaxMirrors = 4;
+struct MirrorBlocks {
+  int64_t bi[kMaxMirrors], bj[kMaxMirrors], size[kMaxMirrors];
+  int32_t tile_begin[kMaxMirrors + 1];
+  int32_t count;
+};
+
+__global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, const __grid_constant__ MirrorBlocks mb,
+                                                     int64_t sa) {
   __shared__ uint32_t tile[64][33];
+  int q = 0;
+  while (q + 1 < mb.count && (int)blockIdx.x >= mb.tile_begin[q + 1]) ++q;
+  const int64_t bi = mb.bi[q], bj = mb.bj[q], h = mb.size[q];
+  const int64_t tiles = (h + 63) / 64;
+  const int64_t tix = (int64_t)blockIdx.x - mb.tile_begin[q];
+  uint16_t* M = A + (int64_t)blockIdx.y * sa;
   // the h x h block at rows bi, columns bj, mirrored to rows bj, columns bi
-  uint16_t* M = A + (int64_t)blockIdx.z * sa;
-  const int64_t i0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
+  const int64_t i0 = tix / tiles * 64, j0 = tix % tiles * 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // source block (0,1): rows i0 + r, columns h + j0 + 2 lane (+1)
   for (int r = warp; r < 64; r += 8) {
     const int64_t i = i0 + r, j = j0 + 2 * lane;
     uint32_t w = 0;
@@ -234,8 +246,8 @@ __global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, int
     tile[r][lane] = w;
   }
   __syncthreads();
-  // destination block (1,0): row h + j0 + c holds source column j0 + c;
-  // its word `lane` holds source rows i0 + 2 lane and i0 + 2 lane + 1
+  // destination row bj + j0 + c holds source column j0 + c; its word `lane`
+  // holds source rows i0 + 2 lane and i0 + 2 lane + 1
   for (int c = warp; c < 64; c += 8) {
     const int64_t orow = j0 + c, ocol = i0 + 2 * lane;
     if (orow >= h || ocol >= h) continue;
@@ -564,11 +576,21 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
         }
       }
     }
+    if (mirrors.size() > (size_t)kMaxMirrors)
+      return fail(VSF_ERR_STATE, "vsf_muon_step: too many mirrored blocks");
+    MirrorBlocks mb{};
+    mb.count = (int32_t)mirrors.size();
+    mb.tile_begin[0] = 0;
+    for (size_t q = 0; q < mirrors.size(); ++q) {
+      mb.bi[q] = mirrors[q].i0;
+      mb.bj[q] = mirrors[q].j0;
+      mb.size[q] = mirrors[q].size;
+      const int64_t t = (mirrors[q].size + 63) / 64;
+      mb.tile_begin[q + 1] = mb.tile_begin[q] + (int32_t)(t * t);
+    }
     auto mirror_all = [&](uint16_t* M) {
-      for (const Blk& b : mirrors) {
-        const unsigned t = (unsigned)((b.size + 63) / 64);
-        mirror_kernel<<<dim3(t, t, (unsigned)c.batch), 256, 0, st>>>(M, n, b.i0, b.j0, b.size, sa);
-      }
+      mirror_kernel<<<dim3((unsigned)mb.tile_begin[mb.count], (unsigned)c.batch), 256, 0, st>>>(
+          M, n, mb, sa);
       const cudaError_t e2 = cudaGetLastError();
       return e2 == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e2));
     };
