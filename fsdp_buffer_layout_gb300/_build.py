@@ -1,4 +1,9 @@
-"""Builds libvsf.so in-tree with nvcc for sm_103a (no torch extension machinery)."""
+"""Builds libvsf.so in-tree with nvcc for sm_103a (no torch extension machinery).
+
+build(variant="bounds") builds libvsf_bounds.so instead: the same library
+with -DVSF_DEBUG_BOUNDS, whose kernels check every range they index against
+the packed buffers' extent and record a failed check in the device error
+word (bit 4) instead of accessing; load it with VSF_LIBRARY=<path>."""
 from __future__ import annotations
 
 import os
@@ -12,6 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libvsf.so")
 BUILD = os.path.join(PKG, "_build")
+VARIANTS = {None: ("libvsf.so", []), "bounds": ("libvsf_bounds.so", ["-DVSF_DEBUG_BOUNDS"])}
 
 SOURCES = ["plan.cpp", "vsf_kernels.cu", "muon.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -23,32 +29,40 @@ def nvcc() -> str:
 
 
 def _inputs():
-    files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "vsf_internal.h"), os.path.join(INCLUDE, "vsf.h")]
-    return files
+    files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
+             if f.endswith((".cu", ".cuh", ".cpp", ".h"))]
+    return files + [os.path.join(INCLUDE, "vsf.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def lib_path(variant: str | None = None) -> str:
+    return os.path.join(PKG, VARIANTS[variant][0])
+
+
+def up_to_date(variant: str | None = None) -> bool:
+    out = lib_path(variant)
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(out)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          variant: str | None = None) -> str:
+    out = lib_path(variant)
+    if not force and up_to_date(variant):
+        return out
+    objdir = os.path.join(BUILD, variant or "release")
+    os.makedirs(objdir, exist_ok=True)
     # -fmad=false: no floating-point multiply-add contraction anywhere in
     # device code, so every fp32 operation of the update rounds once, in the
     # order written (explicit __fmaf_rn calls stay fused).
     common = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler",
-              "-fPIC,-O2,-ffp-contract=off", "-I", INCLUDE, "-I", CSRC] + ARCH
+              "-fPIC,-O2,-ffp-contract=off", "-I", INCLUDE, "-I", CSRC] + ARCH + VARIANTS[variant][1]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + common
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -60,15 +74,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if verbose or ptxas_info:
         for _, err in results:
             sys.stderr.write(err)
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
     cmd = [nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + [
         "-lcudart_static", "-L" + cuda_lib, "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -37,6 +37,7 @@
 
 struct AdamConsts {
   float b1, omb1, b2, omb2, eps_hat, decay, alpha;
+  Bounds bd;  // index checks of the debug build
 };
 
 // ---------------------------------------------------------------- memory ops
@@ -396,6 +397,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) adam_block_kernel(
   for (int j = cid; j < nlist; j += nclusters, par ^= 1) {
     const int q = list[j];
     const QBlock b = qb[q];
+    // the same answer in every CTA of the cluster: all skip together
+    if (!in_bounds(k.bd, b.base, b.base + (int64_t)(b.nrows - 1) * b.stride + b.ncols)) continue;
     c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
     c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
 
@@ -549,6 +552,7 @@ __global__ void __launch_bounds__(kSmallThreads) adam_small_kernel(
   if (j >= nlist) return;
   const int q = list[j];
   const QBlock b = qb[q];
+  if (!in_bounds(k.bd, b.base, b.base + b.ncols)) return;
   Consts2 c;
   c.b1 = f2(k.b1);
   c.omb1 = f2(k.omb1);
@@ -598,6 +602,7 @@ __global__ void __launch_bounds__(kCopyThreads) adam_fp32_kernel(
     const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
     const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
     const int64_t base = t_off[t];
+    if (b < e && !in_bounds(k.bd, base + b, base + e)) continue;
     for (int64_t i = b + threadIdx.x; i < e; i += kCopyThreads) {
       const int64_t x = base + i;
       float m, v;

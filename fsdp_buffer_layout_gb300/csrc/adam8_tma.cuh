@@ -280,6 +280,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
             const uint32_t len = (uint32_t)ch.len();
             if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
             const uint32_t fb = full_bar(s);
+            const int64_t last = ch.gstart + (int64_t)(ch.rows - 1) * ch.stride + ch.row_len;
+            if (!in_bounds(k.bd, ch.gstart, last)) {
+              mbar_arrive(fb);  // no copy: complete the slot's phase without data
+              continue;
+            }
             mbar_expect_tx(fb, len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u));
             const uint32_t slot = s0 + s * Lay::slot;
             const uint64_t pol = ph == 0 ? keep : drop;
@@ -434,6 +439,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
             uint2 ocm, ocv;
             phase2_group<GT>(c, r, pa, pb, o0, o1, ob, ocm, ocv);
             const int64_t e = ch.at(g * 8);
+            if (!in_bounds(k.bd, e, e + 8)) continue;
             st_v4(master + e, o0, drop);
             st_v4(master + e + 4, o1, drop);
             st_v4(bf + e, ob, drop);

@@ -36,6 +36,7 @@
 #include <tuple>
 #include <vector>
 
+#include "bounds.cuh"
 #include "vsf_internal.h"
 
 namespace vsf {
@@ -122,8 +123,9 @@ struct Vec<8> {
 template <int V>
 __global__ void __launch_bounds__(kMuonThreads) muon_momentum_kernel(
     const uint16_t* __restrict__ g, float* M, const __grid_constant__ MatTable tab, int64_t mat,
-    float mu, double* partials) {
+    float mu, double* partials, Bounds bd) {
   const int64_t off = tab.off[blockIdx.y];
+  if (!in_bounds(bd, off, off + mat)) return;  // the whole CTA: uniform
   DFm acc;
   for (int64_t i = ((int64_t)blockIdx.x * kMuonThreads + threadIdx.x) * V; i < mat;
        i += (int64_t)gridDim.x * kMuonThreads * V) {
@@ -156,7 +158,9 @@ __global__ void __launch_bounds__(kMuonThreads) muon_momentum_kernel(
 template <int V>
 __global__ void __launch_bounds__(kMuonThreads) muon_normalize_kernel(
     const uint16_t* __restrict__ g, const float* __restrict__ M, const __grid_constant__ MatTable tab,
-    int64_t mat, float mu, const double* __restrict__ partials, double eps, uint16_t* X) {
+    int64_t mat, float mu, const double* __restrict__ partials, double eps, uint16_t* X,
+    Bounds bd) {
+  if (!in_bounds(bd, tab.off[blockIdx.y], tab.off[blockIdx.y] + mat)) return;  // uniform
   __shared__ double red[kMuonThreads / 32];
   __shared__ float r_s;
   {
@@ -191,8 +195,9 @@ __global__ void __launch_bounds__(kMuonThreads) muon_normalize_kernel(
 template <int V>
 __global__ void __launch_bounds__(kMuonThreads) muon_update_kernel(
     const uint16_t* __restrict__ O, float* master, uint16_t* bf, const __grid_constant__ MatTable tab,
-    int64_t mat, float decay, float alpha) {
+    int64_t mat, float decay, float alpha, Bounds bd) {
   const int64_t off = tab.off[blockIdx.y];
+  if (!in_bounds(bd, off, off + mat)) return;
   const uint16_t* o = O + (int64_t)blockIdx.y * mat;
   for (int64_t i = ((int64_t)blockIdx.x * kMuonThreads + threadIdx.x) * V; i < mat;
        i += (int64_t)gridDim.x * kMuonThreads * V) {
@@ -521,6 +526,7 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
   const float mu = (float)hp->momentum;
   const float decay = (float)(1.0 - hp->lr * hp->weight_decay);
   const float na = (float)hp->ns_a, nb = (float)hp->ns_b, nc = (float)hp->ns_c;
+  const Bounds bd{plan->total, reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error)};
 
   for (const MuonChunk& c : muon_chunks(plan)) {
     MatTable tab;
@@ -533,14 +539,14 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
     for (int64_t j = 0; j < c.batch; ++j) vec = vec && c.off[(size_t)j] % 8 == 0;
     if (vec) {
       muon_momentum_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                             partials);
+                                                             partials, bd);
       muon_normalize_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                              partials, hp->eps, X);
+                                                              partials, hp->eps, X, bd);
     } else {
       muon_momentum_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                             partials);
+                                                             partials, bd);
       muon_normalize_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                              partials, hp->eps, X);
+                                                              partials, hp->eps, X, bd);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
@@ -630,10 +636,10 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
     const float alpha = (float)(hp->lr * std::sqrt(std::max(1.0, (double)c.R / (double)c.C)));
     if (vec)
       muon_update_kernel<8><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
-                                                           alpha);
+                                                           alpha, bd);
     else
       muon_update_kernel<1><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
-                                                           alpha);
+                                                           alpha, bd);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
   }

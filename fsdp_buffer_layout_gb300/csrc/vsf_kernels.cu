@@ -36,6 +36,7 @@
 #include <mutex>
 #include <string>
 
+#include "bounds.cuh"
 #include "vsf_internal.h"
 
 namespace cg = cooperative_groups;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
                                                             const int64_t* __restrict__ t_off,
                                                             const int64_t* __restrict__ t_lo, const int64_t* __restrict__ t_hi,
                                                             const CopySpan* __restrict__ spans,
-                                                            T* packed, double* partials) {
+                                                            T* packed, double* partials, Bounds bd) {
   constexpr int V = 16 / sizeof(T);
   const CopySpan s0 = spans[blockIdx.x];
   const CopySpan s1 = spans[blockIdx.x + 1];
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(TensorPtrs ptrs,
   for (int t = s0.tensor; t <= s1.tensor; ++t) {
     const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
     const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
-    if (b >= e) continue;
+    if (b >= e || !in_bounds(bd, t_off[t] + b, t_off[t] + e)) continue;
     T* pk = packed + t_off[t];
     T* tp = const_cast<T*>(static_cast<const T*>(ptrs.p[t]));
     const T* src = (kMode == kUnpack) ? pk : (kMode == kPack ? tp : pk);
@@ -289,7 +290,8 @@ struct Group {
 template <typename DT, typename ST, int kOp>
 __global__ void __launch_bounds__(kCopyThreads) group_op_kernel(
     const int64_t* __restrict__ t_off, const int64_t* __restrict__ t_lo, const int64_t* __restrict__ t_hi,
-    const CopySpan* __restrict__ spans, DT* dst, const ST* __restrict__ src, float alpha) {
+    const CopySpan* __restrict__ spans, DT* dst, const ST* __restrict__ src, float alpha,
+    Bounds bd) {
   // elements per vector group: 16 bytes of the wider type (8 bf16, 4 fp32)
   constexpr int E = 16 / (sizeof(DT) > sizeof(ST) ? sizeof(DT) : sizeof(ST));
   const CopySpan s0 = spans[blockIdx.x];
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(kCopyThreads) group_op_kernel(
   for (int t = s0.tensor; t <= s1.tensor; ++t) {
     const int64_t b = (t == s0.tensor) ? s0.elem : t_lo[t];
     const int64_t e = (t == s1.tensor) ? s1.elem : t_hi[t];
-    if (b >= e) continue;
+    if (b >= e || !in_bounds(bd, t_off[t] + b, t_off[t] + e)) continue;
     const int64_t base = t_off[t];
     // buffer elements [x0, x1): scalar up to a multiple of E, then groups of
     // E (vector-aligned in both buffers), then the scalar tail
@@ -343,6 +345,10 @@ vsf_status check_ready(const vsf_plan* plan, const char* who) {
 template <typename T>
 const T* ws_ptr(const vsf_plan* plan, size_t off) {
   return reinterpret_cast<const T*>(plan->d_ws + off);
+}
+
+Bounds bounds_of(const vsf_plan* plan) {
+  return Bounds{plan->total, reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error)};
 }
 
 // Step-t constants, each computed in double and rounded once to fp32
@@ -410,7 +416,7 @@ vsf_status launch_copy(const vsf_plan* plan, const void* const* tensors, void* p
       ws_ptr<int64_t>(plan, plan->layout.tensor_lo),
       ws_ptr<int64_t>(plan, plan->layout.tensor_hi),
       ws_ptr<CopySpan>(plan, plan->layout.spans), static_cast<T*>(packed),
-      reinterpret_cast<double*>(plan->d_ws + plan->layout.partials));
+      reinterpret_cast<double*>(plan->d_ws + plan->layout.partials), bounds_of(plan));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VSF_OK : cuda_fail(e, who);
 }
@@ -800,7 +806,8 @@ vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t
       misaligned(v_state) || misaligned(packed_bf16) || misaligned(d_factor) ||
       (hp->quantized && (misaligned(m_scale) || misaligned(v_scale))))
     return fail(VSF_ERR_ALIGN, "vsf_adam8_step: pointer not 16-byte aligned");
-  const AdamConsts k = make_consts(*hp, step);
+  AdamConsts k = make_consts(*hp, step);
+  k.bd = bounds_of(plan);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (grad_dtype == VSF_BF16)
     return launch_adam<uint16_t>(plan, packed_grad, d_factor, master, m_state, v_state, m_scale,
@@ -837,7 +844,7 @@ vsf_status launch_group(const vsf_plan* plan, void* dst, const void* src, float 
       ws_ptr<int64_t>(plan, plan->layout.tensor_lo),
       ws_ptr<int64_t>(plan, plan->layout.tensor_hi),
       ws_ptr<CopySpan>(plan, plan->layout.spans), static_cast<DT*>(dst),
-      static_cast<const ST*>(src), alpha);
+      static_cast<const ST*>(src), alpha, bounds_of(plan));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VSF_OK : cuda_fail(e, who);
 }

@@ -60,7 +60,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """libvsf.so, or the library named by VSF_LIBRARY (the bounds-checking
+    build, libvsf_bounds.so)."""
+    return os.environ.get("VSF_LIBRARY") or _build.LIB
 
 
 def lib():
@@ -68,10 +70,11 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_build.LIB):
-                raise RuntimeError(f"libvsf.so is not built ({_build.LIB}); "
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libvsf is not built ({path}); "
                                    "run `python -c 'import __graft_entry__ as g; g.build()'`")
-            L = ctypes.CDLL(_build.LIB)
+            L = ctypes.CDLL(path)
             vp, i32, i64, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32
             P = ctypes.POINTER
             L.vsf_plan_create.restype = st

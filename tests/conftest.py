@@ -25,3 +25,24 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _bounds_checked_on_close(monkeypatch):
+    """Under the bounds-checking build (VSF_LIBRARY set), every ShardStep
+    must close with no failed index check (bit 4 of its device error word)."""
+    if not os.environ.get("VSF_LIBRARY"):
+        yield
+        return
+    import torch
+    from fsdp_buffer_layout_gb300 import step
+    orig = step.ShardStep.close
+
+    def close(self):
+        if self.plan:
+            torch.cuda.synchronize()
+            assert self.device_error() & 4 == 0, "a kernel's index check failed"
+        orig(self)
+
+    monkeypatch.setattr(step.ShardStep, "close", close)
+    yield
