@@ -89,13 +89,14 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) 
 }
 
 // Bounded wait for the phase of the given parity; returns false after
-// kWaitNs of wall-clock time (global timer), having set bit 1 of the error
-// word.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+// limit_ns (kWaitNs unless given) of wall-clock time (global timer), having
+// set bit 1 of the error word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                          uint64_t limit_ns = kWaitNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try(bar, parity)) {
-    if (global_ns() - t0 > kWaitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(err, 2u);
       return false;
     }
@@ -458,4 +459,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
   // serialization), finish only after it, so that later launches on the
   // stream see both kernels' writes. Returns at once otherwise.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Self-test of the bounded wait: one CTA waits on a barrier that no one
+// arrives on; the wait must give up after limit_ns and set bit 1 of *err.
+__global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, err, limit_ns);
 }

@@ -779,6 +779,15 @@ vsf_status vsf_group_sumsq(const vsf_plan* plan, const void* packed_grad, int32_
   return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_group_sumsq");
 }
 
+vsf_status vsf_selftest_wait_timeout(unsigned* d_err, uint64_t limit_ns, void* stream) {
+  if (d_err == nullptr) return fail(VSF_ERR_ARG, "vsf_selftest_wait_timeout: NULL error word");
+  if (limit_ns > 1000000000ull)
+    return fail(VSF_ERR_ARG, "vsf_selftest_wait_timeout: limit above 1 s");
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d_err, limit_ns);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_selftest_wait_timeout");
+}
+
 vsf_status vsf_group_scale_from_sumsq(const double* d_sumsq, const vsf_adam_hparams* hp,
                                       float* d_factor, double* d_norm, void* stream) {
   if (d_sumsq == nullptr || hp == nullptr || d_factor == nullptr)

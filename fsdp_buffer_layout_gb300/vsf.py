@@ -97,6 +97,8 @@ def lib():
             L.vsf_plan_upload.argtypes = [vp, vp, ctypes.c_size_t, vp]
             L.vsf_pack.restype = st
             L.vsf_pack.argtypes = [vp, P(vp), i32, vp, vp]
+            L.vsf_selftest_wait_timeout.restype = st
+            L.vsf_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
             L.vsf_plan_restrict.restype = st
             L.vsf_plan_restrict.argtypes = [vp, i32, i32]
             L.vsf_group_sumsq.restype = st
@@ -173,6 +175,10 @@ def vsf_plan_create(descs, m: int, g_coll: int, order: int = VSF_ORDER_DEFAULT) 
 
 def vsf_plan_destroy(plan: int) -> None:
     lib().vsf_plan_destroy(plan)
+
+
+def vsf_selftest_wait_timeout(d_err: int, limit_ns: int, stream: int) -> None:
+    _check(lib().vsf_selftest_wait_timeout(d_err, limit_ns, stream))
 
 
 def vsf_plan_restrict(plan: int, rank_begin: int, rank_end: int) -> None:

@@ -305,6 +305,14 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream);
 
+/* Self-test of the kernels' bounded waits (every wait on a barrier gives up
+ * after a time limit, sets bit 1 of the device error word and lets the kernel
+ * finish, so no thread can hang): launches one CTA that waits on a barrier
+ * nobody arrives on, with limit_ns (at most 1 s) instead of the kernels' 2 s.
+ * After the stream reaches it, *d_err (a device uint32 the caller zeroed)
+ * has bit 1 set. Errors: VSF_ERR_ARG (NULL, limit above 1 s), VSF_ERR_CUDA. */
+vsf_status vsf_selftest_wait_timeout(unsigned* d_err, uint64_t limit_ns, void* stream);
+
 /* Group norm and scale WITHOUT any device allocation or workspace. The pages
  * have no counterpart: this entry point exists for callers that cannot
  * allocate device memory where they need the gradient norm, such as a hook

@@ -44,3 +44,11 @@ def test_per_step_calls_reject_unuploaded_plan():
         assert e.value.status == V.VSF_ERR_STATE
     finally:
         V.vsf_plan_destroy(p)
+
+
+def test_wait_selftest_refuses_a_limit_above_one_second():
+    """Host-side argument check of the bounded-wait self-test (no launch)."""
+    from fsdp_buffer_layout_gb300 import vsf as V
+    with pytest.raises(V.VsfError) as e:
+        V.vsf_selftest_wait_timeout(1 << 20, 2_000_000_000, 0)
+    assert e.value.status == V.VSF_ERR_ARG
