@@ -86,6 +86,15 @@ def test_single_rank_and_many_empty_ranks():
     compare(many, run_gpu(many), run_oracle(many))
 
 
+def test_S_equal_to_one_block():
+    """Four 8192-element row blocks on four ranks: S is exactly one block,
+    every rank holds one whole block and every boundary is a block edge."""
+    case = _normal_case([((128, 256), W.GRAN_ROWS, 32, 0)], m=4, g=128, steps=3)
+    o = run_oracle(case)
+    assert o["S"] == 8192
+    compare(case, run_gpu(case), o)
+
+
 def test_all_zero_blocks_keep_zero_codes():
     specs = [((64, 256), W.GRAN_ROWS, 16, 0), ((512,), W.GRAN_ELEM, 0, 0)]
     case = _normal_case(specs, m=2, g=128, steps=3)

@@ -101,3 +101,23 @@ def test_bad_descriptors_are_rejected():
     with pytest.raises(V.VsfError) as e:
         V.vsf_plan_create([V.make_desc((1 << 40, 1 << 40), V.VSF_GRAN_ELEM)], 2, 8)
     assert e.value.status == V.VSF_ERR_OVERFLOW
+
+
+def test_size_limits_are_refused_not_truncated():
+    """The kernels keep block extents in 32-bit fields: a quantisation block
+    of 2^31 elements or more, or a tile tensor with 2^31 or more rows or
+    columns, must be refused at plan time (VSF_ERR_OVERFLOW)."""
+    big_rows = V.make_desc((2, (1 << 30) + 8), V.VSF_GRAN_ROWS, 2)  # one block of > 2^31
+    with pytest.raises(V.VsfError) as e:
+        V.vsf_plan_create([big_rows], 1, 8)
+    assert e.value.status == V.VSF_ERR_OVERFLOW
+    wide_tile = V.make_desc((1, (1 << 31) + 16), V.VSF_GRAN_TILE, 1, 16)
+    with pytest.raises(V.VsfError) as e:
+        V.vsf_plan_create([wide_tile], 1, 16)
+    assert e.value.status == V.VSF_ERR_OVERFLOW
+    # just below the limit is planned
+    ok = V.vsf_plan_create([V.make_desc((1, (1 << 31) - 16), V.VSF_GRAN_ROWS, 1)], 1, 16)
+    try:
+        assert V.vsf_plan_get_info(ok).n_qblocks == 1
+    finally:
+        V.vsf_plan_destroy(ok)
