@@ -502,6 +502,7 @@ int32_t vsf_muon_chunk_count(const vsf_plan* plan) {
 vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream) {
+  vsf::Range nvtx_range("vsf_muon_step");
   if (plan == nullptr || packed_grad == nullptr || momentum == nullptr || master == nullptr ||
       packed_bf16 == nullptr || hp == nullptr || d_workspace == nullptr)
     return fail(VSF_ERR_ARG, "vsf_muon_step: NULL argument");

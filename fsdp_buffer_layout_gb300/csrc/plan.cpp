@@ -320,6 +320,7 @@ extern "C" {
 
 vsf_status vsf_plan_create(const vsf_tensor_desc* descs, int32_t n, int32_t m, int64_t g_coll,
                            int32_t order, vsf_plan** out) {
+  vsf::Range nvtx_range("vsf_plan_create");
   const auto t0 = std::chrono::steady_clock::now();
   if (out == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_create: out is NULL");
   *out = nullptr;

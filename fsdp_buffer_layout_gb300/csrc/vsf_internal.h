@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 #include <string>
 #include <vector>
 
@@ -124,6 +126,14 @@ struct vsf_plan {
 };
 
 namespace vsf {
+// A named host range around one ABI call, for profilers' timelines (NVTX v3,
+// header only; without an attached tool each push and pop is a no-op call).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 vsf_status fail(vsf_status s, const std::string& msg);
 vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1);
 }  // namespace vsf

@@ -574,6 +574,7 @@ using namespace vsf;
 extern "C" {
 
 vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void* stream) {
+  vsf::Range nvtx_range("vsf_plan_upload");
   if (plan == nullptr || d_workspace == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_upload: NULL");
   if (misaligned(d_workspace)) return fail(VSF_ERR_ALIGN, "vsf_plan_upload: workspace alignment");
   if (bytes < plan->layout.bytes) return fail(VSF_ERR_ARG, "vsf_plan_upload: workspace too small");
@@ -714,6 +715,7 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
 
 vsf_status vsf_pack(const vsf_plan* plan, const void* const* grads, int32_t dtype,
                     void* packed_grad, void* stream) {
+  vsf::Range nvtx_range("vsf_pack");
   vsf_status s = check_ready(plan, "vsf_pack");
   if (s != VSF_OK) return s;
   if (packed_grad == nullptr) return fail(VSF_ERR_ARG, "vsf_pack: NULL packed buffer");
@@ -727,6 +729,7 @@ vsf_status vsf_pack(const vsf_plan* plan, const void* const* grads, int32_t dtyp
 vsf_status vsf_group_norm_scale(const vsf_plan* plan, const void* packed_grad, int32_t dtype,
                                 const vsf_adam_hparams* hp, float* d_factor, double* d_norm,
                                 void* stream) {
+  vsf::Range nvtx_range("vsf_group_norm_scale");
   vsf_status s = check_ready(plan, "vsf_group_norm_scale");
   if (s != VSF_OK) return s;
   if (plan->rank_begin != 0 || plan->rank_end != plan->m)
@@ -757,6 +760,7 @@ vsf_status vsf_group_norm_scale(const vsf_plan* plan, const void* packed_grad, i
 
 vsf_status vsf_group_sumsq(const vsf_plan* plan, const void* packed_grad, int32_t dtype,
                            double* d_sumsq, void* stream) {
+  vsf::Range nvtx_range("vsf_group_sumsq");
   vsf_status s = check_ready(plan, "vsf_group_sumsq");
   if (s != VSF_OK) return s;
   if (d_sumsq == nullptr) return fail(VSF_ERR_ARG, "vsf_group_sumsq: NULL d_sumsq");
@@ -790,6 +794,7 @@ vsf_status vsf_selftest_wait_timeout(unsigned* d_err, uint64_t limit_ns, void* s
 
 vsf_status vsf_group_scale_from_sumsq(const double* d_sumsq, const vsf_adam_hparams* hp,
                                       float* d_factor, double* d_norm, void* stream) {
+  vsf::Range nvtx_range("vsf_group_scale_from_sumsq");
   if (d_sumsq == nullptr || hp == nullptr || d_factor == nullptr)
     return fail(VSF_ERR_ARG, "vsf_group_scale_from_sumsq: NULL argument");
   if (hp->world < 1) return fail(VSF_ERR_ARG, "vsf_group_scale_from_sumsq: world must be >= 1");
@@ -803,6 +808,7 @@ vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t
                           const float* d_factor, float* master, void* m_state, void* v_state,
                           float* m_scale, float* v_scale, uint16_t* packed_bf16,
                           const vsf_adam_hparams* hp, int32_t step, void* stream) {
+  vsf::Range nvtx_range("vsf_adam8_step");
   vsf_status s = check_ready(plan, "vsf_adam8_step");
   if (s != VSF_OK) return s;
   if (hp == nullptr || packed_grad == nullptr || d_factor == nullptr || master == nullptr ||
@@ -829,6 +835,7 @@ vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t
 
 vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* const* params,
                       void* stream) {
+  vsf::Range nvtx_range("vsf_unpack");
   vsf_status s = check_ready(plan, "vsf_unpack");
   if (s != VSF_OK) return s;
   if (packed_bf16 == nullptr) return fail(VSF_ERR_ARG, "vsf_unpack: NULL packed buffer");
@@ -864,6 +871,7 @@ vsf_status launch_group(const vsf_plan* plan, void* dst, const void* src, float 
 extern "C" {
 
 vsf_status vsf_group_zero(const vsf_plan* plan, void* buf, int32_t dtype, void* stream) {
+  vsf::Range nvtx_range("vsf_group_zero");
   using namespace vsf;
   vsf_status s = check_ready(plan, "vsf_group_zero");
   if (s != VSF_OK) return s;
@@ -877,6 +885,7 @@ vsf_status vsf_group_zero(const vsf_plan* plan, void* buf, int32_t dtype, void* 
 
 vsf_status vsf_group_scale(const vsf_plan* plan, void* buf, int32_t dtype, float alpha,
                            void* stream) {
+  vsf::Range nvtx_range("vsf_group_scale");
   using namespace vsf;
   vsf_status s = check_ready(plan, "vsf_group_scale");
   if (s != VSF_OK) return s;
@@ -890,6 +899,7 @@ vsf_status vsf_group_scale(const vsf_plan* plan, void* buf, int32_t dtype, float
 
 vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, const void* src,
                          int32_t src_dtype, void* stream) {
+  vsf::Range nvtx_range("vsf_group_add");
   using namespace vsf;
   vsf_status s = check_ready(plan, "vsf_group_add");
   if (s != VSF_OK) return s;
@@ -1001,6 +1011,7 @@ extern "C" vsf_status vsf_group_norm_scale_static(const void* const* grads, cons
                                                   const vsf_adam_hparams* hp, float* d_factor,
                                                   double* d_norm, void* stream) {
   using namespace vsf;
+  Range nvtx_range("vsf_group_norm_scale_static");
   if (grads == nullptr || numel == nullptr || hp == nullptr || d_factor == nullptr)
     return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: NULL argument");
   if (n < 1 || n > kStaticMaxTensors)
