@@ -437,6 +437,7 @@ def muon_arm(args, rank: int, world: int):
     iterations of 3 GEMMs, update of master and bf16 copy), copy-out."""
     import torch
     import torch.distributed as dist
+    from fsdp_buffer_layout_gb300 import vsf as V
     from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
     from synth import workloads as W
 
@@ -594,10 +595,11 @@ def muon_arm(args, rank: int, world: int):
                 "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(host_g.numel() * 2),
                 "d2h_bytes_per_step": int(host_p.numel() * 2)},
-        "gpu_launches": (2 + 3 * ss.muon_chunks()) * args.steps,
-        "gpu_launches_note": "own kernels: copy-in, copy-out, and momentum, normalise and "
-                             "update per batched chunk of same-shape matrices; the 15 "
-                             "Newton-Schulz GEMMs per chunk are cuBLASLt launches, not counted",
+        "gpu_launches": (2 + V.vsf_muon_kernel_launches(ss.plan, 5)) * args.steps,
+        "gpu_launches_note": "own kernels: copy-in, copy-out, and per batched chunk of "
+                             "same-shape matrices momentum, normalise, update and the block "
+                             "transposes of the symmetric products; the Newton-Schulz GEMMs "
+                             "are cuBLASLt launches, not counted",
         "clocks": clocks,
     }
 

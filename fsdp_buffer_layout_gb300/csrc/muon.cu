@@ -499,6 +499,16 @@ int32_t vsf_muon_chunk_count(const vsf_plan* plan) {
   return plan == nullptr ? 0 : (int32_t)muon_chunks(plan).size();
 }
 
+int64_t vsf_muon_kernel_launches(const vsf_plan* plan, int32_t ns_steps) {
+  if (plan == nullptr || ns_steps < 0) return 0;
+  int64_t n = 0;
+  for (const MuonChunk& c : muon_chunks(plan)) {
+    const int64_t nm = std::min(c.R, c.C);
+    n += 3 + (nm >= kSymBlockMin && nm % 16 == 0 ? 2 * (int64_t)ns_steps : 0);
+  }
+  return n;
+}
+
 vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream) {

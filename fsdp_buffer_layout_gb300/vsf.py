@@ -129,6 +129,8 @@ def lib():
             L.vsf_muon_workspace_bytes.argtypes = [vp]
             L.vsf_muon_chunk_count.restype = ctypes.c_int32
             L.vsf_muon_chunk_count.argtypes = [vp]
+            L.vsf_muon_kernel_launches.restype = ctypes.c_int64
+            L.vsf_muon_kernel_launches.argtypes = [vp, ctypes.c_int32]
             L.vsf_muon_step.restype = st
             L.vsf_muon_step.argtypes = [vp, vp, vp, vp, vp, P(vsf_muon_hparams), vp,
                                         ctypes.c_size_t, vp]
@@ -305,6 +307,10 @@ def vsf_muon_workspace_bytes(plan: int) -> int:
 
 def vsf_muon_chunk_count(plan: int) -> int:
     return int(lib().vsf_muon_chunk_count(plan))
+
+
+def vsf_muon_kernel_launches(plan: int, ns_steps: int = 5) -> int:
+    return int(lib().vsf_muon_kernel_launches(plan, ns_steps))
 
 
 def vsf_muon_step(plan: int, packed_grad: int, momentum: int, master: int, packed_bf16: int,

@@ -301,6 +301,11 @@ typedef struct {
 vsf_status vsf_muon_select_roots(const vsf_plan* plan, int32_t* root, double* load_balance);
 size_t vsf_muon_workspace_bytes(const vsf_plan* plan);
 int32_t vsf_muon_chunk_count(const vsf_plan* plan);
+/* Launches of the library's own kernels in one vsf_muon_step with ns_steps
+ * iterations: 3 per chunk, plus 2 per iteration (the block transposes of the
+ * two symmetric products) for chunks whose n = min(R, C) >= 1024 is a multiple
+ * of 16. The cuBLASLt GEMMs are not counted. 0 for a NULL plan. */
+int64_t vsf_muon_kernel_launches(const vsf_plan* plan, int32_t ns_steps);
 vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream);
