@@ -220,6 +220,26 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+def host_link_ms(host_in, dev_in, host_out, dev_out, s_in, s_out, steps: int) -> float:
+    """The host link's bound on one end-to-end step: the same copy-in and
+    copy-out, issued concurrently on the two copy streams with no compute,
+    `steps` times; milliseconds per step."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(s_in)
+    s_out.wait_event(a)
+    for _ in range(steps):
+        with torch.cuda.stream(s_in):
+            dev_in.copy_(host_in, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            host_out.copy_(dev_out, non_blocking=True)
+    s_in.wait_stream(s_out)
+    b.record(s_in)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def gpu_arm(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -253,15 +273,18 @@ def gpu_arm(args, rank: int, world: int):
     params = [dev_p[s:s + n] for s, n in zip(starts, ss.numels)]
     gviews = pviews = None
     if args.zero_copy:
-        # gradients and parameters live in the packed buffers (address map)
-        gviews = ss.views(ss.packed_grad.view(torch.int16))
-        pviews = ss.views(ss.packed_bf16.view(torch.int16))
-        for v, g in zip(gviews, grads):
+        # gradients and parameters live in the packed buffers (address map);
+        # the end-to-end leg double-buffers them (a second gradient and bf16
+        # buffer with their own views)
+        zc_grad = [ss.packed_grad, torch.zeros_like(ss.packed_grad)]
+        zc_bf = [ss.packed_bf16, torch.zeros_like(ss.packed_bf16)]
+        gviews = [ss.views(b.view(torch.int16)) for b in zc_grad]
+        pviews = [ss.views(b.view(torch.int16)) for b in zc_bf]
+        for v, g in zip(gviews[0], grads):
             v.copy_(g)
 
-    def gviews_of(_buf):
-        # zero-copy mode has one packed gradient buffer: its views
-        return gviews
+    def gviews_of(buf):
+        return gviews[buf]
     torch.cuda.synchronize(dev)
 
     # pack (or norm pass) + norm finalize + AdamW kernels (+ unpack)
@@ -348,9 +371,8 @@ def gpu_arm(args, rank: int, world: int):
     e_start.record(s_in)
     s_out.wait_event(e_start)
     stream.wait_event(e_start)
-    # buffer reuse distance: two device buffer sets, or the single packed
-    # buffers in zero-copy mode
-    dist_k = 1 if args.zero_copy else 2
+    # buffer reuse distance: two device buffer sets in both modes
+    dist_k = 2
     for k in range(e2e_steps):
         buf = k % 2
         with torch.cuda.stream(s_in):
@@ -368,7 +390,7 @@ def gpu_arm(args, rank: int, world: int):
                 stream.wait_event(ev_out[k - dist_k])  # copy-out k-d has read this buffer
             step += 1
             if args.zero_copy:
-                ss.zero_copy_step(step)
+                ss.zero_copy_step(step, zc_grad[buf], zc_bf[buf])
             else:
                 ss.pack(grads2[buf])
                 ss.group_norm_scale()
@@ -379,7 +401,7 @@ def gpu_arm(args, rank: int, world: int):
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[k])
             if args.zero_copy:
-                for v, s0, n in zip(pviews, starts, ss.numels):
+                for v, s0, n in zip(pviews[buf], starts, ss.numels):
                     host_p[s0:s0 + n].copy_(v, non_blocking=True)
             else:
                 host_p.copy_(dev_p2[buf], non_blocking=True)
@@ -392,6 +414,7 @@ def gpu_arm(args, rank: int, world: int):
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
+    link_ms = host_link_ms(host_g, dev_g2[0], host_p, dev_p2[0], s_in, s_out, e2e_steps)
 
     peak, peak_kind = measured_peak()
     adam_gbs = nbytes["adam"] / (k_adam * 1e-3) / 1e9
@@ -424,7 +447,9 @@ def gpu_arm(args, rank: int, world: int):
         "e2e": {"value": round(nbytes["step"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(host_g.numel() * 2),
-                "d2h_bytes_per_step": int(host_p.numel() * 2 + 16)},
+                "d2h_bytes_per_step": int(host_p.numel() * 2 + 16),
+                "host_link_ms_per_step": round(link_ms, 5),
+                "frac_of_host_link_bound": round(link_ms / e2e_ms, 4)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }

@@ -155,11 +155,21 @@ class ShardStep:
             out.append(v)
         return out
 
-    def zero_copy_step(self, step: int):
+    def zero_copy_step(self, step: int, packed_grad=None, packed_bf16=None):
         """One step when gradients and parameters are views of the packed
-        buffers: group norm/scale on the packed gradient, then AdamW."""
-        self.group_norm_scale(standalone=True)
-        self.adam(step)
+        buffers: group norm/scale on the packed gradient, then AdamW. A caller
+        that double-buffers passes the gradient and bf16 buffers of this step
+        (same size and type as self.packed_grad / self.packed_bf16); the
+        optimizer state is always this object's."""
+        g = self.packed_grad if packed_grad is None else packed_grad
+        out = self.packed_bf16 if packed_bf16 is None else packed_bf16
+        V.vsf_group_norm_scale(self.plan, g.data_ptr(), self.grad_dtype, self.hp,
+                               self.factor.data_ptr(), self.norm.data_ptr(),
+                               self.stream.cuda_stream)
+        V.vsf_adam8_step(self.plan, g.data_ptr(), self.grad_dtype, self.factor.data_ptr(),
+                         self.master.data_ptr(), self.m_state.data_ptr(), self.v_state.data_ptr(),
+                         self.m_scale.data_ptr(), self.v_scale.data_ptr(), out.data_ptr(),
+                         self.hp, step, self.stream.cuda_stream)
 
     def step(self, grads, params, step: int):
         """pack -> group norm/scale -> 8-bit AdamW -> unpack."""
