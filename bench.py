@@ -706,20 +706,34 @@ def group_ops_arm(args, rank: int, world: int):
     op_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(len(ops))]
 
     # end to end: each step copies a micro-batch gradient in from pinned host
-    # memory into the packed buffer, accumulates it into the fp32 buffer and
-    # reads one accumulated value back
+    # memory into a packed buffer, accumulates it into the fp32 buffer and
+    # reads one accumulated value back; two gradient buffers, so the copy-in
+    # of step k+1 overlaps the accumulation of step k
     host_g = g2.view(torch.int16).cpu().pin_memory()
     host_out = torch.empty(1, dtype=torch.float32).pin_memory()
+    gbuf = [g2, torch.zeros_like(g2)]
+    s_in = torch.cuda.Stream(dev)
     e2e_steps = max(3, min(args.steps, 50))
+    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e_start.record(stream)
-        for _ in range(e2e_steps):
-            g2.view(torch.int16).copy_(host_g, non_blocking=True)
-            ops[3]()
+    e_start.record(s_in)
+    stream.wait_event(e_start)
+    for k in range(e2e_steps):
+        b = gbuf[k % 2]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_done[k - 2])
+            b.view(torch.int16).copy_(host_g, non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[k])
+            V.vsf_group_add(ss.plan, acc.data_ptr(), V.VSF_FP32, b.data_ptr(), V.VSF_BF16, st)
             host_out.copy_(acc[:1], non_blocking=True)
-        e_end.record(stream)
+            ev_done[k].record(stream)
+    s_in.wait_stream(stream)
+    e_end.record(s_in)
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
 
@@ -746,7 +760,7 @@ def group_ops_arm(args, rank: int, world: int):
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": round(nbytes[3] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "workload": "H2D of one bf16 gradient, "
-                "fp32 accumulate, D2H of one value",
+                "fp32 accumulate, D2H of one value; double-buffered",
                 "h2d_bytes_per_step": int(host_g.numel() * 2), "d2h_bytes_per_step": 4},
         "gpu_launches": len(ops) * args.steps,
         "clocks": clocks,

@@ -115,6 +115,24 @@ def test_large_blocks_use_clusters():
     compare(case, run_gpu(case), run_oracle(case))
 
 
+def test_large_blocks_fp32_gradients():
+    """fp32 gradients on large blocks: the bulk-copy ring then holds 2 slots
+    of 80 KB instead of 3 of 64 KB, with clusters of 2 for the 352K-element
+    blocks, and 128x128 tiles through the 2-D tensor copies."""
+    specs = [((96, 11008), W.GRAN_ROWS, 32, 0), ((512, 512), W.GRAN_TILE, 128, 128),
+             ((4096,), W.GRAN_ELEM, 0, 0)]
+    case = _normal_case(specs, m=4, g=128, steps=3)
+    case.grad_dtype = 1
+
+    def grads(s, t):  # seeded fp32 gradients (full fp32 mantissas)
+        from synth import DIST_NORMAL, KIND_GRAD, fill_f32, key
+        n = int(np.prod(specs[t][0]))
+        return fill_f32(key(11, s, t, KIND_GRAD), DIST_NORMAL, 1e-3, 0, np.empty(n, np.float32))
+
+    case.grads = grads
+    compare(case, run_gpu(case), run_oracle(case))
+
+
 def test_tiles_on_every_path():
     """Full tiles of mapped tile tensors (2-D tensor copies: 128x128, 32x64),
     ragged bottom tiles and tiles wider than a copy box (register kernel),
