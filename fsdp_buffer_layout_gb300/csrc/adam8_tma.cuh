@@ -2,8 +2,8 @@
 // TMA (bulk-copy) pipeline. Included by vsf_kernels.cu after adam8.cuh (same
 // element math, same results bit for bit).
 //
-// Structure of one CTA: warp 0..kConsumerWarps-1 compute, the last warp is
-// the producer. The producer streams fixed-size chunks of the CTA's share of
+// Structure of one CTA: warps 0..W-1 compute, the last warp (W) is the
+// producer. The producer streams fixed-size chunks of the CTA's share of
 // each block from global memory into a ring of shared-memory slots with
 // cp.async.bulk (the Blackwell bulk-copy engine), each slot guarded by a
 // "full" mbarrier (transaction bytes) and an "empty" mbarrier (one arrival per
@@ -24,22 +24,30 @@
 // then wrong but every CTA still finishes, so no thread hangs and no CTA
 // leaves while a copy or a peer's write into it is still pending).
 
-constexpr int kConsumerWarps = VSF_TMA_WARPS;   // consumer warps per CTA
-constexpr int kTmaGroups = VSF_TMA_GROUPS;       // 8-element groups per thread and chunk
-constexpr int kTmaChunk = kTmaChunkElems;         // elements per ring chunk
-constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
+// One shape of the kernel: W consumer warps and one producer warp per CTA,
+// chunks of W * 512 elements, and a ring of 200 KB at 16 warps or
+// proportionally less for narrower shapes, so that 16 / W CTAs share an SM.
+template <int W>
+struct TmaShape {
+  static constexpr int threads = (W + 1) * 32;
+  static constexpr int chunk = tma_chunk_elems(W);
+  static constexpr int ctas_per_sm = kTmaWideWarps / W;
+  static constexpr uint32_t ring_bytes = 200u * 1024u / ctas_per_sm;
+};
 constexpr uint32_t kSuspendNs = 1u << 20;        // sleep limit of one barrier test
 constexpr uint64_t kWaitNs = 2000000000ull;       // bound of one wait: 2 s
 
-template <typename GT>
+template <typename GT, int W>
 struct TmaLayout {
+  static constexpr uint32_t chunk = TmaShape<W>::chunk;
   static constexpr uint32_t grad = 0;
-  static constexpr uint32_t mq = kTmaChunk * sizeof(GT);
-  static constexpr uint32_t vq = mq + kTmaChunk;
-  static constexpr uint32_t master = vq + kTmaChunk;
-  static constexpr uint32_t slot = master + kTmaChunk * 4;  // bytes per slot
-  // ring depth: as many slots as fit in 200 KB, at least two
-  static constexpr int slots = (200u * 1024u / slot) < 2 ? 2 : (int)(200u * 1024u / slot);
+  static constexpr uint32_t mq = chunk * sizeof(GT);
+  static constexpr uint32_t vq = mq + chunk;
+  static constexpr uint32_t master = vq + chunk;
+  static constexpr uint32_t slot = master + chunk * 4;  // bytes per slot
+  // ring depth: as many slots as fit in the shape's ring, at least two
+  static constexpr uint32_t budget = TmaShape<W>::ring_bytes;
+  static constexpr int slots = (budget / slot) < 2 ? 2 : (int)(budget / slot);
   static constexpr uint32_t ring = slot * slots;
   // then: full[slots], empty[slots], maxbar[2] (8 B each), and the block
   // maxima maxima[2][kMaxCluster][kMaxUnitTiles] (float2)
@@ -171,7 +179,7 @@ __device__ __forceinline__ void dsmem_arrive(uint32_t local_bar, uint32_t rank) 
 }
 
 // One ring chunk of a work unit. Contiguous blocks (one row) are cut into
-// kTmaChunk-element pieces; a unit of k tiles into boxes of whole rows of
+// CH-element pieces (CH: the shape's chunk); a unit of k tiles into boxes of whole rows of
 // W = k * tile_cols elements (a power of two <= 256), which the tensor copy
 // packs back to back in the slot.
 struct TmaChunk {
@@ -190,30 +198,33 @@ struct TmaChunk {
 
 // Unit width: the block's row length times its tiles (1 for contiguous).
 __device__ __forceinline__ int tma_width(const QBlock& b, int k) { return b.ncols * k; }
+template <int CH>
 __device__ __forceinline__ int tma_rows_per_chunk(const QBlock& b, int k) {
-  return kTmaChunk / tma_width(b, k);
+  return CH / tma_width(b, k);
 }
 
 // Chunks [c0, c1) of a unit that CTA `crank` of CL owns.
+template <int CH>
 __device__ __forceinline__ void tma_share(const QBlock& b, int k, int CL, int crank, int& c0,
                                           int& c1) {
-  const int rpc = b.nrows == 1 ? 1 : tma_rows_per_chunk(b, k);
-  const int nch = b.nrows == 1 ? (b.ncols + kTmaChunk - 1) / kTmaChunk : (b.nrows + rpc - 1) / rpc;
+  const int rpc = b.nrows == 1 ? 1 : tma_rows_per_chunk<CH>(b, k);
+  const int nch = b.nrows == 1 ? (b.ncols + CH - 1) / CH : (b.nrows + rpc - 1) / rpc;
   const int per = (nch + CL - 1) / CL;
   c0 = min(nch, crank * per);
   c1 = min(nch, c0 + per);
 }
 
+template <int CH>
 __device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int k, int c) {
   TmaChunk ch;
   if (b.nrows == 1) {
-    ch.gstart = b.base + (int64_t)c * kTmaChunk;
+    ch.gstart = b.base + (int64_t)c * CH;
     ch.rows = 1;
-    ch.row_len = (int)min64(kTmaChunk, (int64_t)b.ncols - (int64_t)c * kTmaChunk);
+    ch.row_len = (int)min64(CH, (int64_t)b.ncols - (int64_t)c * CH);
     ch.stride = 0;
     ch.row_log2 = 0;
   } else {
-    const int rpc = tma_rows_per_chunk(b, k);
+    const int rpc = tma_rows_per_chunk<CH>(b, k);
     const int r0 = c * rpc;
     ch.gstart = b.base + (int64_t)r0 * b.stride;
     ch.rows = min(rpc, b.nrows - r0);
@@ -224,13 +235,14 @@ __device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int k, int c) {
   return ch;
 }
 
-template <typename GT>
-__global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
+template <typename GT, int W>
+__global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm) adam_tma_kernel(
     const __grid_constant__ TileMaps maps, const QBlock* __restrict__ qb,
     const int32_t* __restrict__ list, const int32_t* __restrict__ ktab, int nlist, int nclusters,
     const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
     uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k, unsigned* err) {
-  using Lay = TmaLayout<GT>;
+  using Lay = TmaLayout<GT, W>;
+  constexpr int CH = TmaShape<W>::chunk;
   constexpr int kTmaSlots = Lay::slots;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // tensor copies want 128-byte aligned destinations: round the base up
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
   if (tid == 0) {
     for (int s = 0; s < kTmaSlots; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps);
+      mbar_init(empty_bar(s), W);
     }
     mbar_init(max_bar(0), CL);
     mbar_init(max_bar(1), CL);
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
   }
   cluster.sync();
 
-  if (warp == kConsumerWarps) {
+  if (warp == W) {
     // ---------------- producer warp: lane 0 waits for the slot, posts the
     // byte count and issues the copies (one 1-D bulk copy per array for a
     // contiguous chunk, one 2-D tensor copy per array for a tile chunk).
@@ -268,7 +280,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       const QBlock b = qb[list[j]];
       const int kt = ktab[j];
       int c0, c1;
-      tma_share(b, kt, CL, crank, c0, c1);
+      tma_share<CH>(b, kt, CL, crank, c0, c1);
       int mi = 0;
       if (b.tx >= 0)
         while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
           if (lane == 0) {
             const int s = p % kTmaSlots;
             const uint32_t round = p / kTmaSlots;
-            const TmaChunk ch = tma_chunk(b, kt, c);
+            const TmaChunk ch = tma_chunk<CH>(b, kt, c);
             const uint32_t len = (uint32_t)ch.len();
             if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
             const uint32_t fb = full_bar(s);
@@ -296,7 +308,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
               bulk_g2s(slot + Lay::vq, vq + e, len, fb, pol);
               if (ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, fb, drop);
             } else {
-              const int y = b.ty + c * tma_rows_per_chunk(b, kt);
+              const int y = b.ty + c * tma_rows_per_chunk<CH>(b, kt);
               tensor2d_g2s(slot + Lay::grad, &maps.m[mi][0], b.tx, y, fb, pol);
               tensor2d_g2s(slot + Lay::mq, &maps.m[mi][1], b.tx, y, fb, pol);
               tensor2d_g2s(slot + Lay::vq, &maps.m[mi][2], b.tx, y, fb, pol);
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
     c.alpha = f2(k.alpha);
     c.factor = f2(*d_factor);
     const uint64_t drop = l2_policy_evict_first();
-    __shared__ float red[2][2][kConsumerWarps][kMaxUnitTiles];
+    __shared__ float red[2][2][W][kMaxUnitTiles];
     uint32_t p = 0;
     int nb = 0;  // units done by this CTA
     for (int j = cid; j < nlist; j += nclusters, ++nb) {
@@ -344,7 +356,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
       c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
       int c0, c1;
-      tma_share(b, kt, CL, crank, c0, c1);
+      tma_share<CH>(b, kt, CL, crank, c0, c1);
       const int par = nb & 1;
 
       // phase 1: maxima of the new moments
@@ -352,11 +364,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const int len = tma_chunk(b, kt, ci).len();
+        const int len = tma_chunk<CH>(b, kt, ci).len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll
         for (int gi = 0; gi < kTmaGroups; ++gi) {
-          const int g = tid + gi * kConsumerWarps * 32;
+          const int g = tid + gi * W * 32;
           if (g * 8 < len) {
             Raw r;
             r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 8 * sizeof(GT));
@@ -383,13 +395,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
         red[par][0][warp][lane / gpt] = mx;
         red[par][1][warp][lane / gpt] = vx;
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
       if (warp == 0) {
         // the CTA's maxima, one warp entry per lane; lane r then writes them
         // into cluster rank r and arrives there (release covers its stores)
         for (int t = 0; t < kt; ++t) {
-          float bm = lane < kConsumerWarps ? red[par][0][lane][t] : 0.0f;
-          float bv = lane < kConsumerWarps ? red[par][1][lane][t] : 0.0f;
+          float bm = lane < W ? red[par][0][lane][t] : 0.0f;
+          float bv = lane < W ? red[par][1][lane][t] : 0.0f;
           bm = fmaxf(bm, 0.0f);
           bv = fmaxf(bv, 0.0f);
 #pragma unroll
@@ -421,12 +433,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) adam_tma_kernel(
       for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const TmaChunk ch = tma_chunk(b, kt, ci);
+        const TmaChunk ch = tma_chunk<CH>(b, kt, ci);
         const int len = ch.len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll
         for (int gi = 0; gi < kTmaGroups; ++gi) {
-          const int g = tid + gi * kConsumerWarps * 32;
+          const int g = tid + gi * W * 32;
           if (g * 8 < len) {
             Raw r;
             r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 8 * sizeof(GT));

@@ -158,8 +158,9 @@ vsf_status check_tables(const vsf_plan& plan) {
 // crosses a rank boundary: RaggedShard's Non-Sharded Block rule for row and
 // tile atoms; element chunks start on g_coll multiples, as do offsets and
 // S). Buffer elements are counted from the window start r0 * S.
-vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
+static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
   const int n = plan->n;
+  const int64_t chunk = tma_chunk_elems(plan->tma_warps);
   const int64_t g_coll = plan->g_coll;
   const int64_t wlo = (int64_t)r0 * plan->S, whi = (int64_t)r1 * plan->S;
   plan->rank_begin = r0;
@@ -200,7 +201,7 @@ vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
       if (bc >= 32 && bc <= 256 && (bc & (bc - 1)) == 0) {
         k = std::min<int64_t>(256 / bc, kMaxUnitTiles);
         const int64_t box_cols = k * bc;
-        const int64_t box_rows = std::min<int64_t>(br, kTmaChunkElems / box_cols);
+        const int64_t box_rows = std::min<int64_t>(br, chunk / box_cols);
         const int64_t map_off = off + row_lo * x.cols;
         if (box_rows >= 1 && box_rows <= 256 && br % box_rows == 0 && x.cols % 16 == 0 &&
             map_off % 16 == 0 && x.cols >= box_cols) {
@@ -307,6 +308,18 @@ vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
   L.partials = section(sizeof(double) * kMaxCopyGrid);
   L.bytes = (cur + 255) / 256 * 256;
   return VSF_OK;
+}
+
+// The tables with the wide bulk-copy chunk; if every work unit is small,
+// again with the narrow one (tile copy boxes follow the chunk size; a smaller
+// chunk can only move tile units to the register kernel, never enlarge one).
+vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
+  plan->tma_warps = kTmaWideWarps;
+  const vsf_status st = build_tables_for(plan, r0, r1);
+  if (st != VSF_OK || plan->max_tma_elems == 0 || plan->max_tma_elems > kTmaNarrowMaxUnit)
+    return st;
+  plan->tma_warps = kTmaNarrowWarps;
+  return build_tables_for(plan, r0, r1);
 }
 
 
@@ -427,6 +440,7 @@ vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info) {
   info->padding_ratio = 1.0 - (double)plan->real / (double)plan->total;
   info->plan_seconds = plan->plan_seconds;
   info->order_used = plan->order_used;
+  info->bulk_warps = plan->tma_warps;
   info->n_bulk_units = (int64_t)plan->tma_blocks.size();
   info->n_register_blocks = (int64_t)plan->big_blocks.size();
   info->n_element_chunks = (int64_t)plan->small_blocks.size();

@@ -21,15 +21,21 @@ constexpr int kMaxTensors = 2048;
 // device is known.
 constexpr int kMaxCopyGrid = 4096;
 
-// Bulk-copy (TMA) AdamW kernel geometry: consumer warps per CTA, 8-element
-// groups per consumer thread, hence elements per ring chunk.
-#ifndef VSF_TMA_WARPS
-#define VSF_TMA_WARPS 16
-#endif
-#ifndef VSF_TMA_GROUPS
-#define VSF_TMA_GROUPS 2
-#endif
-constexpr int kTmaChunkElems = VSF_TMA_WARPS * 32 * 8 * VSF_TMA_GROUPS;
+// Bulk-copy (TMA) AdamW kernel geometry. Each consumer thread takes two
+// 8-element groups of a ring chunk, so a chunk holds warps * 512 elements.
+// Two shapes, chosen per plan: wide (16 consumer warps, one CTA per SM) for
+// plans with large work units, narrow (4 consumer warps, four CTAs per SM)
+// when every unit has at most kTmaNarrowMaxUnit elements. Small units leave a
+// single pipeline per SM idle while its consumers wait for the block maxima;
+// four pipelines per SM overlap those waits. The bound keeps the narrow
+// shape cluster-free: 4 CTAs on each of 152 SMs, each holding one unit's
+// gradient and codes (4 bytes an element for bf16 gradients) in L2 between
+// the two passes, stay within the 128 MB L2 budget (608 * 4 * 48 Ki = 114 MB).
+constexpr int kTmaGroups = 2;
+constexpr int kTmaWideWarps = 16;
+constexpr int kTmaNarrowWarps = 4;
+constexpr int64_t kTmaNarrowMaxUnit = 48 * 1024;
+constexpr int tma_chunk_elems(int warps) { return warps * 32 * 8 * kTmaGroups; }
 
 // One quantisation block as the kernels see it: a row-major region.
 struct QBlock {
@@ -105,6 +111,7 @@ struct vsf_plan {
   std::vector<int32_t> small_blocks;  // ELEM chunks: warp kernel
   int64_t max_big_elems = 0;
   int64_t max_tma_elems = 0;
+  int tma_warps = vsf::kTmaWideWarps;  // shape of the bulk-copy kernel (consumer warps)
   vsf::DeviceLayout layout;
 
   // Set by vsf_plan_upload.

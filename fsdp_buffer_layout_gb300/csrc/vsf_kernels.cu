@@ -253,6 +253,23 @@ __global__ void factor_kernel(const double* __restrict__ d_sumsq, int world, dou
 #include "adam8.cuh"
 #include "adam8_tma.cuh"
 
+// The bulk-copy kernel instance of a plan's shape, with its block size and
+// dynamic shared memory.
+template <typename GT>
+struct TmaLaunch {
+  decltype(&adam_tma_kernel<GT, kTmaWideWarps>) fn;
+  int threads;
+  uint32_t smem;
+};
+template <typename GT>
+TmaLaunch<GT> tma_launch(int warps) {
+  if (warps == kTmaNarrowWarps)
+    return {adam_tma_kernel<GT, kTmaNarrowWarps>, TmaShape<kTmaNarrowWarps>::threads,
+            TmaLayout<GT, kTmaNarrowWarps>::total};
+  return {adam_tma_kernel<GT, kTmaWideWarps>, TmaShape<kTmaWideWarps>::threads,
+          TmaLayout<GT, kTmaWideWarps>::total};
+}
+
 // Fused group ops over every real element of a packed buffer (all tensors
 // in one launch, over the copy spans): 0 zero, 1 scale by alpha, 2 add src.
 // fp32 arithmetic with one rounding, then the buffer's type (bf16 RNE).
@@ -517,10 +534,11 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
   if (ntma > 0) {
     const int CL = plan->tma_cluster;
     const int ncl = std::min(plan->tma_clusters, ntma);
+    const TmaLaunch<GT> tl = tma_launch<GT>(plan->tma_warps);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncl * CL);
-    cfg.blockDim = dim3(kTmaThreads);
-    cfg.dynamicSmemBytes = TmaLayout<GT>::total;
+    cfg.blockDim = dim3(tl.threads);
+    cfg.dynamicSmemBytes = tl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -537,7 +555,7 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
                               master, &maps);
     if (ms != VSF_OK) return ms;
     cudaError_t e = cudaLaunchKernelEx(
-        &cfg, adam_tma_kernel<GT>, maps, qb, ws_ptr<int32_t>(plan, plan->layout.tma),
+        &cfg, tl.fn, maps, qb, ws_ptr<int32_t>(plan, plan->layout.tma),
         ws_ptr<int32_t>(plan, plan->layout.tma_k), ntma, ncl, g,
         d_factor, master, mq, vq, m_scale, v_scale, bf, k,
         reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error));
@@ -642,21 +660,24 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     if ((double)active * (double)plan->max_big_elems * 4.0 <= budget) break;
   }
 
-  // Bulk-copy kernel: one CTA per SM (its ring takes ~200 KB of shared
-  // memory); the cluster size follows the same L2 budget.
+  // Bulk-copy kernel: 16 / warps CTAs per SM (their rings take ~200 KB of
+  // shared memory together); the cluster size follows the same L2 budget.
   int tma_CL = 1, tma_ncl = 1;
   {
-    for (auto fn : {(const void*)adam_tma_kernel<uint16_t>, (const void*)adam_tma_kernel<float>}) {
-      const int bytes = fn == (const void*)adam_tma_kernel<uint16_t> ? (int)TmaLayout<uint16_t>::total
-                                                                     : (int)TmaLayout<float>::total;
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    for (int w : {kTmaWideWarps, kTmaNarrowWarps}) {
+      const TmaLaunch<uint16_t> a = tma_launch<uint16_t>(w);
+      const TmaLaunch<float> b = tma_launch<float>(w);
+      e = cudaFuncSetAttribute(a.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(b.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b.smem);
       if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (shared memory size)");
     }
+    const TmaLaunch<uint16_t> tl = tma_launch<uint16_t>(plan->tma_warps);
     for (int cand = 1; cand <= kMaxCluster; cand *= 2) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cand * 64);
-      cfg.blockDim = dim3(kTmaThreads);
-      cfg.dynamicSmemBytes = TmaLayout<uint16_t>::total;
+      cfg.blockDim = dim3(tl.threads);
+      cfg.dynamicSmemBytes = tl.smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = cand;
@@ -665,7 +686,7 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int active = 0;
-      e = cudaOccupancyMaxActiveClusters(&active, adam_tma_kernel<uint16_t>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&active, tl.fn, &cfg);
       if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (bulk-copy clusters)");
       tma_CL = cand;
       tma_ncl = std::max(1, active);

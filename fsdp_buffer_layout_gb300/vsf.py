@@ -42,7 +42,7 @@ class vsf_plan_info(ctypes.Structure):
                 ("n_qblocks", ctypes.c_int64), ("n_tensors", ctypes.c_int32),
                 ("m", ctypes.c_int32), ("g_coll", ctypes.c_int64),
                 ("padding_ratio", ctypes.c_double), ("plan_seconds", ctypes.c_double),
-                ("order_used", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("order_used", ctypes.c_int32), ("bulk_warps", ctypes.c_int32),
                 ("n_bulk_units", ctypes.c_int64), ("n_register_blocks", ctypes.c_int64),
                 ("n_element_chunks", ctypes.c_int64), ("rank_begin", ctypes.c_int32),
                 ("rank_end", ctypes.c_int32)]

@@ -98,7 +98,9 @@ typedef struct {
   double padding_ratio;  /* 1 - real / total */
   double plan_seconds;   /* host time spent in vsf_plan_create */
   int32_t order_used;    /* VSF_ORDER_* actually chosen */
-  int32_t reserved;
+  int32_t bulk_warps;    /* consumer warps per CTA of the bulk-copy AdamW kernel:
+                          * 16 (one CTA per SM), or 4 (four CTAs per SM) when
+                          * every bulk-copy unit has at most 49152 elements */
   /* how vsf_adam8_step splits the blocks (each non-zero count is one launch):
    * bulk-copy work units (contiguous blocks, or k full tiles), blocks of the
    * register kernel (ragged or unaligned), element-granular chunks */

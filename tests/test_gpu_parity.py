@@ -70,6 +70,7 @@ RAGGED = [
 
 def test_ragged_mixed_several_steps():
     case = _normal_case(RAGGED, m=5, g=128, steps=4)
+    assert _bulk_warps(case) == 4
     compare(case, run_gpu(case), run_oracle(case))
 
 
@@ -107,11 +108,23 @@ def test_all_zero_blocks_keep_zero_codes():
     assert not g["v_state"][off:off + 64 * 256].any()
 
 
+def _bulk_warps(case):
+    """Consumer warps of the bulk-copy AdamW kernel shape the case's plan uses."""
+    from fsdp_buffer_layout_gb300 import vsf as V
+    p = V.vsf_plan_create([V.make_desc(*s) for s in case.specs], case.m, case.g_coll)
+    try:
+        return V.vsf_plan_get_info(p).bulk_warps
+    finally:
+        V.vsf_plan_destroy(p)
+
+
 def test_large_blocks_use_clusters():
-    """Blocks of 352,256 elements (a 32-row stripe of an 11008-column matrix)."""
+    """Blocks of 352,256 elements (a 32-row stripe of an 11008-column matrix):
+    the wide kernel shape."""
     specs = [((96, 11008), W.GRAN_ROWS, 32, 0), ((256, 4096), W.GRAN_ROWS, 32, 0),
              ((4096,), W.GRAN_ELEM, 0, 0)]
     case = _normal_case(specs, m=4, g=128, steps=3)
+    assert _bulk_warps(case) == 16
     compare(case, run_gpu(case), run_oracle(case))
 
 
@@ -133,14 +146,20 @@ def test_large_blocks_fp32_gradients():
     compare(case, run_gpu(case), run_oracle(case))
 
 
-def test_tiles_on_every_path():
+@pytest.mark.parametrize("warps", [4, 16])
+def test_tiles_on_every_path(warps):
     """Full tiles of mapped tile tensors (2-D tensor copies: 128x128, 32x64),
     ragged bottom tiles and tiles wider than a copy box (register kernel),
-    next to element chunks: all bit-exact."""
+    next to element chunks: all bit-exact, in both kernel shapes (a tensor of
+    352,256-element row blocks selects the wide one; the copy boxes are then
+    4 times taller)."""
     specs = [((256, 512), W.GRAN_TILE, 128, 128), ((96, 256), W.GRAN_TILE, 32, 64),
              ((200, 384), W.GRAN_TILE, 64, 128), ((64, 4096), W.GRAN_TILE, 16, 1024),
              ((1024,), W.GRAN_ELEM, 0, 0)]
+    if warps == 16:
+        specs.append(((64, 11008), W.GRAN_ROWS, 32, 0))
     case = _normal_case(specs, m=4, g=128, steps=3)
+    assert _bulk_warps(case) == warps
     compare(case, run_gpu(case), run_oracle(case))
 
 
