@@ -828,8 +828,6 @@ def muon_cpu_baseline(w, threads: int | None = None):
 # of the AdamW bulk-copy kernel, from the ncu captures summarised in profiles/
 # (adam8_tma_*.md); a workload without a capture of the current kernel is None.
 TRAFFIC: dict = {
-    "llama_layer": 1.729086e9 + 1.547686e9,
-    "dsv3_block": 2.467177e9 + 2.040693e9,
 }
 
 

@@ -8,7 +8,8 @@
 // cp.async.bulk (the Blackwell bulk-copy engine), each slot guarded by a
 // "full" mbarrier (transaction bytes) and an "empty" mbarrier (one arrival per
 // consumer warp). Per block the sequence is: every phase-1 chunk (gradient and
-// codes, kept in L2 with an evict-last hint), then every phase-2 chunk
+// codes, kept in L2 with an evict-last hint; two chunks per slot where they
+// fit, as a phase-1 chunk needs half a slot), then every phase-2 chunk
 // (gradient and codes again, now L2 hits, plus the master). The producer runs
 // ahead across phases and blocks as far as the ring allows, so HBM requests
 // keep flowing while the consumers wait for the block maxima.
@@ -45,6 +46,14 @@ struct TmaLayout {
   static constexpr uint32_t vq = mq + chunk;
   static constexpr uint32_t master = vq + chunk;
   static constexpr uint32_t slot = master + chunk * 4;  // bytes per slot
+  // A phase-1 ring chunk holds no master, so where two chunks' gradient and
+  // codes fit in a slot, phase 1 takes chunks in pairs (p1 = 2): the same
+  // ring then keeps twice the phase-1 bytes in flight.
+  static constexpr int p1 = 2 * chunk * (sizeof(GT) + 2) <= slot ? 2 : 1;
+  static constexpr uint32_t grad1 = 0;
+  static constexpr uint32_t mq1 = p1 * chunk * sizeof(GT);
+  static constexpr uint32_t vq1 = mq1 + p1 * chunk;
+  static_assert(vq1 + p1 * chunk <= slot, "phase-1 chunks fit in a slot");
   // ring depth: as many slots as fit in the shape's ring, at least two
   static constexpr uint32_t budget = TmaShape<W>::ring_bytes;
   static constexpr int slots = (budget / slot) < 2 ? 2 : (int)(budget / slot);
@@ -285,34 +294,46 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       if (b.tx >= 0)
         while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
       for (int ph = 0; ph < 2; ++ph) {
-        for (int c = c0; c < c1; ++c, ++p) {
+        const int step = ph == 0 ? Lay::p1 : 1;
+        for (int c = c0; c < c1; c += step, ++p) {
           if (lane == 0) {
             const int s = p % kTmaSlots;
             const uint32_t round = p / kTmaSlots;
+            // ring chunk = chunks c .. c + n - 1 of the share (n = 2 for a
+            // phase-1 pair), adjacent in the buffer or boxes packed in order
+            const int n = min(step, c1 - c);
             const TmaChunk ch = tma_chunk<CH>(b, kt, c);
-            const uint32_t len = (uint32_t)ch.len();
+            const TmaChunk cl = n == 2 ? tma_chunk<CH>(b, kt, c + 1) : ch;
+            const uint32_t len0 = (uint32_t)ch.len();
+            const uint32_t len = len0 + (n == 2 ? (uint32_t)cl.len() : 0u);
             if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
             const uint32_t fb = full_bar(s);
-            const int64_t last = ch.gstart + (int64_t)(ch.rows - 1) * ch.stride + ch.row_len;
+            const int64_t last = cl.gstart + (int64_t)(cl.rows - 1) * cl.stride + cl.row_len;
             if (!in_bounds(k.bd, ch.gstart, last)) {
               mbar_arrive(fb);  // no copy: complete the slot's phase without data
               continue;
             }
             mbar_expect_tx(fb, len * (uint32_t)(sizeof(GT) + 2) + (ph ? len * 4u : 0u));
             const uint32_t slot = s0 + s * Lay::slot;
+            const uint32_t og = ph ? Lay::grad : Lay::grad1;
+            const uint32_t om = ph ? Lay::mq : Lay::mq1;
+            const uint32_t ov = ph ? Lay::vq : Lay::vq1;
             const uint64_t pol = ph == 0 ? keep : drop;
             if (b.tx < 0) {
               const int64_t e = ch.gstart;
-              bulk_g2s(slot + Lay::grad, grad + e, len * sizeof(GT), fb, pol);
-              bulk_g2s(slot + Lay::mq, mq + e, len, fb, pol);
-              bulk_g2s(slot + Lay::vq, vq + e, len, fb, pol);
+              bulk_g2s(slot + og, grad + e, len * sizeof(GT), fb, pol);
+              bulk_g2s(slot + om, mq + e, len, fb, pol);
+              bulk_g2s(slot + ov, vq + e, len, fb, pol);
               if (ph) bulk_g2s(slot + Lay::master, master + e, len * 4u, fb, drop);
             } else {
-              const int y = b.ty + c * tma_rows_per_chunk<CH>(b, kt);
-              tensor2d_g2s(slot + Lay::grad, &maps.m[mi][0], b.tx, y, fb, pol);
-              tensor2d_g2s(slot + Lay::mq, &maps.m[mi][1], b.tx, y, fb, pol);
-              tensor2d_g2s(slot + Lay::vq, &maps.m[mi][2], b.tx, y, fb, pol);
-              if (ph) tensor2d_g2s(slot + Lay::master, &maps.m[mi][3], b.tx, y, fb, drop);
+              for (int i = 0; i < n; ++i) {
+                const int y = b.ty + (c + i) * tma_rows_per_chunk<CH>(b, kt);
+                const uint32_t at = i * len0;  // elements before this box in the slot
+                tensor2d_g2s(slot + og + at * sizeof(GT), &maps.m[mi][0], b.tx, y, fb, pol);
+                tensor2d_g2s(slot + om + at, &maps.m[mi][1], b.tx, y, fb, pol);
+                tensor2d_g2s(slot + ov + at, &maps.m[mi][2], b.tx, y, fb, pol);
+                if (ph) tensor2d_g2s(slot + Lay::master, &maps.m[mi][3], b.tx, y, fb, drop);
+              }
             }
           }
         }
@@ -361,21 +382,22 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
 
       // phase 1: maxima of the new moments
       float mx = 0.0f, vx = 0.0f;
-      for (int ci = c0; ci < c1; ++ci, ++p) {
+      for (int ci = c0; ci < c1; ci += Lay::p1, ++p) {
         const int s = p % kTmaSlots;
         mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
-        const int len = tma_chunk<CH>(b, kt, ci).len();
+        int len = tma_chunk<CH>(b, kt, ci).len();
+        if (Lay::p1 == 2 && ci + 1 < c1) len += tma_chunk<CH>(b, kt, ci + 1).len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll
-        for (int gi = 0; gi < kTmaGroups; ++gi) {
+        for (int gi = 0; gi < Lay::p1 * kTmaGroups; ++gi) {
           const int g = tid + gi * W * 32;
           if (g * 8 < len) {
             Raw r;
-            r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 8 * sizeof(GT));
+            r.g0 = *reinterpret_cast<const uint4*>(sl + Lay::grad1 + g * 8 * sizeof(GT));
             if constexpr (sizeof(GT) == 4)
-              r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad + g * 32 + 16);
-            r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq + g * 8);
-            r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq + g * 8);
+              r.g1 = *reinterpret_cast<const uint4*>(sl + Lay::grad1 + g * 32 + 16);
+            r.cm = *reinterpret_cast<const uint2*>(sl + Lay::mq1 + g * 8);
+            r.cv = *reinterpret_cast<const uint2*>(sl + Lay::vq1 + g * 8);
             phase1_group<GT>(c, r, mx, vx);
           }
         }
