@@ -828,6 +828,8 @@ def muon_cpu_baseline(w, threads: int | None = None):
 # of the AdamW bulk-copy kernel, from the ncu captures summarised in profiles/
 # (adam8_tma_*.md); a workload without a capture of the current kernel is None.
 TRAFFIC: dict = {
+    "llama_layer": 1.733897e9 + 1.547784e9,
+    "dsv3_block": 2.478061e9 + 2.040586e9,
 }
 
 
