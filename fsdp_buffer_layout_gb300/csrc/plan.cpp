@@ -311,14 +311,20 @@ static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
 }
 
 // The tables with the wide bulk-copy chunk; if every work unit is small,
-// again with the narrow one (tile copy boxes follow the chunk size; a smaller
-// chunk can only move tile units to the register kernel, never enlarge one).
+// again with the narrow one. Tile copy boxes follow the chunk size, so a
+// smaller chunk can only move tile units to the register kernel (a stripe
+// height the shorter box does not divide), never enlarge one; if it moves
+// any, the wide tables are rebuilt and kept.
 vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
   plan->tma_warps = kTmaWideWarps;
-  const vsf_status st = build_tables_for(plan, r0, r1);
+  vsf_status st = build_tables_for(plan, r0, r1);
   if (st != VSF_OK || plan->max_tma_elems == 0 || plan->max_tma_elems > kTmaNarrowMaxUnit)
     return st;
+  const size_t wide_units = plan->tma_blocks.size();
   plan->tma_warps = kTmaNarrowWarps;
+  st = build_tables_for(plan, r0, r1);
+  if (st != VSF_OK || plan->tma_blocks.size() == wide_units) return st;
+  plan->tma_warps = kTmaWideWarps;
   return build_tables_for(plan, r0, r1);
 }
 

@@ -5,8 +5,9 @@ warps, one CTA per SM) and narrow (4 consumer warps, four CTAs per SM). A
 plan takes the narrow shape exactly when it has bulk-copy units and every
 unit holds at most 49152 elements (48 Ki); the plan info reports the choice
 as bulk_warps. Checked here on row-atom layouts, whose contiguous blocks are
-the units, so that the largest unit is known from the shapes alone, and on
-rank windows, which choose again for the blocks they hold.
+the units, so that the largest unit is known from the shapes alone, on
+rank windows, which choose again for the blocks they hold, and on tile
+stripes that only the wide shape's taller copy box divides.
 """
 import pytest
 
@@ -75,3 +76,16 @@ def test_workload_shapes():
         info = _info([(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors],
                      w.m, w.g_coll)
         assert info.bulk_warps == warps, name
+
+
+@pytest.mark.parametrize("block_rows,want", [(8, 4), (16, 4), (12, 16), (20, 16)])
+def test_tile_stripes_keep_their_bulk_copies(block_rows, want):
+    # 128-column tiles go two to a 256-column copy box of min(block_rows, 32)
+    # rows in the wide shape and min(block_rows, 8) in the narrow one; a
+    # stripe the narrow box does not divide would leave the bulk-copy kernel,
+    # so such a plan keeps the wide shape and all of its units
+    specs = [((block_rows * 4, 1024), W.GRAN_TILE, block_rows, 128)]
+    info = _info(specs, m=1, g_coll=128)
+    assert info.n_bulk_units == 4 * 1024 // 256
+    assert info.n_register_blocks == 0
+    assert info.bulk_warps == want
