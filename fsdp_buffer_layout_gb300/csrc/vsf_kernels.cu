@@ -519,6 +519,15 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
   }
   int8_t* mq = static_cast<int8_t*>(m_state);
   uint8_t* vq = static_cast<uint8_t*>(v_state);
+  // Tensor maps before any launch: an encoding error must not leave the
+  // step half applied.
+  const int ntma = (int)plan->tma_blocks.size();
+  TileMaps maps;
+  if (ntma > 0) {
+    vsf_status ms = tile_maps(plan, grad, sizeof(GT) == 2 ? VSF_BF16 : VSF_FP32, m_state, v_state,
+                              master, &maps);
+    if (ms != VSF_OK) return ms;
+  }
   // Element chunks first: a short kernel that lets the bulk-copy kernel start
   // while it runs (the two touch disjoint blocks).
   const int nsmall = (int)plan->small_blocks.size();
@@ -530,7 +539,6 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "vsf_adam8_step (element chunks)");
   }
-  const int ntma = (int)plan->tma_blocks.size();
   if (ntma > 0) {
     const int CL = plan->tma_cluster;
     const int ncl = std::min(plan->tma_clusters, ntma);
@@ -550,10 +558,6 @@ vsf_status launch_adam(const vsf_plan* plan, const void* grad, const float* d_fa
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = nsmall > 0 ? 2 : 1;
-    TileMaps maps;
-    vsf_status ms = tile_maps(plan, grad, sizeof(GT) == 2 ? VSF_BF16 : VSF_FP32, m_state, v_state,
-                              master, &maps);
-    if (ms != VSF_OK) return ms;
     cudaError_t e = cudaLaunchKernelEx(
         &cfg, tl.fn, maps, qb, ws_ptr<int32_t>(plan, plan->layout.tma),
         ws_ptr<int32_t>(plan, plan->layout.tma_k), ntma, ncl, g,

@@ -244,7 +244,15 @@ vsf_status vsf_group_scale_from_sumsq(const double* d_sumsq, const vsf_adam_hpar
  * quantized = 0: m_state / v_state are fp32 arrays of m*S; scales unused.
  * packed_grad: m*S elements of grad_dtype; d_factor: device fp32 scalar (from
  * vsf_group_norm_scale); master: fp32 m*S (in/out); packed_bf16: bf16 bits,
- * m*S (out). step >= 1. */
+ * m*S (out). step >= 1.
+ * Errors: VSF_ERR_ARG (NULL pointer, step < 1, bad grad_dtype),
+ * VSF_ERR_ALIGN, VSF_ERR_STATE (plan not uploaded), VSF_ERR_CUDA (tensor-map
+ * encoding or a launch). Every error but a failed launch is found before the
+ * first launch, so the buffers are untouched. A failed launch may follow a
+ * successful one, so the state buffers of that step are then undefined.
+ * Kernel-side failures (a bounded wait that timed out, a failed index check
+ * in the bounds-checking build) set bits in the plan's device error word
+ * (vsf_plan_device_error_offset). */
 vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t grad_dtype,
                           const float* d_factor, float* master, void* m_state, void* v_state,
                           float* m_scale, float* v_scale, uint16_t* packed_bf16,
