@@ -302,7 +302,10 @@ vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, con
  *   gives the number of batches (each: 3 own kernels and 3 * ns_steps
  *   cuBLASLt GEMMs); 0 for a NULL plan. Errors: VSF_ERR_ARG (NULL, small
  *   workspace, ns_steps < 0), VSF_ERR_ALIGN (a pointer not 16-byte aligned),
- *   VSF_ERR_STATE (plan not uploaded), VSF_ERR_CUDA (launch or cuBLASLt). */
+ *   VSF_ERR_STATE (plan not uploaded), VSF_ERR_CUDA (launch or cuBLASLt).
+ *   Argument errors are found before the first launch (buffers untouched);
+ *   after VSF_ERR_CUDA, chunks before the failing one have been updated and
+ *   the step's momentum, master and bf16 buffers are undefined. */
 typedef struct {
   double lr, momentum, weight_decay, eps, ns_a, ns_b, ns_c;
   int32_t ns_steps, reserved;
