@@ -830,6 +830,7 @@ def muon_cpu_baseline(w, threads: int | None = None):
 TRAFFIC: dict = {
     "llama_layer": 1.733897e9 + 1.547784e9,
     "dsv3_block": 2.478061e9 + 2.040586e9,
+    "moe_layer": 8.500441e9 + 6.297023e9,
 }
 
 
