@@ -40,10 +40,12 @@ def _p(a):
 
 
 def lib():
+    """The oracle library: liboracle.so, built on first use, or the library
+    named by ORACLE_LIBRARY (the mutation test's planted-mistake builds)."""
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
+            L = ctypes.CDLL(os.environ.get("ORACLE_LIBRARY") or build())
             vp, i64, i32, dbl, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                         ctypes.c_double, ctypes.c_int)
             desc = [c_int, vp, vp, vp, vp, vp]

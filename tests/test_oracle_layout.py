@@ -93,6 +93,37 @@ def test_invariants_random(seed):
         check_invariants(d, m, g, S, off)
 
 
+@pytest.mark.parametrize("seed", range(30))
+def test_order_policies_place_as_read(seed):
+    """The tensor orders of Algorithm 1's first step, as read: DEFAULT keeps the
+    input order, BLOCK sorts by atom size and SHAPE by element count, both
+    descending with ties in input order; BEST3 returns the plan of the first of
+    the three (DEFAULT, BLOCK, SHAPE) that reaches the smallest S. Tensors are
+    placed one after another, so sorting them by offset recovers the order a
+    plan used."""
+    rng = np.random.default_rng(1000 + seed)
+    d = random_desc(rng, int(rng.integers(2, 7)))
+    m = int(rng.integers(1, 6))
+    g = int(rng.choice([1, 2, 4, 8]))
+    block, _ = oracle.atoms(d, g)
+    numel = d.numel
+    want = {oracle.ORDER_DEFAULT: list(range(d.n)),
+            oracle.ORDER_BLOCK: sorted(range(d.n), key=lambda t: (-int(block[t]), t)),
+            oracle.ORDER_SHAPE: sorted(range(d.n), key=lambda t: (-int(numel[t]), t))}
+    plans = {}
+    for policy, order in want.items():
+        S, off = oracle.plan(d, m, g, policy)
+        assert [int(t) for t in np.argsort(off, kind="stable")] == order, policy
+        S2, off2 = oracle.plan(d, m, g, order=order)
+        assert S == S2 and list(off) == list(off2)
+        plans[policy] = (S, list(off))
+    S3, off3 = oracle.plan(d, m, g, oracle.ORDER_BEST3)
+    best = min(S for S, _ in plans.values())
+    first = next(p for p in (oracle.ORDER_DEFAULT, oracle.ORDER_BLOCK, oracle.ORDER_SHAPE)
+                 if plans[p][0] == best)
+    assert (S3, list(off3)) == plans[first]
+
+
 @pytest.mark.parametrize("seed", range(60))
 def test_greedy_over_orders_equals_exhaustive(seed):
     """min over orders of the greedy placement == the true optimum (micro cases)."""

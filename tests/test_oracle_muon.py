@@ -9,14 +9,32 @@ Method: "veScale-FSDP: Flexible and High-Performance FSDP at Scale (MLSys
     iterating and transposing back;
   - band: with bf16 rounding the output's singular values stay in [0.5, 1.5];
   - SelectRoot's greedy: within Graham's (4/3 - 1/(3m)) bound of the optimum
-    found by brute force.
+    found by brute force, and Graham's own worst case for two machines;
+  - momentum and update: the closed form of two Nesterov steps, decoupled
+    weight decay on a non-zero master, the sqrt(R/C) scale of a tall matrix;
+  - FLOPs: numpy's einsum_path count of the three products of an iteration.
 """
+import importlib.util
 import itertools
+import math
+import os
 
 import numpy as np
 import pytest
 
-from oracle import muon
+if os.environ.get("ORACLE_MUON"):  # a planted-mistake copy (tests/test_oracle_mutants.py)
+    _spec = importlib.util.spec_from_file_location("muon_mutant", os.environ["ORACLE_MUON"])
+    muon = importlib.util.module_from_spec(_spec)
+    _spec.loader.exec_module(muon)
+else:
+    from oracle import muon
+
+HP = dict(lr=0.02, momentum=0.95, weight_decay=0.01, eps=1e-7, ns_steps=5,
+          ns_a=3.4445, ns_b=-4.7750, ns_c=2.0315)
+
+
+def _grad(rng, shape):
+    return muon.bf16_from_f32((rng.standard_normal(shape) * 1e-3).astype(np.float32))
 
 
 @pytest.mark.parametrize("shape", [(48, 80), (80, 48), (64, 64)])
@@ -53,8 +71,15 @@ def test_scalar_quintic_fixed_band():
 
 
 def test_bf16_rounding_matches_torch():
+    """Random values, and exact ties (low 16 bits 0x8000) with an even and an
+    odd bf16 neighbour below, of both signs: round half to even."""
     torch = pytest.importorskip("torch")
     x = (np.random.default_rng(4).standard_normal(10000) * 3).astype(np.float32)
+    hi = np.random.default_rng(5).integers(0x0080, 0x7F00, 2000, dtype=np.uint32)
+    ties = ((hi << 16) | 0x8000).astype(np.uint32)
+    ties = np.concatenate([ties, ties | 0x80000000]).view(np.float32)
+    assert (hi & 1).min() == 0 and (hi & 1).max() == 1
+    x = np.concatenate([x, ties])
     want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
     assert np.array_equal(muon.bf16_from_f32(x), want)
 
@@ -82,3 +107,89 @@ def test_muon_step_one_matrix_shapes_and_decay():
     assert np.allclose(p, -np.float32(0.02) * O)  # zero master: the update alone
     s = np.linalg.svd(O.astype(np.float64), compute_uv=False)
     assert 0.5 <= s.min() and s.max() <= 1.5
+
+
+def test_two_nesterov_steps_closed_form():
+    """M1 = g1, M2 = mu g1 + g2, so U2 = g2 + mu M2 = (1 + mu) g2 + mu^2 g1.
+    Step 2's exact-iteration output must be NS(U2 / ||U2||) up to the bf16
+    rounding of X0 (2^-9 relative): 0.002 here, against 0.4 with the
+    Nesterov term dropped."""
+    rng = np.random.default_rng(7)
+    g1, g2 = _grad(rng, (32, 64)), _grad(rng, (32, 64))
+    z = np.zeros_like(g1)
+    M1, p1, _, _ = muon.muon_matrix(g1, z, z, HP)
+    M2, _, _, O2 = muon.muon_matrix(g2, M1, p1, HP, exact=True)
+    mu = HP["momentum"]
+    assert np.abs(M2 - (mu * g1.astype(np.float64) + g2)).max() < 1e-9
+    U = (1 + mu) * g2.astype(np.float64) + mu * mu * g1.astype(np.float64)
+    ref = muon.newton_schulz(U / np.linalg.norm(U), exact=True)
+    assert np.linalg.norm(O2 - ref) / np.linalg.norm(ref) < 0.02
+
+
+@pytest.mark.parametrize("shape", [(64, 32), (32, 64)])
+def test_decay_and_shape_scale(shape):
+    """Decoupled weight decay on a master of order 1, and the update scaled by
+    sqrt(max(1, R/C)): sqrt(2) for the tall matrix, 1 for the wide one. The
+    fp32 roundings are far below both effects (lr wd = 2e-4, (sqrt 2 - 1) lr)."""
+    rng = np.random.default_rng(8)
+    g = _grad(rng, shape)
+    p0 = rng.uniform(0.5, 1.5, shape).astype(np.float32)
+    _, p1, _, O = muon.muon_matrix(g, np.zeros_like(g), p0, HP)
+    R, C = shape
+    want = (p0.astype(np.float64) * (1 - HP["lr"] * HP["weight_decay"])
+            - HP["lr"] * math.sqrt(max(1.0, R / C)) * O.astype(np.float64))
+    assert np.abs(p1 - want).max() < 1e-6
+
+
+def test_select_roots_graham_worst_case():
+    """Graham's worst case of longest-processing-time for two machines: loads
+    3, 3, 2, 2, 2 (given here out of order) end at 7 and 5 against an optimum
+    of 6. Ties go to the lower rank."""
+    root, total = muon.select_roots([2.0, 3.0, 2.0, 3.0, 2.0], 2)
+    assert total == [7.0, 5.0]
+    assert root == [0, 0, 1, 1, 0]
+
+
+class _CountingProducts:
+    """Matrix products by explicit loops, counting one multiply and one add
+    per term."""
+
+    def __init__(self):
+        self.flops = 0
+
+    def mm(self, a, b):
+        p, q = a.shape
+        r = b.shape[1]
+        out = np.zeros((p, r))
+        for i in range(p):
+            for j in range(r):
+                acc = 0.0
+                for l in range(q):
+                    acc += a[i, l] * b[l, j]
+                    self.flops += 2
+                out[i, j] = acc
+        return out
+
+
+@pytest.mark.parametrize("shape", [(3, 5), (5, 3), (4, 4), (2, 3, 5)])
+def test_ns_flops_counts_the_products_of_one_iteration(shape):
+    """One exact quintic iteration run with counted loop products (the
+    Gram matrix of the smaller side, A A, then B X or X B) must give the
+    oracle's one-iteration result, and its count must equal ns_flops."""
+    *lead, R, C = shape
+    a, b, c = muon.NS_COEFFS
+    rng = np.random.default_rng(9)
+    cp = _CountingProducts()
+    for _ in range(math.prod(lead)):
+        x = rng.standard_normal((R, C))
+        x /= np.linalg.norm(x)
+        if R > C:
+            A = cp.mm(x.T, x)
+            B = c * cp.mm(A, A) + b * A
+            y = a * x + cp.mm(x, B)
+        else:
+            A = cp.mm(x, x.T)
+            B = c * cp.mm(A, A) + b * A
+            y = a * x + cp.mm(B, x)
+        assert np.abs(y - muon.newton_schulz(x, steps=1, exact=True)).max() < 1e-12
+    assert muon.ns_flops(shape) == cp.flops
