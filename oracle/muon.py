@@ -24,8 +24,12 @@ algorithm, Keller Jordan, 2024):
 SelectRoot: longest-processing-time greedy over the Newton-Schulz FLOPs
 (ties to the lower rank).
 Parity status: the Newton-Schulz map is pinned to the SVD identity and to
-the transpose identity in exact arithmetic; the bf16 rounding points are a
-reading, pinned only by the output's singular-value band.
+the transpose identity in exact arithmetic; the momentum and update to the
+closed form of two Nesterov steps, decoupled decay on a non-zero master and
+the sqrt(R/C) scale of a tall matrix; the FLOP count to an iteration run with
+counted products; SelectRoot to Graham's bound and his two-machine worst
+case. The bf16 rounding points are a reading, pinned only by the output's
+singular-value band.
 """
 from __future__ import annotations
 
