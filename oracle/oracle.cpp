@@ -30,9 +30,12 @@
 // the fp32 op order written out in adam_element().
 //
 // Parity status: layout, copy-in/out, grad norm and the fp32-state AdamW are
-// pinned by the tests (invariants, brute force, closed forms, torch's AdamW).
-// The 8-bit requantisation is pinned only through its own properties and the
-// first-step closed form, because the pages print no quantised values.
+// pinned by the tests (invariants, brute force, closed forms, torch's AdamW),
+// the tensor orders through the offsets they produce. The 8-bit
+// requantisation is pinned only through its own properties and the
+// first-step closed form, because the pages print no quantised values. A
+// mutation test plants one mistake at a time into a copy of this file, and
+// every one of them must fail a pin.
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off (no FMA contraction: every fp32
 // operation below rounds once, in the order written).
