@@ -26,7 +26,7 @@ def test_algorithmic_bytes_per_element(grad_bytes, zero_copy, per_elem):
     b = bench.algorithmic_bytes(N, Q, grad_bytes=grad_bytes, zero_copy=zero_copy)
     assert b["step"] == per_elem * N + 16 * Q
     assert b["step"] == b["pack"] + b["adam"] + b["unpack"]
-    assert b["adam"] == (grad_bytes + 16) * N + 16 * Q
+    assert b["adam"] == (grad_bytes + 14) * N + 16 * Q
 
 
 @pytest.mark.parametrize("n,frac", [(512, 1.0), (1000, 1.0), (1024, 0.75), (2048, 0.75),
