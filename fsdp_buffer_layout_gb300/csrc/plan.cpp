@@ -316,6 +316,10 @@ static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
 // height the shorter box does not divide), never enlarge one; if it moves
 // any, the wide tables are rebuilt and kept.
 vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1) {
+  if (plan->forced_warps != 0) {
+    plan->tma_warps = plan->forced_warps;
+    return build_tables_for(plan, r0, r1);
+  }
   plan->tma_warps = kTmaWideWarps;
   vsf_status st = build_tables_for(plan, r0, r1);
   if (st != VSF_OK || plan->max_tma_elems == 0 || plan->max_tma_elems > kTmaNarrowMaxUnit)
@@ -429,6 +433,15 @@ vsf_status vsf_plan_restrict(vsf_plan* plan, int32_t rank_begin, int32_t rank_en
   if (rank_begin < 0 || rank_end > plan->m || rank_begin >= rank_end)
     return fail(VSF_ERR_ARG, "vsf_plan_restrict: need 0 <= rank_begin < rank_end <= m");
   return vsf::build_tables(plan, rank_begin, rank_end);
+}
+
+vsf_status vsf_plan_set_bulk_warps(vsf_plan* plan, int32_t warps) {
+  if (plan == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_set_bulk_warps: NULL plan");
+  if (plan->uploaded) return fail(VSF_ERR_STATE, "vsf_plan_set_bulk_warps: plan already uploaded");
+  if (warps != 0 && warps != vsf::kTmaWideWarps && warps != vsf::kTmaNarrowWarps)
+    return fail(VSF_ERR_ARG, "vsf_plan_set_bulk_warps: warps must be 0, 4 or 16");
+  plan->forced_warps = warps;
+  return vsf::build_tables(plan, plan->rank_begin, plan->rank_end);
 }
 
 void vsf_plan_destroy(vsf_plan* plan) { delete plan; }

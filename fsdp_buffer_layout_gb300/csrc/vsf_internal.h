@@ -112,6 +112,7 @@ struct vsf_plan {
   int64_t max_big_elems = 0;
   int64_t max_tma_elems = 0;
   int tma_warps = vsf::kTmaWideWarps;  // shape of the bulk-copy kernel (consumer warps)
+  int forced_warps = 0;                // vsf_plan_set_bulk_warps: 0 = the planner's choice
   vsf::DeviceLayout layout;
 
   // Set by vsf_plan_upload.

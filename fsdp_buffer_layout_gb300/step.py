@@ -37,7 +37,7 @@ class ShardStep:
                  grad_dtype: int = V.VSF_BF16, quantized: bool = True, lr=1e-3, beta1=0.9,
                  beta2=0.999, eps=1e-8, weight_decay=0.01, max_norm=float("inf"),
                  world: int | None = None, device=None, stream: torch.cuda.Stream | None = None,
-                 ranks: tuple[int, int] | None = None):
+                 ranks: tuple[int, int] | None = None, bulk_warps: int = 0):
         self.specs = list(specs)
         self.m, self.g_coll = m, g_coll
         self.grad_dtype = grad_dtype
@@ -46,6 +46,8 @@ class ShardStep:
         self.plan = V.vsf_plan_create(descs, m, g_coll, order)
         if ranks is not None:  # this process owns virtual ranks [r0, r1) only
             V.vsf_plan_restrict(self.plan, int(ranks[0]), int(ranks[1]))
+        if bulk_warps:  # force a bulk-copy AdamW kernel shape (4 or 16); results are the same
+            V.vsf_plan_set_bulk_warps(self.plan, int(bulk_warps))
         self.info = V.vsf_plan_get_info(self.plan)
         self.offsets = V.vsf_plan_offsets(self.plan, len(self.specs))
         self.numels = [int(torch.Size(s.shape).numel()) for s in self.specs]

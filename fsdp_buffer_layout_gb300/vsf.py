@@ -101,6 +101,8 @@ def lib():
             L.vsf_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
             L.vsf_plan_restrict.restype = st
             L.vsf_plan_restrict.argtypes = [vp, i32, i32]
+            L.vsf_plan_set_bulk_warps.restype = st
+            L.vsf_plan_set_bulk_warps.argtypes = [vp, i32]
             L.vsf_group_sumsq.restype = st
             L.vsf_group_sumsq.argtypes = [vp, vp, i32, vp, vp]
             L.vsf_group_scale_from_sumsq.restype = st
@@ -185,6 +187,10 @@ def vsf_selftest_wait_timeout(d_err: int, limit_ns: int, stream: int) -> None:
 
 def vsf_plan_restrict(plan: int, rank_begin: int, rank_end: int) -> None:
     _check(lib().vsf_plan_restrict(plan, rank_begin, rank_end))
+
+
+def vsf_plan_set_bulk_warps(plan: int, warps: int) -> None:
+    _check(lib().vsf_plan_set_bulk_warps(plan, warps))
 
 
 def vsf_group_sumsq(plan: int, packed_grad, dtype: int, d_sumsq: int, stream: int) -> None:

@@ -144,6 +144,18 @@ void vsf_plan_destroy(vsf_plan* plan);
  * 0 <= rank_begin < rank_end <= m), VSF_ERR_STATE (already uploaded). */
 vsf_status vsf_plan_restrict(vsf_plan* plan, int32_t rank_begin, int32_t rank_end);
 
+/* Shape of the bulk-copy AdamW kernel (vsf_plan_info.bulk_warps). warps = 16
+ * (wide: one CTA per SM) or 4 (narrow: four CTAs per SM) forces that shape;
+ * 0 restores the planner's choice (narrow when every bulk-copy unit has at
+ * most 49152 elements and the narrow copy boxes keep every unit). Results are
+ * identical in either shape; only speed differs. A forced narrow shape may
+ * send tile units whose stripe height its 8-row copy box does not divide to
+ * the register kernel. Rebuilds the tables for the plan's rank window and
+ * stays in force across vsf_plan_restrict. Host only.
+ * Errors: VSF_ERR_ARG (NULL plan, warps not 0, 4 or 16), VSF_ERR_STATE
+ * (already uploaded). */
+vsf_status vsf_plan_set_bulk_warps(vsf_plan* plan, int32_t warps);
+
 vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info);
 
 /* Per-tensor element offsets into the m*S buffer; offsets has n entries. */

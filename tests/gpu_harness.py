@@ -37,6 +37,7 @@ class Case:
     grad_dtype: int = 0  # 0 bf16, 1 fp32
     world: int | None = None
     standalone_norm: bool = False
+    bulk_warps: int = 0  # forced bulk-copy kernel shape (0: the planner's choice)
 
     @property
     def numels(self):
@@ -93,7 +94,8 @@ def run_gpu(case: Case):
     from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
     specs = [TensorSpec(tuple(s[0]), s[1], s[2], s[3]) for s in case.specs]
     ss = ShardStep(specs, case.m, case.g_coll, grad_dtype=case.grad_dtype,
-                   quantized=case.quantized, max_norm=case.max_norm, world=case.world)
+                   quantized=case.quantized, max_norm=case.max_norm, world=case.world,
+                   bulk_warps=case.bulk_warps)
     try:
         dev = ss.device
         for t in range(len(specs)):

@@ -89,3 +89,57 @@ def test_tile_stripes_keep_their_bulk_copies(block_rows, want):
     assert info.n_bulk_units == 4 * 1024 // 256
     assert info.n_register_blocks == 0
     assert info.bulk_warps == want
+
+
+def _plan(specs, m=4, g_coll=128):
+    return V.vsf_plan_create([V.make_desc(*s) for s in specs], m, g_coll)
+
+
+def test_forced_shape_and_back():
+    specs = [((256, 512), W.GRAN_TILE, 128, 128), ((96, 11008), W.GRAN_ROWS, 32, 0)]
+    p = _plan(specs)
+    try:
+        auto = V.vsf_plan_get_info(p)
+        blocks = V.vsf_plan_qblocks(p, auto.n_qblocks)
+        assert auto.bulk_warps == 16
+        for warps, want in ((4, 4), (16, 16), (0, 16)):
+            V.vsf_plan_set_bulk_warps(p, warps)
+            info = V.vsf_plan_get_info(p)
+            assert info.bulk_warps == want
+            # the blocks and their routing are the same: only the kernel shape moves
+            assert (info.n_bulk_units, info.n_register_blocks) == \
+                (auto.n_bulk_units, auto.n_register_blocks)
+            got = V.vsf_plan_qblocks(p, info.n_qblocks)
+            assert got == blocks
+    finally:
+        V.vsf_plan_destroy(p)
+
+
+def test_forced_narrow_moves_undivided_stripes_to_the_register_kernel():
+    specs = [((48, 1024), W.GRAN_TILE, 12, 128)]  # 12-row stripes: the 8-row box does not divide
+    p = _plan(specs, m=1)
+    try:
+        wide = V.vsf_plan_get_info(p)
+        V.vsf_plan_set_bulk_warps(p, 4)
+        narrow = V.vsf_plan_get_info(p)
+        assert wide.bulk_warps == 16 and wide.n_bulk_units == 16 and wide.n_register_blocks == 0
+        assert narrow.bulk_warps == 4 and narrow.n_bulk_units == 0
+        assert narrow.n_register_blocks == 4 * 8  # every 12x128 tile, one block each
+    finally:
+        V.vsf_plan_destroy(p)
+
+
+def test_forced_shape_survives_restrict_and_rejects_other_values():
+    specs = [((64, 11008), W.GRAN_ROWS, 32, 0), ((256, 1024), W.GRAN_ROWS, 32, 0)]
+    p = _plan(specs)
+    try:
+        V.vsf_plan_set_bulk_warps(p, 4)
+        V.vsf_plan_restrict(p, 0, 1)
+        assert V.vsf_plan_get_info(p).bulk_warps == 4
+        for bad in (1, 8, 15, -4):
+            with pytest.raises(V.VsfError) as e:
+                V.vsf_plan_set_bulk_warps(p, bad)
+            assert e.value.status == V.VSF_ERR_ARG
+        assert V.vsf_plan_get_info(p).bulk_warps == 4
+    finally:
+        V.vsf_plan_destroy(p)

@@ -163,6 +163,18 @@ def test_tiles_on_every_path(warps):
     compare(case, run_gpu(case), run_oracle(case))
 
 
+@pytest.mark.parametrize("warps", [4, 16])
+def test_forced_kernel_shapes_match_the_oracle(warps):
+    """One plan in each forced bulk-copy shape (vsf_plan_set_bulk_warps): the
+    ragged set (the planner's narrow choice) plus 352K-element row blocks (its
+    wide choice). Both shapes must be bit-exact against the oracle, hence
+    equal to each other."""
+    specs = RAGGED + [((64, 11008), W.GRAN_ROWS, 32, 0)]
+    case = _normal_case(specs, m=5, g=128, steps=2, bulk_warps=warps)
+    assert _bulk_warps(case) == 16  # the planner's own choice for this set
+    compare(case, run_gpu(case), run_oracle(case))
+
+
 def test_heavy_tails_student_t():
     w = W.dsv3_block()
     specs = [((512, 1024), W.GRAN_TILE, 128, 128), ((7168,), W.GRAN_ELEM, 0, 0)]
