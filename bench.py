@@ -251,7 +251,8 @@ def gpu_arm(args, rank: int, world: int):
     w = W.get(args.workload)
     specs = [TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
     stream = torch.cuda.Stream(dev)
-    ss = ShardStep(specs, w.m, w.g_coll, max_norm=w.max_norm, stream=stream)
+    ss = ShardStep(specs, w.m, w.g_coll, max_norm=w.max_norm, stream=stream,
+                   bulk_warps=args.bulk_warps)
     n_real, nq = ss.info.real, ss.info.n_qblocks
     nbytes = algorithmic_bytes(n_real, nq, zero_copy=args.zero_copy)
 
@@ -437,10 +438,13 @@ def gpu_arm(args, rank: int, world: int):
                                  "unpack": round(k_unpack, 5)},
                    "frac_of_peak_step": round(value / world / peak, 4),
                    "frac_of_nominal_8tbs_step": round(value / world / NOMINAL_HBM_GBS, 4),
-                   "plan_seconds": round(ss.info.plan_seconds, 6)},
+                   "plan_seconds": round(ss.info.plan_seconds, 6),
+                   "bulk_warps": ss.info.bulk_warps},
         "roofline": {"bound": "hbm", "achieved": round(adam_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(adam_gbs / peak, 4),
-                     "traffic": TRAFFIC.get(w.name), "traffic_unit": "bytes per launch",
+                     # captured with the planner's own kernel shape
+                     "traffic": None if args.bulk_warps else TRAFFIC.get(w.name),
+                     "traffic_unit": "bytes per launch",
                      "kernel": "vsf_adam8_step",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
@@ -907,6 +911,8 @@ def main():
                     help="time the fused DBuffer group ops (zero, scale, add) instead")
     ap.add_argument("--zero-copy", action="store_true",
                     help="gradients/params as views of the packed buffers (no pack/unpack)")
+    ap.add_argument("--bulk-warps", type=int, default=0, choices=[0, 4, 16],
+                    help="force the bulk-copy AdamW kernel shape (0: the planner's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
