@@ -45,7 +45,8 @@ def bf16_from_f32(x: np.ndarray) -> np.ndarray:
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
     nan = (u & 0x7FFFFFFF) > 0x7F800000
     r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
-    r = np.where(nan, np.uint64(0x7FFF0000), r).astype(np.uint32)
+    # a NaN stays a NaN (the quiet NaN 0x7fc0; its bits are not compared)
+    r = np.where(nan, np.uint64(0x7FC00000), r).astype(np.uint32)
     return r.view(np.float32)
 
 

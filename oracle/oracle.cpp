@@ -238,9 +238,10 @@ inline void adam_element(const AdamConsts& k, float factor, float g_in, float& m
 inline uint16_t bf16_round(float f) {
   uint32_t u;
   std::memcpy(&u, &f, 4);
-  // reading: NaN -> 0x7fff, the canonical NaN of the sm_100-family hardware
-  // bf16 conversion (torch's CPU conversion gives 0x7fc0 instead).
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fff;
+  // reading: IEEE 754 fixes only that a NaN converts to a NaN, not which
+  // one; this oracle returns the quiet NaN 0x7fc0, and parity compares bf16
+  // NaNs by class (any NaN matches any NaN).
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;
   u += 0x7fffu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
@@ -255,14 +256,16 @@ inline float bf16_value(uint16_t h) {
 // reading (quantiser): symmetric int8 for m with scale = max |m| of the
 // block, unsigned uint8 for v with scale = max v of the block. Dequantised
 // value = code * (scale / 127) (resp. / 255). Code = round-half-even of
-// x * (127 / scale) (resp. 255 / scale), saturated to the code type's range,
-// NaN giving 0; a zero scale means all codes 0. For a finite block scale
-// whose reciprocal is finite, |x * (127 / scale)| stays below 127.5, so m
-// codes lie in [-127, 127].
+// x * (127 / scale) (resp. 255 / scale), saturated to [-127, 127] (resp.
+// [0, 255]), NaN giving 0; a zero scale means all codes 0. The m quantiser is
+// symmetric: codes are clamped to [-127, 127], never -128, so no code
+// dequantises above the block's absmax. The clamp matters when the scale is
+// so small (subnormal) that 127 / scale overflows to infinity: every nonzero
+// element then saturates, to +127 or -127 alike.
 inline int8_t quant_m(float x, float inv) {
   const float y = x * inv;
   if (std::isnan(y)) return 0;
-  return (int8_t)(int)std::nearbyint(std::fmin(std::fmax(y, -128.0f), 127.0f));
+  return (int8_t)(int)std::nearbyint(std::fmin(std::fmax(y, -127.0f), 127.0f));
 }
 inline uint8_t quant_v(float x, float inv) {
   const float y = x * inv;

@@ -42,6 +42,10 @@ MUTANTS = [
     ("clip epsilon dropped", "double r = max_norm / (norm + 1e-6);", "double r = max_norm / norm;"),
     ("square dropped from the sum", "acc += x * x;", "acc += std::fabs(x);"),
     ("bf16 ties away from zero", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    ("m codes clamped to -128", "std::fmin(std::fmax(y, -127.0f), 127.0f)",
+     "std::fmin(std::fmax(y, -128.0f), 127.0f)"),
+    ("bf16 NaN turned into infinity", "if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;",
+     "if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7f80;"),
     ("rank boundaries may cut atoms", "if ((k * S - o) % x.block != 0) {",
      "if (false && (k * S - o) % x.block != 0) {"),
     ("first rank boundary not checked", "for (int64_t k = o / S + 1; k * S < o + x.numel; ++k) {",

@@ -102,7 +102,17 @@ def test_bf16_round_matches_torch():
     want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = np.array([oracle.bf16_round(float(v)) for v in x], np.uint16)
     assert np.array_equal(got, want)
-    assert oracle.bf16_round(float("nan")) == 0x7FFF
+
+
+def test_bf16_round_nan_is_nan():
+    """IEEE 754 makes a converted NaN a NaN, whatever its bits (torch's own
+    scalar and vectorised conversions disagree on them), so only the class is
+    pinned: exponent all ones and a nonzero fraction, for quiet, signalling
+    and negative NaNs alike."""
+    for bits in (0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF812345, 0x7FFFFFFF):
+        f = float(np.array([bits], np.uint32).view(np.float32)[0])
+        h = oracle.bf16_round(f)
+        assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0, hex(h)
 
 
 # ---------------------------------------------------------------- AdamW, fp32 state
@@ -184,6 +194,28 @@ def test_quantizer_properties():
         assert np.all(np.abs(dv.astype(np.float64) - v) <= sv / 510 * (1 + 1e-5))
         cv2, _, _ = oracle.quantize_v(dv)
         assert np.array_equal(cv2, cv)
+
+
+def test_quantizer_tiny_scale_stays_symmetric():
+    """A block scale below 127 / FLT_MAX (about 3.7e-37) makes 127 / scale
+    overflow to infinity: every nonzero element then saturates. The m codes
+    must stay in the symmetric range, +-127 (a clamp at -128 would give
+    negative elements code -128, which dequantises above the absmax), zeros
+    stay 0, and no dequantised value exceeds the scale."""
+    s = np.float32(127.0 * 2.0 ** -130)          # normal, and 127 / s = 2^130 > FLT_MAX
+    with np.errstate(over="ignore"):
+        assert np.float32(127.0) / s == np.inf
+    x = np.array([s, -s, -s / 2, s / 3, 0.0, -2.0 ** -149, 2.0 ** -140], np.float32)
+    c, scale, dq = oracle.quantize_m(x)
+    assert scale == s
+    assert list(c) == [127, -127, -127, 127, 0, -127, 127]
+    assert np.all(np.abs(dq) <= s)
+    assert np.abs(dq).max() == s                   # 127 * (s / 127) is exact here
+    # the same through the v quantiser: 255 / scale overflows, all saturate to 255
+    v = np.abs(x)
+    cv, sv, dv = oracle.quantize_v(v)
+    assert list(cv) == [255, 255, 255, 255, 0, 255, 255] and sv == s
+    assert np.all(dv <= np.float32(255.0) * (s / np.float32(255.0)))
 
 
 def test_quantizer_zero_block_and_ties():
