@@ -16,8 +16,9 @@
 //        of section 2 of Kingma & Ba's Adam paper)
 //   bf16 copy = round-to-nearest-even(p)
 //   new m_scale = max |m|, new v_scale = max v over the block;
-//   codes = round-half-even(m * (127 / m_scale)) saturated to int8 and
-//           round-half-even(v * (255 / v_scale)) saturated to uint8, NaN -> 0.
+//   codes = round-half-even(m * (127 / m_scale)) saturated to [-127, 127]
+//           and round-half-even(v * (255 / v_scale)) saturated to [0, 255],
+//           NaN -> 0.
 // Every fp32 operation is an explicit round-to-nearest operation, scalar
 // (__fmul_rn, __fadd_rn, __fdiv_rn, __fsqrt_rn) or a packed multiply
 // (mul.rn.f32x2 in inline PTX, which rounds each component like the scalar
@@ -120,9 +121,15 @@ __device__ __forceinline__ float2 s8pair_to_f2(uint32_t word_xor80, int first) {
   return __fadd2_rn(x, f2(-8388736.0f));  // 2^23 + 128
 }
 
+// m code: round-half-even, saturated to the symmetric range [-127, 127]
+// (never -128). The lower clamp comes first and keeps a NaN a NaN
+// (max.NaN), which the conversion then turns into 0. It matters when a
+// block's scale is so small that 127 / scale overflows to infinity.
 __device__ __forceinline__ uint32_t cvt_sat_s8(float x) {
+  float y;
+  asm("max.NaN.f32 %0, %1, 0fC2FE0000;" : "=f"(y) : "f"(x));  // max(x, -127)
   uint32_t r;
-  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(x));
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(y));
   return r & 0xffu;
 }
 __device__ __forceinline__ uint32_t cvt_sat_u8(float x) {

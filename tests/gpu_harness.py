@@ -241,12 +241,24 @@ def check_codes(got, want, name):
     return int((diff == 0).sum())
 
 
-def bit_equal(a: np.ndarray, b: np.ndarray) -> bool:
-    """Byte equality, except that two fp32 NaNs match whatever their payload
-    (a CPU and a GPU pick different NaN bit patterns)."""
+def bf16_nan(h: np.ndarray) -> np.ndarray:
+    """Which bf16 bit patterns are NaNs (exponent all ones, fraction nonzero)."""
+    h = h.view(np.uint16)
+    return ((h & 0x7F80) == 0x7F80) & ((h & 0x007F) != 0)
+
+
+def bit_equal(a: np.ndarray, b: np.ndarray, bf16: bool = False) -> bool:
+    """Byte equality, except that two NaNs match whatever their bits: fp32
+    arrays, and uint16 arrays of bf16 values when bf16=True. IEEE 754 fixes
+    only that a rounded NaN is a NaN; the CPU and the GPU pick different
+    bit patterns."""
     if a.dtype == np.float32:
         same = a.view(np.uint32) == b.view(np.uint32)
         same |= np.isnan(a) & np.isnan(b)
+        return bool(same.all())
+    if bf16:
+        same = a.view(np.uint16) == b.view(np.uint16)
+        same |= bf16_nan(a) & bf16_nan(b)
         return bool(same.all())
     return np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
@@ -274,6 +286,10 @@ def compare(case: Case, g: dict, o: dict, exact: bool = True):
         check_master(g["v_state"], o["v_state"])
     if exact:
         for k in ("master", "m_state", "v_state", "m_scale", "v_scale", "packed_bf16"):
-            assert bit_equal(g[k], o[k]), f"{k} not bit-exact"
+            assert bit_equal(g[k], o[k], bf16=k == "packed_bf16"), f"{k} not bit-exact"
+    # copy-out is a byte copy of the library's own bf16 buffer ...
+    for a, b in zip(g["params"], oracle.unpack(g["packed_bf16"], case.numels, g["offsets"])):
+        assert np.array_equal(a, b), "copy-out differs from the packed bf16 buffer"
+    # ... whose values match the oracle's (NaNs by class)
     for a, b in zip(g["params"], o["params"]):
-        assert np.array_equal(a, b), "copy-out differs"
+        assert bit_equal(a, b, bf16=True), "copy-out differs"

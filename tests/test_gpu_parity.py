@@ -245,7 +245,7 @@ def test_padding_is_never_written():
 def test_special_values_match_oracle():
     """NaN, +-inf, values that overflow bf16, fp32 and bf16 denormals, bf16
     rounding ties and -0 in masters and gradients: same bits as the oracle
-    (NaN payloads aside), including bf16 NaN = 0x7fff and NaN codes = 0."""
+    (NaN bits aside: any NaN matches any NaN), and NaN codes = 0."""
     specs = [((64, 64), W.GRAN_ROWS, 16, 0), ((256,), W.GRAN_ELEM, 0, 0)]
     case = _normal_case(specs, m=2, g=128, steps=2)
     base_g, base_m = case.grads, case.masters
@@ -276,3 +276,30 @@ def test_special_values_match_oracle():
 
     case.masters, case.grads = masters, grads
     compare(case, run_gpu(case), run_oracle(case))
+
+
+def test_tiny_block_scale_codes_stay_symmetric():
+    """Blocks whose gradients are all bf16 subnormals of both signs: the new
+    m scale (about 1e-40) is below 127 / FLT_MAX, so 127 / scale overflows
+    and every nonzero moment saturates. The m codes must be +-127, never
+    -128, in the bulk-copy kernel (row blocks), the register kernel
+    (128-column tiles) and the element-chunk kernel alike."""
+    specs = [((64, 64), W.GRAN_ROWS, 16, 0), ((256,), W.GRAN_ELEM, 0, 0),
+             ((64, 256), W.GRAN_TILE, 16, 128)]
+    case = _normal_case(specs, m=2, g=128, steps=3)
+    base_g = case.grads
+
+    def grads(s, t):
+        x = base_g(s, t).copy()
+        rng = np.random.default_rng((5, s, t))  # the same values on every call
+        lo, hi = {0: (1024, 2048), 1: (128, 256), 2: (16 * 256, 32 * 256)}[t]
+        mag = rng.integers(1, 0x80, hi - lo).astype(np.uint16)        # bf16 subnormals
+        sign = (rng.integers(0, 2, hi - lo).astype(np.uint16) << 15)
+        x[lo:hi] = mag | sign
+        return x
+
+    case.grads = grads
+    o = run_oracle(case)
+    assert not np.any(o["m_state"] == -128)
+    assert np.count_nonzero(o["m_state"] == -127) > 500
+    compare(case, run_gpu(case), o)
