@@ -20,10 +20,19 @@
 // (release at cluster scope); consumers wait on their own barrier (acquire).
 // Slots and barriers alternate between two sets by block parity.
 //
-// Every wait is bounded: after 2 s it sets bit 1 of the device
-// error word and carries on as if the wait had succeeded (the results are
-// then wrong but every CTA still finishes, so no thread hangs and no CTA
-// leaves while a copy or a peer's write into it is still pending).
+// Every wait is bounded, and a timeout is sticky. The first wait of a CTA
+// that runs out (2 s) sets bit 1 of the device error word and the CTA's
+// shared "stop" flag; from then on every wait of that CTA returns at once.
+// The producer issues no further copy. A consumer warp releases a ring slot
+// (arrives on its "empty" barrier) only after its wait for that slot's data
+// succeeded, so the producer never refills a slot whose copy may still be in
+// flight. Consumers still pass every barrier among themselves and still send
+// their block maxima to the peers (which therefore never wait for them), but
+// skip the arithmetic and the stores of every chunk whose data they did not
+// get. Before exit the producer waits, under one more 2 s limit in all, for
+// every copy it issued, so no CTA leaves while a copy into it is pending.
+// The results of a launch that set the error bit are undefined; the kernel
+// finishes within a few limits instead of one limit per wait.
 
 // One shape of the kernel: W consumer warps and one producer warp per CTA,
 // chunks of W * 512 elements, and a ring of 200 KB at 16 warps or
@@ -105,28 +114,47 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) 
   return ok != 0;
 }
 
-// Bounded wait for the phase of the given parity; returns false after
-// limit_ns (kWaitNs unless given) of wall-clock time (global timer), having
-// set bit 1 of the error word.
+// Bounded wait for the phase of the given parity. Returns false at once if
+// the CTA's stop flag is set, or after limit_ns (kWaitNs unless given) of
+// wall-clock time (global timer), having then set the stop flag and bit 1 of
+// the error word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
-                                          uint64_t limit_ns = kWaitNs) {
+                                          volatile uint32_t* stop, uint64_t limit_ns = kWaitNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try(bar, parity)) {
+  while (*stop == 0u) {
+    if (mbar_try(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) {
+      *stop = 1u;
       atomicOr(err, 2u);
       return false;
     }
   }
-  return true;
+  return false;
 }
 
 // The same at cluster scope (acquire), for barriers that peers arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err,
+                                                  volatile uint32_t* stop) {
   if (mbar_try_cluster(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_cluster(bar, parity)) {
+  while (*stop == 0u) {
+    if (mbar_try_cluster(bar, parity)) return true;
     if (global_ns() - t0 > kWaitNs) {
+      *stop = 1u;
+      atomicOr(err, 2u);
+      return false;
+    }
+  }
+  return false;
+}
+
+// Wait for an issued copy to land, ignoring the stop flag, until the global
+// timer passes `deadline`; used once per slot before the CTA exits.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                           unsigned* err) {
+  while (!mbar_try(bar, parity)) {
+    if (global_ns() > deadline) {
       atomicOr(err, 2u);
       return false;
     }
@@ -266,8 +294,11 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
   auto empty_bar = [&](int s) { return s0 + Lay::bars + 8u * (kTmaSlots + s); };
   auto max_bar = [&](int par) { return s0 + Lay::bars + 8u * (2 * kTmaSlots + par); };
   float2* maxima = reinterpret_cast<float2*>(smem + Lay::maxima);
+  __shared__ uint32_t stop_flag;  // set by the first wait of this CTA that runs out
+  volatile uint32_t* stop = &stop_flag;
 
   if (tid == 0) {
+    stop_flag = 0u;
     for (int s = 0; s < kTmaSlots; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), W);
@@ -282,21 +313,22 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
     // ---------------- producer warp: lane 0 waits for the slot, posts the
     // byte count and issues the copies (one 1-D bulk copy per array for a
     // contiguous chunk, one 2-D tensor copy per array for a tile chunk).
-    const uint64_t keep = l2_policy_evict_last();
-    const uint64_t drop = l2_policy_evict_first();
-    uint32_t p = 0;  // position in the ring sequence
-    for (int j = cid; j < nlist; j += nclusters) {
-      const QBlock b = qb[list[j]];
-      const int kt = ktab[j];
-      int c0, c1;
-      tma_share<CH>(b, kt, CL, crank, c0, c1);
-      int mi = 0;
-      if (b.tx >= 0)
-        while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
-      for (int ph = 0; ph < 2; ++ph) {
-        const int step = ph == 0 ? Lay::p1 : 1;
-        for (int c = c0; c < c1; c += step, ++p) {
-          if (lane == 0) {
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t drop = l2_policy_evict_first();
+      uint32_t p = 0;  // ring positions issued so far
+      bool halted = false;
+      for (int j = cid; j < nlist && !halted; j += nclusters) {
+        const QBlock b = qb[list[j]];
+        const int kt = ktab[j];
+        int c0, c1;
+        tma_share<CH>(b, kt, CL, crank, c0, c1);
+        int mi = 0;
+        if (b.tx >= 0)
+          while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
+        for (int ph = 0; ph < 2 && !halted; ++ph) {
+          const int step = ph == 0 ? Lay::p1 : 1;
+          for (int c = c0; c < c1; c += step) {
             const int s = p % kTmaSlots;
             const uint32_t round = p / kTmaSlots;
             // ring chunk = chunks c .. c + n - 1 of the share (n = 2 for a
@@ -306,7 +338,13 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
             const TmaChunk cl = n == 2 ? tma_chunk<CH>(b, kt, c + 1) : ch;
             const uint32_t len0 = (uint32_t)ch.len();
             const uint32_t len = len0 + (n == 2 ? (uint32_t)cl.len() : 0u);
-            if (round > 0) mbar_wait(empty_bar(s), (round - 1) & 1, err);
+            // the slot is free once every consumer warp has used its last
+            // data; after a timeout anywhere in the CTA, stop issuing
+            if ((round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, stop)) || *stop) {
+              halted = true;
+              break;
+            }
+            ++p;
             const uint32_t fb = full_bar(s);
             const int64_t last = cl.gstart + (int64_t)(cl.rows - 1) * cl.stride + cl.row_len;
             if (!in_bounds(k.bd, ch.gstart, last)) {
@@ -338,14 +376,15 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
           }
         }
       }
-    }
-    // Every issued copy has been consumed before the consumers finish; wait
-    // for the last ones anyway so that none is in flight at exit.
-    if (lane == 0) {
+      // Every issued copy has normally been consumed before the consumers
+      // finish; wait for the last one of each slot anyway (one limit for all
+      // slots together, ignoring the stop flag) so that none is in flight at
+      // exit.
+      const uint64_t deadline = global_ns() + kWaitNs;
       for (int s = 0; s < kTmaSlots; ++s) {
         if (p > (uint32_t)s) {
           const uint32_t last = (p - 1 - s) / kTmaSlots * kTmaSlots + s;  // last position in slot s
-          mbar_wait(full_bar(s), (last / kTmaSlots) & 1, err);
+          mbar_drain(full_bar(s), (last / kTmaSlots) & 1, deadline, err);
         }
       }
     }
@@ -384,7 +423,10 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       float mx = 0.0f, vx = 0.0f;
       for (int ci = c0; ci < c1; ci += Lay::p1, ++p) {
         const int s = p % kTmaSlots;
-        mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
+        // warp-uniform: the chunk is used (and its slot released) only if
+        // every lane saw the data arrive
+        const bool got = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err, stop));
+        if (!got) continue;
         int len = tma_chunk<CH>(b, kt, ci).len();
         if (Lay::p1 == 2 && ci + 1 < c1) len += tma_chunk<CH>(b, kt, ci + 1).len();
         const unsigned char* sl = smem + s * Lay::slot;
@@ -437,7 +479,7 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
         }
         if (lane < CL) dsmem_arrive(max_bar(par), lane);
       }
-      mbar_wait_cluster(max_bar(par), (nb >> 1) & 1, err);
+      mbar_wait_cluster(max_bar(par), (nb >> 1) & 1, err, stop);
       float sm = 0.0f, sv = 0.0f;
       for (int rk = 0; rk < CL; ++rk) {
         const float2 v = maxima[(par * kMaxCluster + rk) * kMaxUnitTiles + tt];
@@ -446,7 +488,7 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       }
       c.im = f2(sm > 0.0f ? __fdiv_rn(127.0f, sm) : 0.0f);
       c.iv = f2(sv > 0.0f ? __fdiv_rn(255.0f, sv) : 0.0f);
-      if (crank == 0 && tid < kt * gpt && tid % gpt == 0) {  // one thread per tile
+      if (crank == 0 && tid < kt * gpt && tid % gpt == 0 && *stop == 0u) {  // one thread per tile
         m_scale[q] = sm;
         v_scale[q] = sv;
       }
@@ -454,7 +496,8 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       // phase 2: update, requantise, write
       for (int ci = c0; ci < c1; ++ci, ++p) {
         const int s = p % kTmaSlots;
-        mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err);
+        const bool got = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err, stop));
+        if (!got) continue;
         const TmaChunk ch = tma_chunk<CH>(b, kt, ci);
         const int len = ch.len();
         const unsigned char* sl = smem + s * Lay::slot;
@@ -495,14 +538,23 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// Self-test of the bounded wait: one CTA waits on a barrier that no one
-// arrives on; the wait must give up after limit_ns and set bit 1 of *err.
+// Self-test of the bounded wait: one CTA waits, four times in a row, on
+// barriers that no one arrives on. The first wait must give up after
+// limit_ns and set bit 1 of err[0]; the timeout is sticky, so the other three
+// return at once. err[1] receives the elapsed time of the four waits in
+// microseconds (about one limit, not four).
 __global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar[4];
+  __shared__ uint32_t stop_flag;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar), 1);
+    stop_flag = 0u;
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bar[i]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, err, limit_ns);
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = global_ns();
+    for (int i = 0; i < 4; ++i) mbar_wait(smem_u32(&bar[i]), 0, err, &stop_flag, limit_ns);
+    err[1] = (unsigned)((global_ns() - t0) / 1000u);
+  }
 }

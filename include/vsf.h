@@ -276,6 +276,15 @@ vsf_status vsf_adam8_step(const vsf_plan* plan, const void* packed_grad, int32_t
 vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* const* params,
                       void* stream);
 
+/* Measurement helper: a plain device-to-device copy of `bytes` bytes by a
+ * streaming kernel (128-bit loads and stores, a grid of 4 CTAs of 512
+ * threads per SM, 8 accesses in flight per thread). It sets the copy ceiling
+ * that the shard-step kernels are measured against in the same run. dst and
+ * src are device pointers, 16-byte aligned, not overlapping; bytes a
+ * multiple of 16. Errors: VSF_ERR_ARG (NULL, bytes not a multiple of 16),
+ * VSF_ERR_ALIGN, VSF_ERR_CUDA. */
+vsf_status vsf_device_copy(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Fused group ops ([VSF] 核心方法 › Distributed Buffer: the same
  * element-wise kernel applied to every tensor of the buffer in one launch,
  * e.g. zero_grad and gradient accumulation). They touch every real element
@@ -337,10 +346,14 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
 
 /* Self-test of the kernels' bounded waits (every wait on a barrier gives up
  * after a time limit, sets bit 1 of the device error word and lets the kernel
- * finish, so no thread can hang): launches one CTA that waits on a barrier
- * nobody arrives on, with limit_ns (at most 1 s) instead of the kernels' 2 s.
- * After the stream reaches it, *d_err (a device uint32 the caller zeroed)
- * has bit 1 set. Errors: VSF_ERR_ARG (NULL, limit above 1 s), VSF_ERR_CUDA. */
+ * finish, so no thread can hang; the first timeout in a CTA makes every later
+ * wait of that CTA return at once): launches one CTA that waits four times
+ * in a row on barriers nobody arrives on, with limit_ns (at most 1 s) instead
+ * of the kernels' 2 s. d_err points to two device uint32 words the caller
+ * zeroed. After the stream reaches the kernel, d_err[0] has bit 1 set and
+ * d_err[1] holds the four waits' elapsed time in microseconds: about one
+ * limit, as the timeout is sticky. Errors: VSF_ERR_ARG (NULL, limit above
+ * 1 s), VSF_ERR_CUDA. */
 vsf_status vsf_selftest_wait_timeout(unsigned* d_err, uint64_t limit_ns, void* stream);
 
 /* Group norm and scale WITHOUT any device allocation or workspace. The pages
@@ -362,7 +375,10 @@ vsf_status vsf_selftest_wait_timeout(unsigned* d_err, uint64_t limit_ns, void* s
  * that loads the library keeps it until the process exits. No cudaMalloc,
  * cudaFree or allocating library call is made. The first call on a device
  * looks up the array's device address for that device (with that device
- * current) and caches it; make that first call before any stream capture.
+ * current) and caches it with the current context; make that first call
+ * before any stream capture. After a device reset (a new primary context),
+ * the next call looks the address up again, so it too belongs outside a
+ * capture.
  * Every call on a device shares the array: calls that overlap on the GPU
  * (different streams without ordering) race and give wrong results. Nothing
  * needs to start at zero: each call writes every partial it later reads. */
