@@ -10,9 +10,15 @@ bytes per real element (bf16 gradients): pack 2+2, AdamW 2+1+1+4 read and
 1+1+4+2 written, unpack 2+2, i.e. 24 B, plus 16 B of scales per
 quantisation block. Padding is never touched, so it is not counted.
 
+Default workload: the 24-layer Llama-style 1.3B model (m = 1024 virtual
+ranks), the largest workload that fits one GPU. Every step gets fresh
+gradients (two seeded sets alternate). The line also carries the copy ceiling
+measured in the same run (device-to-device memcpy and a 128-bit copy kernel).
+
 Timing: W untimed steps, then K steps between a barrier and a device
-synchronise, CUDA events on the launch stream; the inputs (4.9 GB per step
-for the Llama layer) are larger than L2, so no flush is needed. Under torchrun
+synchronise, CUDA events on the launch stream; the inputs (32 GB per step for
+the 1.3B model, 4.9 GB for one Llama layer) are larger than L2, so no flush is
+needed. Under torchrun
 (N > 1) every rank runs an independent replica of the workload (the m
 virtual ranks of one buffer live on one GPU); value = sum over ranks.
 """
@@ -240,6 +246,51 @@ def host_link_ms(host_in, dev_in, host_out, dev_out, s_in, s_out, steps: int) ->
     return a.elapsed_time(b) / steps
 
 
+def fill_grads(w, step: int, out: np.ndarray, starts) -> None:
+    """The seeded gradients of `step` for every tensor of w into out (bf16
+    bits), tensor t at starts[t]; tensors are generated in parallel (the
+    generator is C and releases the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
+    from synth import workloads as W
+    jobs = [(t, starts[t], spec.numel) for t, spec in enumerate(w.tensors)]
+    with ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(lambda j: W.grad(w, step, j[0], out=out[j[1]:j[1] + j[2]]), jobs))
+
+
+def copy_ceiling(dev, nbytes: int = 4 << 30, reps: int = 10) -> dict:
+    """The copy ceiling of this GPU, measured in this run: the best of `reps`
+    device-to-device copies of nbytes (counted as read + write) by
+    cudaMemcpyAsync (torch's contiguous copy) and by libvsf's 128-bit copy
+    kernel, and the larger of the two."""
+    import torch
+    from fsdp_buffer_layout_gb300 import vsf as V
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1)
+    st = torch.cuda.current_stream(dev)
+
+    def best(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return 2 * nbytes / (min(ts) * 1e-3) / 1e9
+
+    memcpy = best(lambda: b.copy_(a))
+    kernel = best(lambda: V.vsf_device_copy(b.data_ptr(), a.data_ptr(), nbytes, st.cuda_stream))
+    del a, b
+    torch.cuda.empty_cache()
+    return dict(gbs=round(max(memcpy, kernel), 1), memcpy_d2d_gbs=round(memcpy, 1),
+                copy_kernel_gbs=round(kernel, 1), bytes_per_copy=2 * nbytes, reps=reps,
+                how="best of the reps, CUDA events on the launching stream")
+
+
 def gpu_arm(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -248,7 +299,10 @@ def gpu_arm(args, rank: int, world: int):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    ceiling = copy_ceiling(dev)  # before the workload's buffers take the memory
     w = W.get(args.workload)
+    if args.fraction < 1.0:  # a reduced case of the same tensors (profiling captures)
+        w = sample_workload(w, args.fraction)
     specs = [TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
     stream = torch.cuda.Stream(dev)
     ss = ShardStep(specs, w.m, w.g_coll, max_norm=w.max_norm, stream=stream,
@@ -257,32 +311,39 @@ def gpu_arm(args, rank: int, world: int):
     nbytes = algorithmic_bytes(n_real, nq, zero_copy=args.zero_copy)
 
     # Per-tensor gradients and parameters, 16-byte aligned views of one buffer.
+    # The workload's input stream gives every step fresh gradients: two sets
+    # (the seeded gradients of steps 1 and 2) are generated up front, and the
+    # steps alternate between them, on the device and, for the end-to-end
+    # leg, in pinned host memory.
     starts, cur = [], 0
     for n in ss.numels:
         starts.append(cur)
         cur += (n + 7) // 8 * 8
-    host_g = torch.empty(cur, dtype=torch.int16).pin_memory()
-    hg = host_g.numpy().view(np.uint16)
-    for t, n in enumerate(ss.numels):
-        W.grad(w, 1, t, out=hg[starts[t]:starts[t] + n])
+    host_g2 = [torch.zeros(cur, dtype=torch.int16).pin_memory() for _ in range(2)]
+    for i, h in enumerate(host_g2):
+        fill_grads(w, i + 1, h.numpy().view(np.uint16), starts)
+    for t in range(len(ss.numels)):
         ss.load_master(t, torch.from_numpy(W.master_init(w, t)).to(dev))
-    dev_g = host_g.to(dev)
-    dev_p = torch.empty(cur, dtype=torch.int16, device=dev)
+    dev_g2 = [h.to(dev) for h in host_g2]
+    dev_p2 = [torch.empty(cur, dtype=torch.int16, device=dev) for _ in range(2)]
+    host_g = host_g2[0]
+    dev_g, dev_p = dev_g2[0], dev_p2[0]
     host_p = torch.empty(cur, dtype=torch.int16).pin_memory()
-    host_norm = torch.empty(2, dtype=torch.float64).pin_memory()
-    grads = [dev_g[s:s + n] for s, n in zip(starts, ss.numels)]
-    params = [dev_p[s:s + n] for s, n in zip(starts, ss.numels)]
+    grads2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_g2]
+    params2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_p2]
+    params = params2[0]
     gviews = pviews = None
     if args.zero_copy:
-        # gradients and parameters live in the packed buffers (address map);
-        # the end-to-end leg double-buffers them (a second gradient and bf16
-        # buffer with their own views)
+        # gradients and parameters live in the packed buffers (address map):
+        # two gradient buffers hold the two gradient sets, and the steps (and
+        # the end-to-end leg's double buffering) alternate between them
         zc_grad = [ss.packed_grad, torch.zeros_like(ss.packed_grad)]
         zc_bf = [ss.packed_bf16, torch.zeros_like(ss.packed_bf16)]
         gviews = [ss.views(b.view(torch.int16)) for b in zc_grad]
         pviews = [ss.views(b.view(torch.int16)) for b in zc_bf]
-        for v, g in zip(gviews[0], grads):
-            v.copy_(g)
+        for i in range(2):
+            for v, g in zip(gviews[i], grads2[i]):
+                v.copy_(g)
 
     def gviews_of(buf):
         return gviews[buf]
@@ -295,16 +356,20 @@ def gpu_arm(args, rank: int, world: int):
     def one_step(ev=None):
         nonlocal step
         step += 1
+        gset = step % 2  # fresh gradients: the two sets alternate
         if ev is not None:
             ev[0].record(stream)
         if args.zero_copy:
-            ss.group_norm_scale(standalone=True)
+            ss.zero_copy_norm(zc_grad[gset])
         else:
-            ss.pack(grads)
+            ss.pack(grads2[gset])
             ss.group_norm_scale()
         if ev is not None:
             ev[1].record(stream)
-        ss.adam(step)
+        if args.zero_copy:
+            ss.zero_copy_adam(step, zc_grad[gset])
+        else:
+            ss.adam(step)
         if ev is not None:
             ev[2].record(stream)
         if not args.zero_copy:
@@ -350,16 +415,18 @@ def gpu_arm(args, rank: int, world: int):
     k_unpack = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
     # End to end through the C ABI with host buffers: every step copies its
-    # gradients in from pinned host memory and its bf16 parameters (and the
-    # norm) back out, inside the timed region. Steps are pipelined on three
-    # streams with two device buffer sets: the copy-in of step k+1 and the
-    # copy-out of step k-1 overlap the compute of step k.
+    # gradients in from pinned host memory (the two gradient sets alternate)
+    # and its bf16 parameters and norm back out, inside the timed region.
+    # Steps are pipelined on three streams with two device buffer sets: the
+    # copy-in of step k+1 and the copy-out of step k-1 overlap the compute of
+    # step k. Each step's norm goes to a slot of its own, written by the
+    # library's norm kernel and read back on the copy-out stream, so that no
+    # copy is queued on the compute stream (a device-to-host copy there would
+    # wait for the previous step's copy-out in the copy engine and serialise
+    # the pipeline).
     e2e_steps = max(3, min(args.steps, 100))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    dev_g2 = [dev_g, torch.empty_like(dev_g)]
-    dev_p2 = [dev_p, torch.empty_like(dev_p)]
-    grads2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_g2]
-    params2 = [[b[s0:s0 + n] for s0, n in zip(starts, ss.numels)] for b in dev_p2]
+    dev_norms = torch.zeros(e2e_steps, 2, dtype=torch.float64, device=dev)
     host_norms = torch.empty(e2e_steps, 2, dtype=torch.float64).pin_memory()
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
     ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
@@ -376,14 +443,15 @@ def gpu_arm(args, rank: int, world: int):
     dist_k = 2
     for k in range(e2e_steps):
         buf = k % 2
+        hsrc = host_g2[k % 2]
         with torch.cuda.stream(s_in):
             if k >= dist_k:
                 s_in.wait_event(ev_done[k - dist_k])  # compute k-d has read this buffer
             if args.zero_copy:
                 for v, s0, n in zip(gviews_of(buf), starts, ss.numels):
-                    v.copy_(host_g[s0:s0 + n], non_blocking=True)
+                    v.copy_(hsrc[s0:s0 + n], non_blocking=True)
             else:
-                dev_g2[buf].copy_(host_g, non_blocking=True)
+                dev_g2[buf].copy_(hsrc, non_blocking=True)
             ev_in[k].record(s_in)
         with torch.cuda.stream(stream):
             stream.wait_event(ev_in[k])
@@ -391,13 +459,12 @@ def gpu_arm(args, rank: int, world: int):
                 stream.wait_event(ev_out[k - dist_k])  # copy-out k-d has read this buffer
             step += 1
             if args.zero_copy:
-                ss.zero_copy_step(step, zc_grad[buf], zc_bf[buf])
+                ss.zero_copy_step(step, zc_grad[buf], zc_bf[buf], norm=dev_norms[k])
             else:
                 ss.pack(grads2[buf])
-                ss.group_norm_scale()
+                ss.group_norm_scale(norm=dev_norms[k])
                 ss.adam(step)
                 ss.unpack(params2[buf])
-            host_norms[k].copy_(ss.norm, non_blocking=True)
             ev_done[k].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[k])
@@ -406,11 +473,14 @@ def gpu_arm(args, rank: int, world: int):
                     host_p[s0:s0 + n].copy_(v, non_blocking=True)
             else:
                 host_p.copy_(dev_p2[buf], non_blocking=True)
+            host_norms[k].copy_(dev_norms[k], non_blocking=True)
             ev_out[k].record(s_out)
     s_out.wait_stream(stream)
     e_end.record(s_out)
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    if not all(math.isfinite(x) and x > 0 for x in host_norms[:, 0].tolist()):
+        raise RuntimeError("end-to-end leg: a step's norm did not reach the host")
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -420,6 +490,10 @@ def gpu_arm(args, rank: int, world: int):
     peak, peak_kind = measured_peak()
     adam_gbs = nbytes["adam"] / (k_adam * 1e-3) / 1e9
     value = nbytes["step"] * world / (ms_step * 1e-3) / 1e9
+    traffic = None
+    if not args.bulk_warps and args.fraction == 1.0 and w.name in TRAFFIC:
+        # DRAM bytes per algorithmic byte of the capture, scaled to this launch
+        traffic = round(TRAFFIC[w.name]["ratio"] * nbytes["adam"], 0)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "params_per_s": round(n_real * world / (ms_step * 1e-3), 1),
@@ -438,13 +512,20 @@ def gpu_arm(args, rank: int, world: int):
                                  "unpack": round(k_unpack, 5)},
                    "frac_of_peak_step": round(value / world / peak, 4),
                    "frac_of_nominal_8tbs_step": round(value / world / NOMINAL_HBM_GBS, 4),
+                   "frac_of_copy_ceiling_step": round(value / world / ceiling["gbs"], 4),
+                   "copy_ceiling": ceiling,
+                   "inputs": "fresh gradients each step: two seeded sets (steps 1 and 2) "
+                             "alternate, on the device and in pinned host memory",
                    "plan_seconds": round(ss.info.plan_seconds, 6),
                    "bulk_warps": ss.info.bulk_warps},
         "roofline": {"bound": "hbm", "achieved": round(adam_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(adam_gbs / peak, 4),
+                     "frac_of_copy_ceiling": round(adam_gbs / ceiling["gbs"], 4),
+                     "algorithmic_bytes": nbytes["adam"],
                      # captured with the planner's own kernel shape
-                     "traffic": None if args.bulk_warps else TRAFFIC.get(w.name),
+                     "traffic": traffic,
                      "traffic_unit": "bytes per launch",
+                     "traffic_source": TRAFFIC[w.name]["capture"] if traffic else None,
                      "kernel": "vsf_adam8_step",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
@@ -828,14 +909,14 @@ def muon_cpu_baseline(w, threads: int | None = None):
                        f"{sec:.2f} s, numpy BLAS with {threads} threads")
 
 
-# Per-launch DRAM traffic in bytes (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the AdamW bulk-copy kernel, from the ncu captures summarised in profiles/
-# (adam8_tma_*.md); a workload without a capture of the current kernel is None.
-TRAFFIC: dict = {
-    "llama_layer": 1.733897e9 + 1.547784e9,
-    "dsv3_block": 2.478061e9 + 2.040586e9,
-    "moe_layer": 8.500441e9 + 6.297023e9,
-}
+# DRAM traffic of vsf_adam8_step's bulk-copy kernel per algorithmic byte
+# ((dram__bytes_read.sum + dram__bytes_write.sum) / (16 B per element + 16 B
+# per quantisation block)), from ncu captures of reduced cases of each
+# workload (every tensor cut to a fraction of its rows: the same block sizes,
+# fewer blocks) summarised in profiles/adam8_tma_*.md. The line's `traffic`
+# is this ratio times the full launch's algorithmic bytes. A workload without
+# a capture of the current kernel has no entry (traffic null).
+TRAFFIC: dict = {}
 
 
 def reference_arm(args):
@@ -903,7 +984,10 @@ def main():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="vsf", choices=["vsf", "reference"])
-    ap.add_argument("--workload", default="llama_layer")
+    ap.add_argument("--workload", default="llama_1p3b")
+    ap.add_argument("--fraction", type=float, default=1.0,
+                    help="cut every tensor to this fraction of its rows (reduced cases for "
+                         "profiling captures; not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--optimizer", default="adam8", choices=["adam8", "muon"],
                     help="adam8: the 8-bit AdamW shard step; muon: distributed Muon")

@@ -872,6 +872,51 @@ vsf_status vsf_unpack(const vsf_plan* plan, const uint16_t* packed_bf16, void* c
 
 }  // extern "C"
 
+// ------------------------------------------------------------------ copy ceiling
+
+namespace vsf {
+namespace {
+
+constexpr int kCeilThreads = 512;
+constexpr int kCeilUnroll = 8;
+
+// dst[i] = src[i] over n 16-byte words: each thread keeps kCeilUnroll
+// streaming loads in flight, grid-stride over the whole range.
+__global__ void __launch_bounds__(kCeilThreads) device_copy_kernel(uint4* __restrict__ dst,
+                                                                   const uint4* __restrict__ src,
+                                                                   int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * kCeilThreads;
+  int64_t i = (int64_t)blockIdx.x * kCeilThreads + threadIdx.x;
+  for (; i + (kCeilUnroll - 1) * stride < n; i += kCeilUnroll * stride) {
+    uint4 r[kCeilUnroll];
+#pragma unroll
+    for (int u = 0; u < kCeilUnroll; ++u) r[u] = ld_stream(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kCeilUnroll; ++u) st_stream(dst + i + u * stride, r[u]);
+  }
+  for (; i < n; i += stride) st_stream(dst + i, ld_stream(src + i));
+}
+
+}  // namespace
+}  // namespace vsf
+
+extern "C" vsf_status vsf_device_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  using namespace vsf;
+  if (dst == nullptr || src == nullptr) return fail(VSF_ERR_ARG, "vsf_device_copy: NULL pointer");
+  if (bytes % 16 != 0) return fail(VSF_ERR_ARG, "vsf_device_copy: bytes not a multiple of 16");
+  if (misaligned(dst) || misaligned(src))
+    return fail(VSF_ERR_ALIGN, "vsf_device_copy: pointer not 16-byte aligned");
+  if (bytes == 0) return VSF_OK;
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "vsf_device_copy");
+  device_copy_kernel<<<sms * 4, kCeilThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(dst), static_cast<const uint4*>(src), (int64_t)(bytes / 16));
+  e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : cuda_fail(e, "vsf_device_copy");
+}
+
 // ------------------------------------------------------------------ fused group ops
 
 namespace vsf {
@@ -1011,20 +1056,49 @@ __global__ void __launch_bounds__(kCopyThreads) sumsq_static_kernel(StaticNormAr
 }
 
 std::mutex g_static_mu;
-double* g_static_ptr[256] = {};  // device address of g_static_partials, per device
+// Device address of g_static_partials per device, with the context it was
+// looked up in: after a device reset the primary context (and with it the
+// module and the array's address) is new, and the address is looked up again.
+struct StaticAddr {
+  CUcontext ctx = nullptr;
+  double* ptr = nullptr;
+};
+StaticAddr g_static_addr[256];
 
-// Looks the array's device address up once per device (with that device
-// current); host code cannot use the symbol itself as a device pointer.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+// Looks the array's device address up (with the device current) once per
+// device and context; host code cannot use the symbol itself as a device
+// pointer.
 vsf_status static_partials(int dev, double** out) {
   if (dev < 0 || dev >= 256) return fail(VSF_ERR_ARG, "vsf_group_norm_scale_static: device id");
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (get_ctx == nullptr) return fail(VSF_ERR_CUDA, "cuCtxGetCurrent is unavailable");
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+    return fail(VSF_ERR_CUDA, "vsf_group_norm_scale_static: no current context");
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (g_static_ptr[dev] == nullptr) {
+  StaticAddr& a = g_static_addr[dev];
+  if (a.ptr == nullptr || a.ctx != ctx) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_static_partials);
     if (e != cudaSuccess) return cuda_fail(e, "vsf_group_norm_scale_static (symbol address)");
-    g_static_ptr[dev] = static_cast<double*>(p);
+    a.ptr = static_cast<double*>(p);
+    a.ctx = ctx;
   }
-  *out = g_static_ptr[dev];
+  *out = a.ptr;
   return VSF_OK;
 }
 

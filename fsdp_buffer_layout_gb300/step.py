@@ -92,10 +92,13 @@ class ShardStep:
         V.vsf_pack(self.plan, [g.data_ptr() for g in grads], self.grad_dtype,
                    self.packed_grad.data_ptr(), self.stream.cuda_stream)
 
-    def group_norm_scale(self, standalone: bool = False):
+    def group_norm_scale(self, standalone: bool = False, norm: torch.Tensor | None = None):
+        """Factor into self.factor; the fp64 norm into `norm` (a device fp64
+        tensor, e.g. one slot per step of a pipeline) or else self.norm."""
+        out = self.norm if norm is None else norm
         V.vsf_group_norm_scale(self.plan, self.packed_grad.data_ptr() if standalone else None,
                                self.grad_dtype, self.hp, self.factor.data_ptr(),
-                               self.norm.data_ptr(), self.stream.cuda_stream)
+                               out.data_ptr(), self.stream.cuda_stream)
 
     def group_sumsq(self, standalone: bool = False):
         """This window's fp64 sum of squares into self.sumsq[0] (device)."""
@@ -157,17 +160,29 @@ class ShardStep:
             out.append(v)
         return out
 
-    def zero_copy_step(self, step: int, packed_grad=None, packed_bf16=None):
+    def zero_copy_step(self, step: int, packed_grad=None, packed_bf16=None, norm=None):
         """One step when gradients and parameters are views of the packed
         buffers: group norm/scale on the packed gradient, then AdamW. A caller
         that double-buffers passes the gradient and bf16 buffers of this step
-        (same size and type as self.packed_grad / self.packed_bf16); the
-        optimizer state is always this object's."""
+        (same size and type as self.packed_grad / self.packed_bf16) and may
+        pass a device fp64 slot for the norm; the optimizer state is always
+        this object's."""
+        self.zero_copy_norm(packed_grad, norm)
+        self.zero_copy_adam(step, packed_grad, packed_bf16)
+
+    def zero_copy_norm(self, packed_grad=None, norm=None):
+        """The group norm/scale half of zero_copy_step (one pass over the
+        packed gradient)."""
+        g = self.packed_grad if packed_grad is None else packed_grad
+        nrm = self.norm if norm is None else norm
+        V.vsf_group_norm_scale(self.plan, g.data_ptr(), self.grad_dtype, self.hp,
+                               self.factor.data_ptr(), nrm.data_ptr(),
+                               self.stream.cuda_stream)
+
+    def zero_copy_adam(self, step: int, packed_grad=None, packed_bf16=None):
+        """The AdamW half of zero_copy_step."""
         g = self.packed_grad if packed_grad is None else packed_grad
         out = self.packed_bf16 if packed_bf16 is None else packed_bf16
-        V.vsf_group_norm_scale(self.plan, g.data_ptr(), self.grad_dtype, self.hp,
-                               self.factor.data_ptr(), self.norm.data_ptr(),
-                               self.stream.cuda_stream)
         V.vsf_adam8_step(self.plan, g.data_ptr(), self.grad_dtype, self.factor.data_ptr(),
                          self.master.data_ptr(), self.m_state.data_ptr(), self.v_state.data_ptr(),
                          self.m_scale.data_ptr(), self.v_scale.data_ptr(), out.data_ptr(),

@@ -99,6 +99,8 @@ def lib():
             L.vsf_pack.argtypes = [vp, P(vp), i32, vp, vp]
             L.vsf_selftest_wait_timeout.restype = st
             L.vsf_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+            L.vsf_device_copy.restype = st
+            L.vsf_device_copy.argtypes = [vp, vp, ctypes.c_size_t, vp]
             L.vsf_plan_restrict.restype = st
             L.vsf_plan_restrict.argtypes = [vp, i32, i32]
             L.vsf_plan_set_bulk_warps.restype = st
@@ -183,6 +185,10 @@ def vsf_plan_destroy(plan: int) -> None:
 
 def vsf_selftest_wait_timeout(d_err: int, limit_ns: int, stream: int) -> None:
     _check(lib().vsf_selftest_wait_timeout(d_err, limit_ns, stream))
+
+
+def vsf_device_copy(dst: int, src: int, nbytes: int, stream: int) -> None:
+    _check(lib().vsf_device_copy(dst, src, nbytes, stream))
 
 
 def vsf_plan_restrict(plan: int, rank_begin: int, rank_end: int) -> None:
