@@ -81,28 +81,30 @@ def measured_bf16_peak(sustained: bool):
         return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
 
 
-SYM_BLOCK_MIN = 1024  # libvsf splits a symmetric product's diagonal block of this size or more
+GEMM_BM, GEMM_BN = 128, 256  # output tile of libvsf's Newton-Schulz kernel (rows, columns)
+
+
+def sym_tiles(n: int) -> int:
+    """Output tiles of one n x n symmetric product that libvsf computes: in
+    column block J (256 columns) the row blocks 0 .. 2J+1 (128 rows each),
+    the tiles that reach the diagonal or lie above it."""
+    mb, nb = -(-n // GEMM_BM), -(-n // GEMM_BN)
+    return sum(min(mb, 2 * J + 2) for J in range(nb))
 
 
 def sym_fraction(n: int) -> float:
-    """Share of a symmetric n x n product's FLOPs that libvsf's blocking
-    executes: a diagonal block splits into two halves plus their off-diagonal
-    block (mirrored) when it is >= 1024 at the top and >= 2048 one level down."""
-    def cost(size, level):
-        lim = SYM_BLOCK_MIN if level == 0 else 2 * SYM_BLOCK_MIN
-        if level < 2 and size >= lim and size % 16 == 0:
-            h = size // 2
-            return 2 * cost(h, level + 1) + h * h
-        return size * size
-    return cost(n, 0) / float(n * n)
+    """Share of a symmetric n x n product's FLOPs that libvsf's tensor-core
+    kernel executes (its computed tiles over all tiles; about 1/2 for large n)."""
+    mb, nb = -(-n // GEMM_BM), -(-n // GEMM_BN)
+    return sym_tiles(n) / float(mb * nb)
 
 
 def muon_flops(w, ns_steps: int = 5, executed: bool = False) -> float:
     """Newton-Schulz FLOPs of one Muon step over every matrix tensor of w.
     By the definition, per iteration: 2 n^2 k for the Gram matrix, 2 n^3 for
     its square, 2 n^2 k for the product with X (n = min(R, C), k = max(R, C)).
-    executed=True counts what the tensor cores run: libvsf computes the two
-    symmetric products by blocks (sym_fraction of their FLOPs)."""
+    executed=True counts what the tensor cores run: the two symmetric
+    products only on the tiles that reach or lie above the diagonal."""
     total = 0.0
     for t in w.tensors:
         if len(t.shape) < 2:
@@ -688,7 +690,9 @@ def muon_arm(args, rank: int, world: int):
                    "ns_steps": 5,
                    "ns_flops_per_step": flops, "ns_flops_executed_per_step": flops_exec,
                    "root_load_balance": round(balance, 4),
-                   "gemm": "cuBLASLt bf16 x bf16 -> bf16, fp32 accumulation, strided batch",
+                   "gemm": "libvsf tcgen05 kernel: bf16 x bf16 -> bf16, fp32 accumulation "
+                           "in TMEM, 128x256 tiles, symmetric products on the tiles at or "
+                           "above the diagonal",
                    "l2": "working set (master, momentum, Newton-Schulz buffers) larger than "
                          "L2, no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU, m virtual ranks",
@@ -698,8 +702,8 @@ def muon_arm(args, rank: int, world: int):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": "vsf_muon_step (Newton-Schulz GEMM chain with its element-wise "
                                "kernels)",
-                     "flops": "executed by the tensor cores (symmetric products by "
-                              "blocks); value counts the definition's full products",
+                     "flops": "executed by the tensor cores (symmetric products on half "
+                              "their tiles); value counts the definition's full products",
                      "peak_source": peak_src},
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5),
@@ -707,9 +711,8 @@ def muon_arm(args, rank: int, world: int):
                 "d2h_bytes_per_step": int(host_p.numel() * 2)},
         "gpu_launches": (2 + V.vsf_muon_kernel_launches(ss.plan, 5)) * args.steps,
         "gpu_launches_note": "own kernels: copy-in, copy-out, and per batched chunk of "
-                             "same-shape matrices momentum, normalise, update and the block "
-                             "transposes of the symmetric products; the Newton-Schulz GEMMs "
-                             "are cuBLASLt launches, not counted",
+                             "same-shape matrices momentum, normalise, update and 3 "
+                             "Newton-Schulz products per iteration",
         "clocks": clocks,
     }
 

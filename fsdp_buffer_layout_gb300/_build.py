@@ -77,7 +77,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     tmp = out + ".tmp"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
     cmd = [nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + [
-        "-lcudart_static", "-L" + cuda_lib, "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib]
+        "-lcudart_static", "-L" + cuda_lib, "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")

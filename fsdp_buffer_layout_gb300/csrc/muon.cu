@@ -10,8 +10,10 @@
 //   Redistribute(u, root) zero-copy: a tensor is contiguous in the buffer, so
 //                         the root's "whole matrix" is a view of it;
 //   Newton-Schulz         on the root: 5 quintic iterations, 3 tensor-core
-//                         GEMMs each (cuBLASLt, bf16 operands, fp32
-//                         accumulation), batched over a tensor's matrices;
+//                         products each (this library's tcgen05 kernel,
+//                         ns_gemm.cuh: bf16 operands, fp32 accumulation in
+//                         TMEM, the two symmetric products on half their
+//                         tiles), batched over a tensor's matrices;
 //   Redistribute back     zero-copy again; the element-wise update writes the
 //                         ragged shards in place.
 // Matrices of one shape from every tensor are batched into the same launches
@@ -23,7 +25,8 @@
 // (a, b, c) = (3.4445, -4.7750, 2.0315); wide matrices A = X X^T,
 // X = a X + B X; tall ones A = X^T X, X = a X + X B; p = p (1 - lr wd) -
 // fp32(lr sqrt(max(1, R/C))) O; the fp32 ops rounded once (-fmad=false).
-#include <cublasLt.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,12 +49,9 @@ constexpr int kMuonThreads = 256;
 constexpr int kMuonTargetCtas = 152 * 8;         // fills every SM of the GPU
 constexpr int kMaxChunk = 192;                    // matrices in one batched chunk
 constexpr int64_t kChunkElems = int64_t(1) << 28;  // bf16 elements of X per chunk (512 MB)
-constexpr size_t kLtWorkspace = 64u << 20;         // cuBLASLt workspace bytes
-constexpr int64_t kSymBlockMin = 1024;             // n from which symmetric products use blocks
-#ifndef VSF_SYM_LEVELS
-#define VSF_SYM_LEVELS 2
-#endif
-constexpr int kSymLevels = VSF_SYM_LEVELS;         // levels of splitting (a lower one needs 2048)
+
+#include "mbarrier.cuh"
+#include "ns_gemm.cuh"
 
 // Packed-buffer offset of every matrix of one chunk (kernel parameter).
 struct MatTable {
@@ -211,62 +211,6 @@ __global__ void __launch_bounds__(kMuonThreads) muon_update_kernel(
   }
 }
 
-// Symmetric products computed by blocks: an off-diagonal block below the
-// diagonal is the transpose of its mirror above it. A is row-major n x n;
-// block sizes and offsets are multiples of 8 (rows start on 16 bytes).
-// One launch mirrors every block of one product: the grid's x index runs
-// over the 64 x 64 tiles of all blocks in turn (tile_begin holds each block's
-// first tile), y over the matrices of the chunk. One CTA (8 warps) per tile:
-// rows of the source tile are read as 32-bit bf16 pairs (coalesced), kept in
-// shared memory (rows padded to 33 words), and each output word pairs the
-// same column of two adjacent source rows; output rows are written as
-// 32-bit words (coalesced).
-constexpr int kMaxMirrors = 4;
-struct MirrorBlocks {
-  int64_t bi[kMaxMirrors], bj[kMaxMirrors], size[kMaxMirrors];
-  int32_t tile_begin[kMaxMirrors + 1];
-  int32_t count;
-};
-
-__global__ void __launch_bounds__(256) mirror_kernel(uint16_t* A, int64_t n, const __grid_constant__ MirrorBlocks mb,
-                                                     int64_t sa) {
-  __shared__ uint32_t tile[64][33];
-  int q = 0;
-  while (q + 1 < mb.count && (int)blockIdx.x >= mb.tile_begin[q + 1]) ++q;
-  const int64_t bi = mb.bi[q], bj = mb.bj[q], h = mb.size[q];
-  const int64_t tiles = (h + 63) / 64;
-  const int64_t tix = (int64_t)blockIdx.x - mb.tile_begin[q];
-  uint16_t* M = A + (int64_t)blockIdx.y * sa;
-  // the h x h block at rows bi, columns bj, mirrored to rows bj, columns bi
-  const int64_t i0 = tix / tiles * 64, j0 = tix % tiles * 64;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int r = warp; r < 64; r += 8) {
-    const int64_t i = i0 + r, j = j0 + 2 * lane;
-    uint32_t w = 0;
-    if (i < h && j + 1 < h) {
-      w = *reinterpret_cast<const uint32_t*>(M + (bi + i) * n + bj + j);
-    } else if (i < h && j < h) {
-      w = M[(bi + i) * n + bj + j];
-    }
-    tile[r][lane] = w;
-  }
-  __syncthreads();
-  // destination row bj + j0 + c holds source column j0 + c; its word `lane`
-  // holds source rows i0 + 2 lane and i0 + 2 lane + 1
-  for (int c = warp; c < 64; c += 8) {
-    const int64_t orow = j0 + c, ocol = i0 + 2 * lane;
-    if (orow >= h || ocol >= h) continue;
-    const uint32_t a = tile[2 * lane][c >> 1], b = tile[2 * lane + 1][c >> 1];
-    const uint32_t lo = (c & 1) ? (a >> 16) : (a & 0xffffu);
-    const uint32_t hi = (c & 1) ? (b >> 16) : (b & 0xffffu);
-    uint16_t* dst = M + (bj + orow) * n + bi + ocol;
-    if (ocol + 1 < h)
-      *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);
-    else
-      *dst = (uint16_t)lo;
-  }
-}
-
 struct MuonMatrix {
   int tensor;
   int64_t batch, R, C;
@@ -339,7 +283,7 @@ int muon_per(int64_t batch, int64_t mat) {
 }
 
 struct MuonLayout {
-  size_t lt = 0, partials = 0, x = 0, xn = 0, a = 0, b = 0, bytes = 0;
+  size_t partials = 0, x = 0, xn = 0, a = 0, b = 0, bytes = 0;
 };
 
 MuonLayout muon_layout(const vsf_plan* plan) {
@@ -357,7 +301,6 @@ MuonLayout muon_layout(const vsf_plan* plan) {
     cur = at + bytes;
     return at;
   };
-  L.lt = section(kLtWorkspace);
   L.partials = section(sizeof(double) * std::max<int64_t>(1, max_part));
   L.x = section(2 * std::max<int64_t>(1, max_elems));
   L.xn = section(2 * std::max<int64_t>(1, max_elems));
@@ -367,94 +310,124 @@ MuonLayout muon_layout(const vsf_plan* plan) {
   return L;
 }
 
-// cuBLASLt: one handle per process, plans cached by GEMM shape.
-struct LtGemm {
-  cublasLtMatmulDesc_t op = nullptr;
-  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-  cublasLtMatmulAlgo_t algo;
-  bool ok = false;
-};
-
-std::mutex g_lt_mu;
-cublasLtHandle_t g_lt = nullptr;
-std::map<std::tuple<int, int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
-                    uint32_t, uint32_t, uint32_t>,
-         LtGemm>
-    g_lt_cache;
-
-// Largest power of two (at most 256) dividing the address of every matrix of
-// a strided batch; the algorithm heuristic assumes 256 unless told.
-uint32_t batch_alignment(const void* p, int64_t stride_elems) {
-  uint64_t v = (uint64_t)reinterpret_cast<uintptr_t>(p) | (uint64_t)(stride_elems * 2) | 256u;
-  return (uint32_t)(v & (~v + 1));
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 gemm_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
 }
 
-vsf_status lt_fail(cublasStatus_t s, const char* what) {
-  return fail(VSF_ERR_CUDA, std::string(what) + ": cuBLASLt status " + std::to_string((int)s));
+// Tensor map of one GEMM operand over a strided batch of row-major bf16
+// matrices (leading dimension ld, batch stride bs, in elements). K-major:
+// `rows` rows of K elements, box 64 K x box_rows rows. MN-major: K rows of
+// `rows` (the M or N extent) elements, box 64 x 64. 128-byte swizzle; copies
+// outside the matrix read zeros.
+vsf_status gemm_operand_map(CUtensorMap* map, const uint16_t* ptr, bool mn, int64_t rows,
+                            int64_t K, int64_t ld, int64_t bs, int64_t batch, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = gemm_map_encoder();
+  if (encode == nullptr) return fail(VSF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)(mn ? rows : K), (cuuint64_t)(mn ? K : rows),
+                        (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)std::max<int64_t>(bs, ld) * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)(mn ? 64 : box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(VSF_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return VSF_OK;
 }
 
-// Column-major D[M x N] = alpha * op(A)[M x K] * op(B)[K x N] + beta * C, bf16
-// in and out, fp32 accumulation, strided batch. lda/ldb/ldc are the
-// column-major leading dimensions of the stored A, B, C/D.
-vsf_status lt_gemm(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                   int64_t sa, const void* B, int64_t ldb, int64_t sb, float alpha, float beta,
-                   const void* C, void* D, int64_t ldc, int64_t sc, int64_t batch, void* ws,
-                   cudaStream_t st) {
-  std::lock_guard<std::mutex> lock(g_lt_mu);
-  cublasStatus_t s;
-  if (g_lt == nullptr) {
-    s = cublasLtCreate(&g_lt);
-    if (s != CUBLAS_STATUS_SUCCESS) return lt_fail(s, "cublasLtCreate");
+template <bool AMN, bool BMN, bool SYM>
+vsf_status launch_ns_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const NsGemmArgs& g,
+                          unsigned* err, int sms, cudaStream_t st) {
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      ns_gemm_kernel<AMN, BMN, SYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  if (attr != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("ns_gemm: ") + cudaGetErrorString(attr));
+  const int ntiles = g.batch * g.tiles_per_matrix;
+  ns_gemm_kernel<AMN, BMN, SYM><<<std::max(1, std::min(sms, ntiles)), kGemmThreads, kGemmSmem, st>>>(
+      ma, mb, g, err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("ns_gemm: ") + cudaGetErrorString(e));
+}
+
+template <bool AMN, bool BMN, bool SYM>
+vsf_status launch_ns_gemm_simt(const uint16_t* A, int64_t lda, int64_t sa, const uint16_t* B,
+                               int64_t ldb, int64_t sb, const NsGemmArgs& g, cudaStream_t st) {
+  const dim3 grid((unsigned)((g.N + 15) / 16), (unsigned)((g.M + 15) / 16), (unsigned)g.batch);
+  ns_gemm_simt_kernel<AMN, BMN, SYM><<<grid, 256, 0, st>>>(A, lda, sa, B, ldb, sb, g);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("ns_gemm: ") + cudaGetErrorString(e));
+}
+
+bool tma_ok(const void* p, int64_t ld, int64_t bs) {
+  return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && ld % 8 == 0 && bs % 8 == 0;
+}
+
+// D[b] = alpha * opA[b] opB[b]^T + beta * C[b] over a strided batch (see
+// ns_gemm.cuh). Operand combinations: K-major x K-major (symmetric or not),
+// MN-major x MN-major (symmetric), K-major x MN-major. The tensor-core
+// kernel needs leading dimensions and batch strides that are multiples of 8
+// elements and 16-byte aligned operands; anything else takes the CUDA-core
+// kernel.
+vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t K, int64_t batch,
+                   const uint16_t* A, int64_t lda, int64_t sa, const uint16_t* B, int64_t ldb,
+                   int64_t sb, float alpha, float beta, const uint16_t* C, int64_t ldc, int64_t sc,
+                   uint16_t* D, int64_t ldd, int64_t sd, unsigned* err, int sms, cudaStream_t st) {
+  if (M < 1 || N < 1 || K < 1 || batch < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
+      batch > 65535)
+    return fail(VSF_ERR_ARG, "ns_gemm: sizes out of range");
+  if (sym && (M != N || a_mn != b_mn)) return fail(VSF_ERR_ARG, "ns_gemm: symmetric needs opA = opB");
+  NsGemmArgs g{};
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.batch = (int)batch;
+  g.alpha = alpha;
+  g.beta = beta;
+  g.C = C;
+  g.ldc = ldc;
+  g.sc = sc;
+  g.D = D;
+  g.ldd = ldd;
+  g.sd = sd;
+  g.mblocks = (int)((M + kGemmBM - 1) / kGemmBM);
+  const int nblocks = (int)((N + kGemmBN - 1) / kGemmBN);
+  if (sym) {
+    g.tiles_per_matrix = 0;
+    for (int J = 0; J < nblocks; ++J) g.tiles_per_matrix += std::min(g.mblocks, 2 * J + 2);
+  } else {
+    g.tiles_per_matrix = g.mblocks * nblocks;
   }
-  const uint32_t al_a = batch_alignment(A, sa), al_b = batch_alignment(B, sb),
-                 al_c = std::min(batch_alignment(C, sc), batch_alignment(D, sc));
-  auto key = std::make_tuple((int)ta, (int)tb, M, N, K, lda, ldb, ldc, batch, al_a, al_b, al_c);
-  LtGemm& g = g_lt_cache[key];
-  if (!g.ok) {
-    const cublasOperation_t opa = ta ? CUBLAS_OP_T : CUBLAS_OP_N;
-    const cublasOperation_t opb = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-    if ((s = cublasLtMatmulDescCreate(&g.op, CUBLAS_COMPUTE_32F, CUDA_R_32F)) != CUBLAS_STATUS_SUCCESS)
-      return lt_fail(s, "cublasLtMatmulDescCreate");
-    cublasLtMatmulDescSetAttribute(g.op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa));
-    cublasLtMatmulDescSetAttribute(g.op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb));
-    const uint64_t ar = ta ? K : M, ac = ta ? M : K, br = tb ? N : K, bc = tb ? K : N;
-    if ((s = cublasLtMatrixLayoutCreate(&g.la, CUDA_R_16BF, ar, ac, lda)) != CUBLAS_STATUS_SUCCESS ||
-        (s = cublasLtMatrixLayoutCreate(&g.lb, CUDA_R_16BF, br, bc, ldb)) != CUBLAS_STATUS_SUCCESS ||
-        (s = cublasLtMatrixLayoutCreate(&g.lc, CUDA_R_16BF, M, N, ldc)) != CUBLAS_STATUS_SUCCESS)
-      return lt_fail(s, "cublasLtMatrixLayoutCreate");
-    const int32_t bcount = (int32_t)batch;
-    cublasLtMatrixLayoutSetAttribute(g.la, CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &bcount, sizeof(bcount));
-    cublasLtMatrixLayoutSetAttribute(g.lb, CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &bcount, sizeof(bcount));
-    cublasLtMatrixLayoutSetAttribute(g.lc, CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &bcount, sizeof(bcount));
-    cublasLtMatrixLayoutSetAttribute(g.la, CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &sa, sizeof(sa));
-    cublasLtMatrixLayoutSetAttribute(g.lb, CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &sb, sizeof(sb));
-    cublasLtMatrixLayoutSetAttribute(g.lc, CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &sc, sizeof(sc));
-    cublasLtMatmulPreference_t pref;
-    cublasLtMatmulPreferenceCreate(&pref);
-    const size_t wsb = kLtWorkspace;
-    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb,
-                                         sizeof(wsb));
-    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES, &al_a,
-                                         sizeof(al_a));
-    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES, &al_b,
-                                         sizeof(al_b));
-    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES, &al_c,
-                                         sizeof(al_c));
-    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES, &al_c,
-                                         sizeof(al_c));
-    cublasLtMatmulHeuristicResult_t res;
-    int found = 0;
-    s = cublasLtMatmulAlgoGetHeuristic(g_lt, g.op, g.la, g.lb, g.lc, g.lc, pref, 1, &res, &found);
-    cublasLtMatmulPreferenceDestroy(pref);
-    if (s != CUBLAS_STATUS_SUCCESS || found == 0)
-      return lt_fail(s == CUBLAS_STATUS_SUCCESS ? CUBLAS_STATUS_NOT_SUPPORTED : s,
-                     "cublasLtMatmulAlgoGetHeuristic");
-    g.algo = res.algo;
-    g.ok = true;
+  const bool tc = tma_ok(A, lda, sa) && tma_ok(B, ldb, sb) && tma_ok(D, ldd, sd) &&
+                  (beta == 0.0f || tma_ok(C, ldc, sc)) &&
+                  (int64_t)g.tiles_per_matrix * batch < INT32_MAX;
+  if (!tc) {
+    if (!a_mn && !b_mn && sym) return launch_ns_gemm_simt<false, false, true>(A, lda, sa, B, ldb, sb, g, st);
+    if (!a_mn && !b_mn) return launch_ns_gemm_simt<false, false, false>(A, lda, sa, B, ldb, sb, g, st);
+    if (a_mn && b_mn && sym) return launch_ns_gemm_simt<true, true, true>(A, lda, sa, B, ldb, sb, g, st);
+    if (!a_mn && b_mn && !sym) return launch_ns_gemm_simt<false, true, false>(A, lda, sa, B, ldb, sb, g, st);
+    return fail(VSF_ERR_ARG, "ns_gemm: unsupported operand layout");
   }
-  s = cublasLtMatmul(g_lt, g.op, &alpha, A, g.la, B, g.lb, &beta, C, g.lc, D, g.lc, &g.algo, ws,
-                     kLtWorkspace, st);
-  return s == CUBLAS_STATUS_SUCCESS ? VSF_OK : lt_fail(s, "cublasLtMatmul");
+  CUtensorMap ma, mb;
+  vsf_status s = gemm_operand_map(&ma, A, a_mn, M, K, lda, sa, batch, kGemmBM);
+  if (s == VSF_OK) s = gemm_operand_map(&mb, B, b_mn, N, K, ldb, sb, batch, kGemmBN);
+  if (s != VSF_OK) return s;
+  if (!a_mn && !b_mn && sym) return launch_ns_gemm<false, false, true>(ma, mb, g, err, sms, st);
+  if (!a_mn && !b_mn) return launch_ns_gemm<false, false, false>(ma, mb, g, err, sms, st);
+  if (a_mn && b_mn && sym) return launch_ns_gemm<true, true, true>(ma, mb, g, err, sms, st);
+  if (!a_mn && b_mn && !sym) return launch_ns_gemm<false, true, false>(ma, mb, g, err, sms, st);
+  return fail(VSF_ERR_ARG, "ns_gemm: unsupported operand layout");
 }
 
 }  // namespace
@@ -463,6 +436,28 @@ vsf_status lt_gemm(bool ta, bool tb, int64_t M, int64_t N, int64_t K, const void
 using namespace vsf;
 
 extern "C" {
+
+vsf_status vsf_ns_gemm(int32_t a_mn, int32_t b_mn, int32_t sym, int64_t M, int64_t N, int64_t K,
+                       int64_t batch, const uint16_t* A, int64_t lda, int64_t sa, const uint16_t* B,
+                       int64_t ldb, int64_t sb, float alpha, float beta, const uint16_t* C,
+                       int64_t ldc, int64_t sc, uint16_t* D, int64_t ldd, int64_t sd,
+                       unsigned* d_err, void* stream) {
+  vsf::Range nvtx_range("vsf_ns_gemm");
+  if (A == nullptr || B == nullptr || D == nullptr || d_err == nullptr ||
+      (beta != 0.0f && C == nullptr))
+    return fail(VSF_ERR_ARG, "vsf_ns_gemm: NULL argument");
+  if (lda < 1 || ldb < 1 || ldd < 1 || (beta != 0.0f && ldc < 1) || sa < 0 || sb < 0 || sd < 0 ||
+      sc < 0)
+    return fail(VSF_ERR_ARG, "vsf_ns_gemm: bad leading dimension or batch stride");
+  if (!((a_mn == 0 && b_mn == 0) || (a_mn && b_mn && sym) || (a_mn == 0 && b_mn && !sym)))
+    return fail(VSF_ERR_ARG, "vsf_ns_gemm: operand layouts must be K/K, MN/MN (symmetric) or K/MN");
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_ns_gemm: ") + cudaGetErrorString(e));
+  return ns_gemm(a_mn != 0, b_mn != 0, sym != 0, M, N, K, batch, A, lda, sa, B, ldb, sb, alpha,
+                 beta, C, ldc, sc, D, ldd, sd, d_err, sms, static_cast<cudaStream_t>(stream));
+}
 
 vsf_status vsf_muon_select_roots(const vsf_plan* plan, int32_t* root, double* load_balance) {
   if (plan == nullptr || root == nullptr) return fail(VSF_ERR_ARG, "vsf_muon_select_roots: NULL");
@@ -504,7 +499,8 @@ int64_t vsf_muon_kernel_launches(const vsf_plan* plan, int32_t ns_steps) {
   int64_t n = 0;
   for (const MuonChunk& c : muon_chunks(plan)) {
     const int64_t nm = std::min(c.R, c.C);
-    n += 3 + (nm >= kSymBlockMin && nm % 16 == 0 ? 2 * (int64_t)ns_steps : 0);
+    (void)nm;
+    n += 3 + 3 * (int64_t)ns_steps;  // momentum, normalise, update; 3 products per iteration
   }
   return n;
 }
@@ -533,7 +529,11 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
   uint16_t* Xn = reinterpret_cast<uint16_t*>(ws + L.xn);
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
   uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
-  void* lt = ws + L.lt;
+  unsigned* err = reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error);
+  int dev = -1, sms = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de == cudaSuccess) de = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (de != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(de));
   const float mu = (float)hp->momentum;
   const float decay = (float)(1.0 - hp->lr * hp->weight_decay);
   const float na = (float)hp->ns_a, nb = (float)hp->ns_b, nc = (float)hp->ns_c;
@@ -561,86 +561,34 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
-    // Newton-Schulz, column-major view of the row-major R x C matrices: Xc is
-    // C x R with leading dimension C.
+    // Newton-Schulz on the row-major R x C matrices of the chunk (X holds
+    // them back to back, stride R*C; A and B are n x n, n = min(R, C)).
+    // Wide (R <= C): A = X X^T, B = c A A + b A, X' = a X + B X.
+    // Tall (R > C):  A = X^T X, B = c A A + b A, X' = a X + X B.
+    // A and B are symmetric, so the B operand of A A is A's rows and that of
+    // X B is B's rows; X^T X reads X's columns (MN-major) and B X reads X's
+    // columns as its second operand.
     const bool tall = c.R > c.C;
-    const int64_t n = std::min(c.R, c.C), sx = mat, sa = n * n;
-    // The two symmetric products (the Gram matrix and c A A + b A) by blocks:
-    // a diagonal block of size s >= 1024 (2048 below the top level) splits
-    // into two diagonal halves and their off-diagonal block, whose mirror is
-    // its transpose. One level costs 3/4 of the FLOPs, two levels 5/8; the
-    // results are exactly symmetric. Column-major operand views of the
-    // row-major buffers.
-    struct Blk {
-      int64_t i0, j0, size;
-    };
-    std::vector<Blk> gemm_blocks, mirrors;
-    {
-      std::vector<std::pair<Blk, int>> todo = {{{0, 0, n}, 0}};
-      while (!todo.empty()) {
-        const Blk b = todo.back().first;
-        const int level = todo.back().second;
-        todo.pop_back();
-        const int64_t smin = level == 0 ? kSymBlockMin : 2 * kSymBlockMin;
-        if (level < kSymLevels && b.size >= smin && b.size % 16 == 0) {
-          const int64_t h2 = b.size / 2;
-          todo.push_back({{b.i0, b.i0, h2}, level + 1});
-          todo.push_back({{b.i0 + h2, b.i0 + h2, h2}, level + 1});
-          gemm_blocks.push_back({b.i0, b.i0 + h2, h2});
-          mirrors.push_back({b.i0, b.i0 + h2, h2});
-        } else {
-          gemm_blocks.push_back(b);
-        }
-      }
-    }
-    if (mirrors.size() > (size_t)kMaxMirrors)
-      return fail(VSF_ERR_STATE, "vsf_muon_step: too many mirrored blocks");
-    MirrorBlocks mb{};
-    mb.count = (int32_t)mirrors.size();
-    mb.tile_begin[0] = 0;
-    for (size_t q = 0; q < mirrors.size(); ++q) {
-      mb.bi[q] = mirrors[q].i0;
-      mb.bj[q] = mirrors[q].j0;
-      mb.size[q] = mirrors[q].size;
-      const int64_t t = (mirrors[q].size + 63) / 64;
-      mb.tile_begin[q + 1] = mb.tile_begin[q] + (int32_t)(t * t);
-    }
-    auto mirror_all = [&](uint16_t* M) {
-      mirror_kernel<<<dim3((unsigned)mb.tile_begin[mb.count], (unsigned)c.batch), 256, 0, st>>>(
-          M, n, mb, sa);
-      const cudaError_t e2 = cudaGetLastError();
-      return e2 == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e2));
-    };
+    const int64_t n = std::min(c.R, c.C), k = std::max(c.R, c.C), sx = mat, sa = n * n;
     for (int it = 0; it < hp->ns_steps; ++it) {
       vsf_status s = VSF_OK;
-      // A (n x n) = X X^T (wide) or X^T X (tall); block (I, J) at A + I0 n + J0
-      for (size_t q = 0; q < gemm_blocks.size() && s == VSF_OK; ++q) {
-        const int64_t I0 = gemm_blocks[q].i0, J0 = gemm_blocks[q].j0, hs = gemm_blocks[q].size;
-        if (!tall)
-          s = lt_gemm(true, false, hs, hs, c.C, X + J0 * c.C, c.C, sx, X + I0 * c.C, c.C, sx, 1.0f,
-                      0.0f, A + I0 * n + J0, A + I0 * n + J0, n, sa, c.batch, lt, st);
-        else
-          s = lt_gemm(false, true, hs, hs, c.R, X + J0, c.C, sx, X + I0, c.C, sx, 1.0f, 0.0f,
-                      A + I0 * n + J0, A + I0 * n + J0, n, sa, c.batch, lt, st);
-      }
-      if (s == VSF_OK && !mirrors.empty()) s = mirror_all(A);
-      if (s != VSF_OK) return s;
-      // B = c A A + b A (A symmetric: block (I, J) = c A[J rows] A[I cols] + b A_IJ)
-      for (size_t q = 0; q < gemm_blocks.size() && s == VSF_OK; ++q) {
-        const int64_t I0 = gemm_blocks[q].i0, J0 = gemm_blocks[q].j0, hs = gemm_blocks[q].size;
-        s = lt_gemm(false, false, hs, hs, n, A + J0, n, sa, A + I0 * n, n, sa, nc, nb,
-                    A + I0 * n + J0, B + I0 * n + J0, n, sa, c.batch, lt, st);
-      }
-      if (s == VSF_OK && !mirrors.empty()) s = mirror_all(B);
-      if (s != VSF_OK) return s;
-      // X' = a X + B X (wide) or a X + X B (tall), column-major Xc' = a Xc +
-      // Xc B (wide) or a Xc + B Xc (tall)
       if (!tall)
-        s = lt_gemm(false, false, c.C, c.R, c.R, X, c.C, sx, B, n, sa, 1.0f, na, X, Xn, c.C, sx,
-                    c.batch, lt, st);
+        s = ns_gemm(false, false, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
+                    nullptr, n, sa, A, n, sa, err, sms, st);
       else
-        s = lt_gemm(false, false, c.C, c.R, c.C, B, n, sa, X, c.C, sx, 1.0f, na, X, Xn, c.C, sx,
-                    c.batch, lt, st);
+        s = ns_gemm(true, true, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
+                    nullptr, n, sa, A, n, sa, err, sms, st);
+      if (s == VSF_OK)
+        s = ns_gemm(false, false, true, n, n, n, c.batch, A, n, sa, A, n, sa, nc, nb, A, n, sa, B,
+                    n, sa, err, sms, st);
+      if (s == VSF_OK) {
+        if (!tall)  // X'[i][l] = a X[i][l] + sum_j B[i][j] X[j][l]
+          s = ns_gemm(false, true, false, n, c.C, n, c.batch, B, n, sa, X, c.C, sx, 1.0f, na, X,
+                      c.C, sx, Xn, c.C, sx, err, sms, st);
+        else        // X'[l][i] = a X[l][i] + sum_j X[l][j] B[i][j]
+          s = ns_gemm(false, false, false, c.R, n, n, c.batch, X, c.C, sx, B, n, sa, 1.0f, na, X,
+                      c.C, sx, Xn, c.C, sx, err, sms, st);
+      }
       if (s != VSF_OK) return s;
       std::swap(X, Xn);
     }

@@ -101,6 +101,10 @@ def lib():
             L.vsf_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
             L.vsf_device_copy.restype = st
             L.vsf_device_copy.argtypes = [vp, vp, ctypes.c_size_t, vp]
+            L.vsf_ns_gemm.restype = st
+            L.vsf_ns_gemm.argtypes = [i32, i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64,
+                                      i64, ctypes.c_float, ctypes.c_float, vp, i64, i64, vp, i64,
+                                      i64, vp, vp]
             L.vsf_plan_restrict.restype = st
             L.vsf_plan_restrict.argtypes = [vp, i32, i32]
             L.vsf_plan_set_bulk_warps.restype = st
@@ -185,6 +189,13 @@ def vsf_plan_destroy(plan: int) -> None:
 
 def vsf_selftest_wait_timeout(d_err: int, limit_ns: int, stream: int) -> None:
     _check(lib().vsf_selftest_wait_timeout(d_err, limit_ns, stream))
+
+
+def vsf_ns_gemm(a_mn: bool, b_mn: bool, sym: bool, M: int, N: int, K: int, batch: int,
+                A: int, lda: int, sa: int, B: int, ldb: int, sb: int, alpha: float, beta: float,
+                C, ldc: int, sc: int, D: int, ldd: int, sd: int, d_err: int, stream: int) -> None:
+    _check(lib().vsf_ns_gemm(int(a_mn), int(b_mn), int(sym), M, N, K, batch, A, lda, sa, B, ldb,
+                             sb, alpha, beta, C, ldc, sc, D, ldd, sd, d_err, stream))
 
 
 def vsf_device_copy(dst: int, src: int, nbytes: int, stream: int) -> None:

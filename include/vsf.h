@@ -336,13 +336,42 @@ vsf_status vsf_muon_select_roots(const vsf_plan* plan, int32_t* root, double* lo
 size_t vsf_muon_workspace_bytes(const vsf_plan* plan);
 int32_t vsf_muon_chunk_count(const vsf_plan* plan);
 /* Launches of the library's own kernels in one vsf_muon_step with ns_steps
- * iterations: 3 per chunk, plus 2 per iteration (the block transposes of the
- * two symmetric products) for chunks whose n = min(R, C) >= 1024 is a multiple
- * of 16. The cuBLASLt GEMMs are not counted. 0 for a NULL plan. */
+ * iterations: per batched chunk, momentum, normalisation and update, plus the
+ * three Newton–Schulz products of every iteration. 0 for a NULL plan. */
 int64_t vsf_muon_kernel_launches(const vsf_plan* plan, int32_t ns_steps);
 vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, float* momentum,
                          float* master, uint16_t* packed_bf16, const vsf_muon_hparams* hp,
                          void* d_workspace, size_t ws_bytes, void* stream);
+
+/* One Newton–Schulz product of distributed Muon ([VSF] 结构感知训练 case study
+ * › 分布式 Muon, Algorithm 2: the root's orthogonalisation needs A = X X^T (or
+ * X^T X), B = c A A + b A and X' = a X + B X (or a X + X B)), as the
+ * library's tcgen05 tensor-core kernel computes it inside vsf_muon_step:
+ *   D[b] = alpha * opA[b] * opB[b]^T + beta * C[b],  b = 0 .. batch-1,
+ * opA M x K, opB N x K, C and D M x N. All matrices are bf16, row-major, with
+ * leading dimension ld* and batch stride s* in elements; accumulation is fp32
+ * and D is rounded to nearest even once, after alpha * acc + beta * C.
+ *   a_mn = 0: opA[i][k] = A[i*lda + k] (K-major); a_mn = 1: A[k*lda + i]
+ *   (MN-major); likewise b_mn for opB[j][k]. Supported: K/K, K/MN, and MN/MN
+ *   with sym = 1.
+ *   sym = 1 (requires M = N and opA = opB, with C symmetric when beta != 0):
+ *   only the output tiles that reach or lie above the diagonal are computed
+ *   (half of the FLOPs); every D[i][j] with i <= j is written to D[i][j] and
+ *   D[j][i], so D is exactly symmetric.
+ *   C is read only when beta != 0 (may be NULL otherwise); D must not overlap
+ *   A, B or C. d_err: the device error word that a bounded wait sets (bit 1)
+ *   if the kernel's pipeline ever stalls for 2 s; a correct launch leaves it
+ *   unchanged.
+ * The tensor-core kernel needs 16-byte aligned A, B, C, D and leading
+ * dimensions and batch strides that are multiples of 8; other operands run a
+ * plain CUDA-core kernel with the same contract. Asynchronous on `stream`.
+ * Errors: VSF_ERR_ARG (NULL, sizes out of range, unsupported layout),
+ * VSF_ERR_CUDA. */
+vsf_status vsf_ns_gemm(int32_t a_mn, int32_t b_mn, int32_t sym, int64_t M, int64_t N, int64_t K,
+                       int64_t batch, const uint16_t* A, int64_t lda, int64_t sa, const uint16_t* B,
+                       int64_t ldb, int64_t sb, float alpha, float beta, const uint16_t* C,
+                       int64_t ldc, int64_t sc, uint16_t* D, int64_t ldd, int64_t sd,
+                       unsigned* d_err, void* stream);
 
 /* Self-test of the kernels' bounded waits (every wait on a barrier gives up
  * after a time limit, sets bit 1 of the device error word and lets the kernel

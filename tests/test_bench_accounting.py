@@ -5,9 +5,9 @@ Algorithmic bytes per real element of the shard step (bf16 gradients): pack
 plus 16 bytes of scales per quantisation block, unpack 2 + 2: 24 in all. With
 fp32 gradients pack moves 8 and AdamW 18 (30 in all); in zero-copy mode the
 step is the norm's read of the packed gradient plus AdamW (18). Muon's
-executed share of a symmetric product: 1 below n = 1024 (or when n is not a
-multiple of 16), 3/4 with one level of blocks (n = 1024..4095), 5/8 with two
-(n >= 4096), with the blocking threshold the library's own.
+executed share of a symmetric product: the 128 x 256 output tiles of the
+library's tensor-core kernel that hold an element on or above the diagonal
+(checked by brute force), with the tile shape the library's own.
 """
 import os
 import re
@@ -29,16 +29,26 @@ def test_algorithmic_bytes_per_element(grad_bytes, zero_copy, per_elem):
     assert b["adam"] == (grad_bytes + 14) * N + 16 * Q
 
 
-@pytest.mark.parametrize("n,frac", [(512, 1.0), (1000, 1.0), (1024, 0.75), (2048, 0.75),
-                                    (4080, 0.75), (4096, 0.625), (8192, 0.625)])
-def test_symmetric_blocking_share(n, frac):
-    assert bench.sym_fraction(n) == frac
+def _sym_tiles_brute(n, bm=128, bn=256):
+    """Tiles of an n x n output (bm x bn) that hold an element (i, j) with i <= j."""
+    count = 0
+    for I in range(-(-n // bm)):
+        for J in range(-(-n // bn)):
+            if any(i <= j for i in range(I * bm, min(n, I * bm + bm))
+                   for j in (min(n, J * bn + bn) - 1,)):
+                count += 1
+    return count
 
 
-def test_blocking_threshold_is_the_librarys():
-    src = open(os.path.join(ROOT, "fsdp_buffer_layout_gb300", "csrc", "muon.cu")).read()
-    lib_min = int(re.search(r"constexpr int64_t kSymBlockMin = (\d+);", src).group(1))
-    lib_levels = int(re.search(r"#define VSF_SYM_LEVELS (\d+)", src).group(1))
-    assert bench.SYM_BLOCK_MIN == lib_min
-    # sym_fraction splits at most twice: one level more would reach 9/16 at 8192
-    assert lib_levels == 2 and bench.sym_fraction(8192) == 0.625
+@pytest.mark.parametrize("n", [32, 100, 128, 200, 256, 300, 1000, 2048, 2880, 4096])
+def test_symmetric_tiles_are_those_touching_the_upper_triangle(n):
+    assert bench.sym_tiles(n) == _sym_tiles_brute(n)
+    assert 0.5 <= bench.sym_fraction(n) <= 1.0
+
+
+def test_tile_shape_is_the_librarys():
+    src = open(os.path.join(ROOT, "fsdp_buffer_layout_gb300", "csrc", "ns_gemm.cuh")).read()
+    bm = int(re.search(r"constexpr int kGemmBM = (\d+);", src).group(1))
+    bn = int(re.search(r"constexpr int kGemmBN = (\d+);", src).group(1))
+    assert (bench.GEMM_BM, bench.GEMM_BN) == (bm, bn)
+    assert bench.sym_fraction(4096) == 272 / 512
