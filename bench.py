@@ -430,9 +430,11 @@ def gpu_arm(args, rank: int, world: int):
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     dev_norms = torch.zeros(e2e_steps, 2, dtype=torch.float64, device=dev)
     host_norms = torch.empty(e2e_steps, 2, dtype=torch.float64).pin_memory()
-    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
-    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
-    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
+    # timing events double as the ordering events: ev_in[k] ends step k's
+    # copy-in, ev_done[k] its compute, ev_out[k] its copy-out
+    ev_in = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ev_done = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ev_out = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -481,6 +483,12 @@ def gpu_arm(args, rank: int, world: int):
     e_end.record(s_out)
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    # steady state: the period of copy-out completions over the second half
+    # of the run; fill: until the first copy-out finished
+    half = e2e_steps // 2
+    steady_ms = (ev_out[half].elapsed_time(ev_out[e2e_steps - 1]) / (e2e_steps - 1 - half)
+                 if e2e_steps - 1 > half else e2e_ms)
+    fill_ms = e_start.elapsed_time(ev_out[0])
     if not all(math.isfinite(x) and x > 0 for x in host_norms[:, 0].tolist()):
         raise RuntimeError("end-to-end leg: a step's norm did not reach the host")
     if world > 1:
@@ -536,7 +544,11 @@ def gpu_arm(args, rank: int, world: int):
                 "h2d_bytes_per_step": int(host_g.numel() * 2),
                 "d2h_bytes_per_step": int(host_p.numel() * 2 + 16),
                 "host_link_ms_per_step": round(link_ms, 5),
-                "frac_of_host_link_bound": round(link_ms / e2e_ms, 4)},
+                "frac_of_host_link_bound": round(link_ms / e2e_ms, 4),
+                "steps": e2e_steps, "fill_ms": round(fill_ms, 4),
+                "steady_ms_per_step": round(steady_ms, 5),
+                "steady_frac_of_host_link_bound": round(link_ms / steady_ms, 4),
+                "pipeline": "3 streams (copy-in, compute, copy-out), 2 device buffer sets"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -556,6 +568,8 @@ def muon_arm(args, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = W.get(args.workload)
+    if args.fraction < 1.0:  # a reduced case (profiling captures)
+        w = sample_workload(w, args.fraction)
     specs = [TensorSpec(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
     stream = torch.cuda.Stream(dev)
     ss = ShardStep(specs, w.m, w.g_coll, stream=stream)

@@ -2,6 +2,9 @@
 // TMA (bulk-copy) pipeline. Included by vsf_kernels.cu after adam8.cuh (same
 // element math, same results bit for bit).
 //
+// Work: cluster c takes the units list[starts[c]] .. list[starts[c+1]-1] in
+// turn (the host balances the clusters' element counts at upload).
+//
 // Structure of one CTA: warps 0..W-1 compute, the last warp (W) is the
 // producer. The producer streams fixed-size chunks of the CTA's share of
 // each block from global memory into a ring of shared-memory slots with
@@ -179,7 +182,8 @@ __device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int k, int c) {
 template <typename GT, int W>
 __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm) adam_tma_kernel(
     const __grid_constant__ TileMaps maps, const QBlock* __restrict__ qb,
-    const int32_t* __restrict__ list, const int32_t* __restrict__ ktab, int nlist, int nclusters,
+    const int32_t* __restrict__ list, const int32_t* __restrict__ ktab,
+    const int32_t* __restrict__ starts,
     const GT* __restrict__ grad, const float* __restrict__ d_factor, float* master, int8_t* mq,
     uint8_t* vq, float* m_scale, float* v_scale, uint16_t* bf, AdamConsts k, unsigned* err) {
   using Lay = TmaLayout<GT, W>;
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       const uint64_t drop = l2_policy_evict_first();
       uint32_t p = 0;  // ring positions issued so far
       bool halted = false;
-      for (int j = cid; j < nlist && !halted; j += nclusters) {
+      for (int j = starts[cid]; j < starts[cid + 1] && !halted; ++j) {
         const QBlock b = qb[list[j]];
         const int kt = ktab[j];
         int c0, c1;
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
     __shared__ float red[2][2][W][kMaxUnitTiles];
     uint32_t p = 0;
     int nb = 0;  // units done by this CTA
-    for (int j = cid; j < nlist; j += nclusters, ++nb) {
+    for (int j = starts[cid]; j < starts[cid + 1]; ++j, ++nb) {
       const int q0 = list[j];
       const QBlock b = qb[q0];
       const int kt = ktab[j];

@@ -303,6 +303,7 @@ static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
   L.small = section(sizeof(int32_t) * std::max<size_t>(1, plan->small_blocks.size()));
   L.tma = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_blocks.size()));
   L.tma_k = section(sizeof(int32_t) * std::max<size_t>(1, plan->tma_tiles.size()));
+  L.tma_start = section(sizeof(int32_t) * (kMaxCopyGrid + 1));
   L.error = section(16);
   L.spans = section(sizeof(CopySpan) * (kMaxCopyGrid + 1));
   L.partials = section(sizeof(double) * kMaxCopyGrid);

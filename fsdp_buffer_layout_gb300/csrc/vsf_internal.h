@@ -86,6 +86,7 @@ struct DeviceLayout {
   size_t qblocks = 0;                       // QBlock[n_qblocks]
   size_t big = 0, small = 0, tma = 0;       // int32 lists of block indices
   size_t tma_k = 0;                         // int32 tiles per TMA work unit
+  size_t tma_start = 0;                     // int32[kMaxCopyGrid + 1]: first unit of each cluster
   size_t error = 0;                         // uint32 device error word
   size_t spans = 0;                         // CopySpan[kMaxCopyGrid + 1]
   size_t partials = 0;                      // double[kMaxCopyGrid]

@@ -2,20 +2,27 @@
 configuration the benchmark times (ShardStep: pack -> group norm/scale ->
 8-bit AdamW -> unpack, every step of the workload's step count).
 
-What the oracle can compute at this size is checked in full; the rest is
-sampled:
+Checked on every workload:
   - every step: the group norm against the oracle's sum of squares over all
     real gradient elements (within the oracle's own summation error bound,
     n 2^-53 relative) and the scale factor bit for bit;
   - last step: copy-in bit for bit over every tensor (the packed gradient
     against the host gradients, padding still zero) and copy-out bit for bit
-    (every parameter tensor against the packed bf16 buffer);
-  - sampled quantisation blocks (first, last and random ones of every tensor,
-    plus element chunks): the oracle replays each block through every step
-    from the same seeded inputs; master, bf16 copy, codes and scales must be
-    bit-identical, and in any case within the tolerances (master 1e-6
-    relative, codes |d| <= 1 at <= 1e-4 of positions).
+    (every parameter tensor against the packed bf16 buffer).
+The optimizer state:
+  - Llama layer and DSv3 block: in full. The oracle runs every quantisation
+    block through every step (per tensor, on the tensor's real elements),
+    and the final master, m and v codes, m and v scales and bf16 copy of
+    every real element must be bit-identical (NaNs by class), and in any
+    case within the tolerances (master 1e-6 relative, codes |d| <= 1 at
+    <= 1e-4 of positions);
+  - MoE layer and 1.3B model: sampled quantisation blocks (first, last and
+    random ones of every tensor, plus element chunks) replayed by the oracle
+    through every step, under the same bar (host time: the oracle runs
+    single-threaded at about 80 M elements per second).
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -48,8 +55,19 @@ def _block_index(qb, q):
             + np.arange(nc, dtype=np.int64)[None, :]).ravel()
 
 
-@pytest.mark.parametrize("name", ["llama_layer", "moe_layer", "dsv3_block", "llama_1p3b"])
-def test_fullsize_workload(name):
+def _tensor_blocks(qb, off_o, t):
+    """The quantisation blocks of tensor t, re-based to the tensor's own
+    element 0 (so that the oracle can run them on per-tensor arrays), and
+    their indices in the whole plan's block table."""
+    ids = np.nonzero(qb["tensor"] == t)[0]
+    blocks = {k: np.ascontiguousarray(qb[k][ids]) for k in ("base", "nrows", "ncols", "stride")}
+    blocks["base"] = blocks["base"] - int(off_o[t])
+    return blocks, ids
+
+
+@pytest.mark.parametrize("name,full", [("llama_layer", True), ("moe_layer", False),
+                                       ("dsv3_block", True), ("llama_1p3b", False)])
+def test_fullsize_workload(name, full):
     from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
     w = W.get(name)
     d = oracle.Desc.from_workload(w)
@@ -75,7 +93,18 @@ def test_fullsize_workload(name):
             ss.load_master(t, torch.from_numpy(W.master_init(w, t)).to(dev))
 
         rng = np.random.default_rng(1234)
-        picks = _sample_blocks(qb, d.n, rng)
+        picks = [] if full else _sample_blocks(qb, d.n, rng)
+        hp = oracle.hparams(w)
+        tstate = []  # full mode: the oracle's state of every tensor, tensor-local
+        if full:
+            for t in range(d.n):
+                blocks, ids = _tensor_blocks(qb, off_o, t)
+                n = numels[t]
+                tstate.append(dict(blocks=blocks, ids=ids, p=W.master_init(w, t).copy(),
+                                   mq=np.zeros(n, np.int8), vq=np.zeros(n, np.uint8),
+                                   msc=np.zeros(ids.size, np.float32),
+                                   vsc=np.zeros(ids.size, np.float32),
+                                   bf=np.zeros(n, np.uint16)))
         state = {}
         for q in picks:
             t = int(qb["tensor"][q])
@@ -84,9 +113,10 @@ def test_fullsize_workload(name):
                             mq=np.zeros(idx.size, np.int8), vq=np.zeros(idx.size, np.uint8),
                             m_scale=0.0, v_scale=0.0)
 
+        pool = ThreadPoolExecutor(8)  # host work per tensor (the C calls release the GIL)
         for s in range(1, w.steps + 1):
-            for t, n in enumerate(numels):
-                W.grad(w, s, t, out=hg[starts[t]:starts[t] + n])
+            list(pool.map(lambda t: W.grad(w, s, t, out=hg[starts[t]:starts[t] + numels[t]]),
+                          range(d.n)))
             views = [hg[starts[t]:starts[t] + n] for t, n in enumerate(numels)]
             factor_o, norm_o = oracle.factor(oracle.sumsq(views), w.m, w.max_norm)
             dev_g.copy_(host_g)
@@ -105,6 +135,12 @@ def test_fullsize_workload(name):
                 g = hg[starts[t]:starts[t] + numels[t]][idx - int(off_o[t])]
                 state[q] = oracle.adam_block(np.ascontiguousarray(g), True, factor_o, state[q], s,
                                              HP)
+            # the oracle on every tensor (each call single-threaded, tensors side by side)
+            def run_tensor(t, s=s, factor=factor_o, views=views):
+                st = tstate[t]
+                oracle.adam_all(st["blocks"], np.ascontiguousarray(views[t]), factor, True,
+                                st["mq"], st["vq"], st["msc"], st["vsc"], st["p"], st["bf"], s, hp)
+            list(pool.map(run_tensor, range(len(tstate))))
 
         # copy-in over every tensor, padding untouched, and copy-out
         packed = ss.packed_grad.view(torch.int16)
@@ -117,6 +153,24 @@ def test_fullsize_workload(name):
         gaps = [(a[1], b[0]) for a, b in zip(ends, ends[1:]) if b[0] > a[1]]
         for lo, hi in gaps[:50]:
             assert not packed[lo:hi].any(), "padding written"
+
+        # full mode: every real element and every block's scales
+        msc_g, vsc_g = ss.m_scale.cpu().numpy(), ss.v_scale.cpu().numpy()
+        for t, st in enumerate(tstate):
+            o, n = ss.offsets[t], numels[t]
+            got_p = ss.master[o:o + n].cpu().numpy()
+            got_mq = ss.m_state[o:o + n].cpu().numpy()
+            got_vq = ss.v_state[o:o + n].cpu().numpy()
+            got_bf = ss.packed_bf16.view(torch.int16)[o:o + n].cpu().numpy().view(np.uint16)
+            check_master(got_p, st["p"])
+            check_codes(got_mq, st["mq"], f"m codes of tensor {t}")
+            check_codes(got_vq, st["vq"], f"v codes of tensor {t}")
+            assert bit_equal(got_p, st["p"]), f"master of tensor {t} not bit-exact"
+            assert np.array_equal(got_mq, st["mq"]), f"m codes of tensor {t} not bit-exact"
+            assert np.array_equal(got_vq, st["vq"]), f"v codes of tensor {t} not bit-exact"
+            assert bit_equal(got_bf, st["bf"], bf16=True), f"bf16 of tensor {t} not bit-exact"
+            assert bit_equal(msc_g[st["ids"]], st["msc"]), f"m scales of tensor {t}"
+            assert bit_equal(vsc_g[st["ids"]], st["vsc"]), f"v scales of tensor {t}"
 
         # sampled blocks against the oracle's replay
         for q in picks:
@@ -131,7 +185,7 @@ def test_fullsize_workload(name):
             check_codes(got_vq, want["vq"], f"v codes of block {q}")
             assert bit_equal(got_p, want["p"]), f"master of block {q} not bit-exact"
             assert np.array_equal(got_mq, want["mq"]) and np.array_equal(got_vq, want["vq"])
-            assert np.array_equal(got_bf, want["bf16"]), f"bf16 of block {q}"
+            assert bit_equal(got_bf, want["bf16"], bf16=True), f"bf16 of block {q}"
             assert float(ss.m_scale[q].item()) == want["m_scale"]
             assert float(ss.v_scale[q].item()) == want["v_scale"]
     finally:

@@ -1,7 +1,7 @@
 """Distributed Muon through the C ABI against the oracle (oracle/muon.py).
 
 Momentum is plain fp32 arithmetic: bit-exact. The orthogonalised update O
-goes through tensor-core GEMMs (bf16 operands, fp32 accumulation in an order
+goes through the library's tcgen05 products (bf16 operands, fp32 accumulation in an order
 the oracle does not reproduce; the oracle's products are exact), so a bf16
 result can round to the neighbouring value and Newton-Schulz carries such
 flips forward. Tolerance, from that arithmetic: the GPU and the oracle are
@@ -79,9 +79,12 @@ def _run(specs, m, g_coll, steps):
      ((2, 128, 256), W.GRAN_ROWS, 64, 0), ((128, 256), W.GRAN_ROWS, 128, 0), ((7,), W.GRAN_ELEM, 0, 0)],
     # 63-element matrices: offsets off the 8-element grid (scalar kernels)
     [((5, 9, 7), W.GRAN_ROWS, 5, 0), ((24, 40), W.GRAN_ROWS, 8, 0)],
-    # n >= 1024: the symmetric products by 2x2 blocks (wide, tall, batched)
+    # several 128 x 256 output tiles of the tensor-core kernel, the symmetric
+    # products on the tiles at or above the diagonal (wide, tall, batched)
     [((1024, 1536), W.GRAN_ROWS, 32, 0), ((2048, 1024), W.GRAN_ROWS, 64, 0)],
     [((2, 1024, 1024), W.GRAN_ROWS, 128, 0)],
+    # ragged tiles: n and k not multiples of the tile (wide, tall)
+    [((300, 700), W.GRAN_ROWS, 30, 0), ((1000, 136), W.GRAN_ROWS, 8, 0)],
     # more matrices of one shape than one chunk holds (192)
     [((200, 16, 32), W.GRAN_ROWS, 16, 0), ((3, 32, 16), W.GRAN_ROWS, 32, 0)],
 ])
@@ -127,14 +130,15 @@ def test_muon_output_is_orthogonal_band():
 
 
 @pytest.mark.parametrize("shape", [(256, 512), (512, 256), (3, 128, 192), (1024, 2048),
-                                   (2048, 1024), (4096, 4096)])
+                                   (2048, 1024), (4096, 4096), (520, 1000)])
 def test_muon_update_one_step(shape):
     """Step 1: the update O recovered from the master, (p0 decay - p1) / alpha,
     against the oracle's O. Both are bf16 roundings of the same exact
     Newton-Schulz iteration, so by the triangle inequality they lie within
     twice the oracle's own distance d from exact arithmetic (the oracle run
-    with exact=True), in Frobenius norm and element by element. Shapes from
-    1024 take the blocked symmetric products, 4096 x 4096 two levels of them."""
+    with exact=True), in Frobenius norm and element by element. The larger
+    shapes span many output tiles (4096 x 4096: 272 of the Gram matrix's 512
+    tiles computed, the rest mirrored)."""
     ss, state, masters = _run([(shape, W.GRAN_ROWS, 64, 0)], 2, 128, steps=1)
     try:
         n = ss.numels[0]
