@@ -348,16 +348,60 @@ vsf_status gemm_operand_map(CUtensorMap* map, const uint16_t* ptr, bool mn, int6
   return VSF_OK;
 }
 
+// Clusters of two CTAs sharing each stage's opB slice by multicast (see
+// ns_gemm.cuh); VSF_GEMM_CLUSTER=1 builds the single-CTA form for A/B timing.
+#ifndef VSF_GEMM_CLUSTER
+#define VSF_GEMM_CLUSTER 2
+#endif
+constexpr int kGemmCluster = VSF_GEMM_CLUSTER;
+
 template <bool AMN, bool BMN, bool SYM>
 vsf_status launch_ns_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const NsGemmArgs& g,
                           unsigned* err, int sms, cudaStream_t st) {
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      ns_gemm_kernel<AMN, BMN, SYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (attr != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("ns_gemm: ") + cudaGetErrorString(attr));
-  const int ntiles = g.batch * g.tiles_per_matrix;
-  ns_gemm_kernel<AMN, BMN, SYM><<<std::max(1, std::min(sms, ntiles)), kGemmThreads, kGemmSmem, st>>>(
-      ma, mb, g, err);
-  const cudaError_t e = cudaGetLastError();
+  constexpr int CL = kGemmCluster;
+  auto fn = ns_gemm_kernel<AMN, BMN, SYM, CL>;
+  // per instantiation, once: the shared memory limit and how many clusters
+  // fit on the GPU at a time (the persistent grid's size)
+  static int max_clusters = [&] {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem) !=
+        cudaSuccess)
+      return -1;
+    if (CL == 1) return sms;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+      return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL * 64);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return -1;
+    return std::max(1, n);
+  }();
+  if (max_clusters < 1) {
+    const cudaError_t e = cudaGetLastError();
+    return fail(VSF_ERR_CUDA, std::string("ns_gemm (set-up): ") + cudaGetErrorString(e));
+  }
+  const int items = g.batch * g.tiles_per_matrix;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(CL * std::max(1, std::min(max_clusters, items))));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, ma, mb, g, err);
   return e == cudaSuccess ? VSF_OK : fail(VSF_ERR_CUDA, std::string("ns_gemm: ") + cudaGetErrorString(e));
 }
 
@@ -401,17 +445,22 @@ vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t
   g.D = D;
   g.ldd = ldd;
   g.sd = sd;
-  g.mblocks = (int)((M + kGemmBM - 1) / kGemmBM);
   const int nblocks = (int)((N + kGemmBN - 1) / kGemmBN);
-  if (sym) {
-    g.tiles_per_matrix = 0;
-    for (int J = 0; J < nblocks; ++J) g.tiles_per_matrix += std::min(g.mblocks, 2 * J + 2);
-  } else {
-    g.tiles_per_matrix = g.mblocks * nblocks;
+  {
+    // work items of the tensor-core kernel: 128-row tiles, or vertical
+    // pairs of them for clusters of two; a symmetric product keeps in column
+    // block J the row blocks 0 .. 2J+1
+    const int64_t rows = (int64_t)kGemmBM * kGemmCluster;
+    g.mgroups = (int)((M + rows - 1) / rows);
+    int64_t items = 0;
+    for (int J = 0; J < nblocks; ++J)
+      items += sym ? std::min<int64_t>(g.mgroups, kGemmCluster == 1 ? 2 * J + 2 : J + 1)
+                   : g.mgroups;
+    if (items * batch >= INT32_MAX) return fail(VSF_ERR_ARG, "ns_gemm: too many tiles");
+    g.tiles_per_matrix = (int)items;
   }
   const bool tc = tma_ok(A, lda, sa) && tma_ok(B, ldb, sb) && tma_ok(D, ldd, sd) &&
-                  (beta == 0.0f || tma_ok(C, ldc, sc)) &&
-                  (int64_t)g.tiles_per_matrix * batch < INT32_MAX;
+                  (beta == 0.0f || tma_ok(C, ldc, sc));
   if (!tc) {
     if (!a_mn && !b_mn && sym) return launch_ns_gemm_simt<false, false, true>(A, lda, sa, B, ldb, sb, g, st);
     if (!a_mn && !b_mn) return launch_ns_gemm_simt<false, false, false>(A, lda, sa, B, ldb, sb, g, st);
@@ -421,7 +470,8 @@ vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t
   }
   CUtensorMap ma, mb;
   vsf_status s = gemm_operand_map(&ma, A, a_mn, M, K, lda, sa, batch, kGemmBM);
-  if (s == VSF_OK) s = gemm_operand_map(&mb, B, b_mn, N, K, ldb, sb, batch, kGemmBN);
+  // a cluster pair loads half of each opB slice per CTA
+  if (s == VSF_OK) s = gemm_operand_map(&mb, B, b_mn, N, K, ldb, sb, batch, kGemmBN / kGemmCluster);
   if (s != VSF_OK) return s;
   if (!a_mn && !b_mn && sym) return launch_ns_gemm<false, false, true>(ma, mb, g, err, sms, st);
   if (!a_mn && !b_mn) return launch_ns_gemm<false, false, false>(ma, mb, g, err, sms, st);

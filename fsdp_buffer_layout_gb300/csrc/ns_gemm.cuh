@@ -36,10 +36,18 @@
 //               nearest even, stores (and mirrored stores). The two
 //               accumulators let the epilogue of one tile overlap the MMAs
 //               of the next.
+// Clusters of two (CL = 2): the two CTAs of a cluster compute vertically
+// adjacent tiles (rows m0 and m0 + 128, the same 256 columns), so they need
+// the same opB slice every stage. Each loads its own opA slice and half of
+// the opB slice, multicast into both CTAs' shared memory: 32 KB of L2 reads
+// per CTA and stage instead of 48. A stage is refilled only when both CTAs'
+// MMAs are done with it (each MMA commit arrives on both CTAs' "empty"
+// barriers).
+//
 // Every wait is bounded (mbarrier.cuh): a broken pipeline sets bit 1 of the
-// device error word and the kernel ends; before exit the producer waits for
-// its issued copies and the MMA thread for its issued MMAs, and TMEM is
-// freed.
+// device error word and the kernel ends (a timeout also stops the cluster
+// peer); before exit the producer waits for its issued copies and the MMA
+// thread for its issued MMAs, the cluster synchronises, and TMEM is freed.
 
 constexpr int kGemmBM = 128;   // rows of an output tile (TMEM lanes)
 constexpr int kGemmBN = 256;   // columns of an output tile (TMEM columns)
@@ -62,7 +70,8 @@ struct NsGemmArgs {
   int64_t ldc, sc;
   uint16_t* D;
   int64_t ldd, sd;
-  int tiles_per_matrix, mblocks;
+  int tiles_per_matrix;  // work items per matrix: tiles (CL = 1) or vertical tile pairs (CL = 2)
+  int mgroups;           // row groups per matrix: 128-row blocks (CL = 1) or 256-row pairs
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -129,6 +138,45 @@ __device__ __forceinline__ void tma3_g2s(uint32_t dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same box written to the same shared-memory offset of every CTA in
+// cta_mask (cluster ranks), each CTA's mbarrier at `bar` receiving its bytes.
+__device__ __forceinline__ void tma3_g2s_multicast(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                   int z, uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+// tcgen05.commit arriving on the mbarrier at `bar` in every CTA of cta_mask.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Sets the stop flag at the same shared-memory offset in cluster rank `rank`.
+__device__ __forceinline__ void remote_stop(volatile uint32_t* stop, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(ra)
+               : "r"(smem_u32(const_cast<uint32_t*>(stop))), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(1u) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 // Shared-memory matrix descriptor of tcgen05 (128-byte swizzle): start
 // address, leading- and stride-dimension byte offsets (all >> 4), the fixed
 // version bits 46-48 = 0b001, swizzle mode 2 (128B) in bits 61-63.
@@ -161,28 +209,31 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 
-// Output tile t of the launch: matrix b, first row m0, first column n0. Tiles
-// run column block by column block (consecutive tiles share the opB panel);
-// a symmetric product keeps, in column block J (columns 256J .. 256J+255),
-// the row blocks 0 .. 2J+1 that reach the diagonal.
-__device__ __forceinline__ void gemm_tile(const NsGemmArgs& g, bool sym, int t, int& b, int& m0,
-                                          int& n0) {
+// Work item t of the launch: matrix b, first row m0 of this CTA's tile
+// (rank: its position in a cluster of CL vertically adjacent tiles), first
+// column n0. Items run column block by column block (consecutive items share
+// the opB panel); a symmetric product keeps, in column block J (columns
+// 256J .. 256J+255), the row blocks 0 .. 2J+1 that reach the diagonal, i.e.
+// the 128-row groups 0 .. 2J+1 (CL = 1) or the 256-row groups 0 .. J (CL = 2).
+template <int CL>
+__device__ __forceinline__ void gemm_tile(const NsGemmArgs& g, bool sym, int t, int rank, int& b,
+                                          int& m0, int& n0) {
   b = t / g.tiles_per_matrix;
   int r = t - b * g.tiles_per_matrix;
   if (!sym) {
-    const int J = r / g.mblocks;
-    m0 = (r - J * g.mblocks) * kGemmBM;
+    const int J = r / g.mgroups;
+    m0 = (r - J * g.mgroups) * (kGemmBM * CL) + rank * kGemmBM;
     n0 = J * kGemmBN;
     return;
   }
   int J = 0;
   for (;;) {
-    const int cnt = imin(g.mblocks, 2 * J + 2);
+    const int cnt = imin(g.mgroups, CL == 1 ? 2 * J + 2 : J + 1);
     if (r < cnt) break;
     r -= cnt;
     ++J;
   }
-  m0 = r * kGemmBM;
+  m0 = r * (kGemmBM * CL) + rank * kGemmBM;
   n0 = J * kGemmBN;
 }
 
@@ -191,10 +242,11 @@ __device__ __forceinline__ uint16_t bf16_rn(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-template <bool AMN, bool BMN, bool SYM>
+template <bool AMN, bool BMN, bool SYM, int CL>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const NsGemmArgs g, unsigned* err) {
+  static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   extern __shared__ __align__(1024) unsigned char gsm_raw[];
   unsigned char* sm = gsm_raw + ((1024u - (smem_u32(gsm_raw) & 1023u)) & 1023u);
   const uint32_t s0 = smem_u32(sm);
@@ -208,12 +260,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __shared__ uint32_t stop_flag;
   volatile uint32_t* stop = &stop_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CL == 1 ? 0 : (int)cluster_rank();
+  const int cid = blockIdx.x / CL, ncid = gridDim.x / CL;
+  constexpr uint16_t kBoth = (1u << CL) - 1u;  // every CTA of the cluster
 
   if (threadIdx.x == 0) {
     stop_flag = 0u;
     for (int s = 0; s < kGemmStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);  // one MMA commit from each CTA of the cluster
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar(i), 1);
@@ -227,25 +282,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (CL > 1)
+    cluster_barrier();  // the peer's barriers exist before any multicast signals them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int ntiles = g.batch * g.tiles_per_matrix;
   const int KB = (g.K + kGemmBK - 1) / kGemmBK;
+  // a timeout here also stops the cluster peer, which would otherwise keep
+  // multicasting into this CTA
+  auto halt_cluster = [&]() {
+    if (CL > 1) remote_stop(stop, (uint32_t)(rank ^ 1));
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- producer
       uint32_t it = 0;  // stages issued
       bool halted = false;
-      for (int t = blockIdx.x; t < ntiles && !halted; t += gridDim.x) {
+      for (int t = cid; t < ntiles && !halted; t += ncid) {
         int b, m0, n0;
-        gemm_tile(g, SYM, t, b, m0, n0);
+        gemm_tile<CL>(g, SYM, t, rank, b, m0, n0);
         for (int kb = 0; kb < KB; ++kb) {
           const int s = it % kGemmStages;
           const uint32_t ph = (it / kGemmStages) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, err, stop)) {
             halted = true;
+            halt_cluster();
             break;
           }
           ++it;
@@ -258,10 +322,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             tma3_g2s(a, &tmA, k0, m0, b, full_bar(s));
           }
-          if (BMN) {
-            for (int h = 0; h < 4; ++h) tma3_g2s(bb + h * 8192u, &tmB, n0 + 64 * h, k0, b, full_bar(s));
+          if (CL == 1) {
+            if (BMN) {
+              for (int h = 0; h < 4; ++h)
+                tma3_g2s(bb + h * 8192u, &tmB, n0 + 64 * h, k0, b, full_bar(s));
+            } else {
+              tma3_g2s(bb, &tmB, k0, n0, b, full_bar(s));
+            }
           } else {
-            tma3_g2s(bb, &tmB, k0, n0, b, full_bar(s));
+            // this CTA's half of the opB slice, into both CTAs
+            if (BMN) {
+              for (int h = 2 * rank; h < 2 * rank + 2; ++h)
+                tma3_g2s_multicast(bb + h * 8192u, &tmB, n0 + 64 * h, k0, b, full_bar(s), kBoth);
+            } else {
+              tma3_g2s_multicast(bb + rank * (kGemmBBytes / 2), &tmB, k0, n0 + rank * (kGemmBN / 2),
+                                 b, full_bar(s), kBoth);
+            }
           }
         }
       }
@@ -281,15 +357,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t it = 0;
       int lt = 0;
       bool halted = false;
-      for (int t = blockIdx.x; t < ntiles && !halted; t += gridDim.x, ++lt) {
+      for (int t = cid; t < ntiles && !halted; t += ncid, ++lt) {
         const int buf = lt & 1;
-        if (!mbar_wait(tempty_bar(buf), ((uint32_t)(lt >> 1) & 1u) ^ 1u, err, stop)) break;
+        if (!mbar_wait(tempty_bar(buf), ((uint32_t)(lt >> 1) & 1u) ^ 1u, err, stop)) {
+          halt_cluster();
+          break;
+        }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * kGemmBN);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % kGemmStages;
           if (!mbar_wait(full_bar(s), (it / kGemmStages) & 1u, err, stop)) {
             halted = true;
+            halt_cluster();
             break;
           }
           tc_fence_after();
@@ -298,7 +378,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
             umma_bf16(d, operand_desc<AMN>(a, kk), operand_desc<BMN>(bb, kk), idesc,
                       (kb | kk) != 0 ? 1u : 0u);
-          umma_commit(empty_bar(s));  // the stage is free once these MMAs are done
+          // the stage is free once these MMAs are done, in this CTA and (its
+          // opB half lives in both) in the peer
+          if (CL == 1)
+            umma_commit(empty_bar(s));
+          else
+            umma_commit_multicast(empty_bar(s), kBoth);
         }
         if (!halted) umma_commit(tfull_bar(buf));  // the accumulator is complete
       }
@@ -310,14 +395,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
     const int q = warp & 3;
     int lt = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+    for (int t = cid; t < ntiles; t += ncid, ++lt) {
       const int buf = lt & 1;
       const bool ok =
           __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(lt >> 1) & 1u, err, stop));
       tc_fence_after();
       if (ok) {
         int b, m0, n0;
-        gemm_tile(g, SYM, t, b, m0, n0);
+        gemm_tile<CL>(g, SYM, t, rank, b, m0, n0);
         const int i = m0 + 32 * q + lane;  // this thread's output row
         const bool row_ok = i < g.M;
         uint16_t* Db = g.D + (int64_t)b * g.sd;
@@ -388,6 +473,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a cluster leaves while its peer may still write into it
+  if (CL > 1) cluster_barrier();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
