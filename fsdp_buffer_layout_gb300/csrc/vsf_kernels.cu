@@ -755,9 +755,15 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     std::vector<int32_t> list, ks, starts(ncl + 1, 0);
     list.reserve(ntma);
     ks.reserve(ntma);
+#ifndef VSF_UNIT_ORDER
+#define VSF_UNIT_ORDER 2
+#endif
     for (int c = 0; c < ncl; ++c) {
-      std::sort(mine[c].begin(), mine[c].end());
-      for (int u : mine[c]) {
+      std::vector<int>& mc = mine[c];
+      if (VSF_UNIT_ORDER >= 1) std::sort(mc.begin(), mc.end());  // 0: largest first
+      if (VSF_UNIT_ORDER == 2 && !mc.empty())  // each cluster starts elsewhere in the tensors
+        std::rotate(mc.begin(), mc.begin() + (size_t)c * mc.size() / ncl, mc.end());
+      for (int u : mc) {
         list.push_back(plan->tma_blocks[u]);
         ks.push_back(plan->tma_tiles[u]);
       }
