@@ -81,15 +81,15 @@ def measured_bf16_peak(sustained: bool):
         return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
 
 
-GEMM_BM, GEMM_BN = 128, 256  # output tile of libvsf's Newton-Schulz kernel (rows, columns)
+GEMM_BM, GEMM_BN = 256, 256  # output tile of libvsf's Newton-Schulz kernel (one CTA pair)
 
 
 def sym_tiles(n: int) -> int:
     """Output tiles of one n x n symmetric product that libvsf computes: in
-    column block J (256 columns) the row blocks 0 .. 2J+1 (128 rows each),
-    the tiles that reach the diagonal or lie above it."""
+    column block J (256 columns) the row groups 0 .. J (256 rows each), the
+    tiles that reach the diagonal or lie above it."""
     mb, nb = -(-n // GEMM_BM), -(-n // GEMM_BN)
-    return sum(min(mb, 2 * J + 2) for J in range(nb))
+    return sum(min(mb, J + 1) for J in range(nb))
 
 
 def sym_fraction(n: int) -> float:
@@ -705,8 +705,8 @@ def muon_arm(args, rank: int, world: int):
                    "ns_flops_per_step": flops, "ns_flops_executed_per_step": flops_exec,
                    "root_load_balance": round(balance, 4),
                    "gemm": "libvsf tcgen05 kernel: bf16 x bf16 -> bf16, fp32 accumulation "
-                           "in TMEM, 128x256 tiles, symmetric products on the tiles at or "
-                           "above the diagonal",
+                           "in TMEM, 256x256 tiles per CTA pair (cta_group::2), symmetric "
+                           "products on the tiles at or above the diagonal",
                    "l2": "working set (master, momentum, Newton-Schulz buffers) larger than "
                          "L2, no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU, m virtual ranks",

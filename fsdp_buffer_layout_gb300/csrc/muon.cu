@@ -348,31 +348,22 @@ vsf_status gemm_operand_map(CUtensorMap* map, const uint16_t* ptr, bool mn, int6
   return VSF_OK;
 }
 
-// Clusters of two CTAs sharing each stage's opB slice by multicast (see
-// ns_gemm.cuh); VSF_GEMM_CLUSTER=1 builds the single-CTA form for A/B timing.
-#ifndef VSF_GEMM_CLUSTER
-#define VSF_GEMM_CLUSTER 2
-#endif
-constexpr int kGemmCluster = VSF_GEMM_CLUSTER;
-
 template <bool AMN, bool BMN, bool SYM>
 vsf_status launch_ns_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const NsGemmArgs& g,
-                          unsigned* err, int sms, cudaStream_t st) {
-  constexpr int CL = kGemmCluster;
-  auto fn = ns_gemm_kernel<AMN, BMN, SYM, CL>;
+                          unsigned* err, cudaStream_t st) {
+  constexpr int CL = 2;  // the CTA pair of one 256 x 256 tile
+  constexpr uint32_t kSmem = kGemmSmem;
+  auto fn = ns_gemm_kernel<AMN, BMN, SYM>;
   // per instantiation, once: the shared memory limit and how many clusters
   // fit on the GPU at a time (the persistent grid's size)
   static int max_clusters = [&] {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem) !=
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
         cudaSuccess)
-      return -1;
-    if (CL == 1) return sms;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
       return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL * 64);
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.dynamicSmemBytes = kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
@@ -392,7 +383,7 @@ vsf_status launch_ns_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Ns
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(CL * std::max(1, std::min(max_clusters, items))));
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -427,7 +418,7 @@ bool tma_ok(const void* p, int64_t ld, int64_t bs) {
 vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t K, int64_t batch,
                    const uint16_t* A, int64_t lda, int64_t sa, const uint16_t* B, int64_t ldb,
                    int64_t sb, float alpha, float beta, const uint16_t* C, int64_t ldc, int64_t sc,
-                   uint16_t* D, int64_t ldd, int64_t sd, unsigned* err, int sms, cudaStream_t st) {
+                   uint16_t* D, int64_t ldd, int64_t sd, unsigned* err, cudaStream_t st) {
   if (M < 1 || N < 1 || K < 1 || batch < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX ||
       batch > 65535)
     return fail(VSF_ERR_ARG, "ns_gemm: sizes out of range");
@@ -447,15 +438,14 @@ vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t
   g.sd = sd;
   const int nblocks = (int)((N + kGemmBN - 1) / kGemmBN);
   {
-    // work items of the tensor-core kernel: 128-row tiles, or vertical
-    // pairs of them for clusters of two; a symmetric product keeps in column
-    // block J the row blocks 0 .. 2J+1
-    const int64_t rows = (int64_t)kGemmBM * kGemmCluster;
+    // work items of the tensor-core kernel: 256 x 256 output tiles (one per
+    // CTA pair); a symmetric product keeps in column block J the 256-row
+    // groups 0 .. J
+    const int64_t rows = 2 * (int64_t)kGemmBM;
     g.mgroups = (int)((M + rows - 1) / rows);
     int64_t items = 0;
     for (int J = 0; J < nblocks; ++J)
-      items += sym ? std::min<int64_t>(g.mgroups, kGemmCluster == 1 ? 2 * J + 2 : J + 1)
-                   : g.mgroups;
+      items += sym ? std::min<int64_t>(g.mgroups, J + 1) : g.mgroups;
     if (items * batch >= INT32_MAX) return fail(VSF_ERR_ARG, "ns_gemm: too many tiles");
     g.tiles_per_matrix = (int)items;
   }
@@ -471,12 +461,13 @@ vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t
   CUtensorMap ma, mb;
   vsf_status s = gemm_operand_map(&ma, A, a_mn, M, K, lda, sa, batch, kGemmBM);
   // a cluster pair loads half of each opB slice per CTA
-  if (s == VSF_OK) s = gemm_operand_map(&mb, B, b_mn, N, K, ldb, sb, batch, kGemmBN / kGemmCluster);
+  // each CTA of the pair loads its own 128 rows of opA and of opB
+  if (s == VSF_OK) s = gemm_operand_map(&mb, B, b_mn, N, K, ldb, sb, batch, kGemmBN / 2);
   if (s != VSF_OK) return s;
-  if (!a_mn && !b_mn && sym) return launch_ns_gemm<false, false, true>(ma, mb, g, err, sms, st);
-  if (!a_mn && !b_mn) return launch_ns_gemm<false, false, false>(ma, mb, g, err, sms, st);
-  if (a_mn && b_mn && sym) return launch_ns_gemm<true, true, true>(ma, mb, g, err, sms, st);
-  if (!a_mn && b_mn && !sym) return launch_ns_gemm<false, true, false>(ma, mb, g, err, sms, st);
+  if (!a_mn && !b_mn && sym) return launch_ns_gemm<false, false, true>(ma, mb, g, err, st);
+  if (!a_mn && !b_mn) return launch_ns_gemm<false, false, false>(ma, mb, g, err, st);
+  if (a_mn && b_mn && sym) return launch_ns_gemm<true, true, true>(ma, mb, g, err, st);
+  if (!a_mn && b_mn && !sym) return launch_ns_gemm<false, true, false>(ma, mb, g, err, st);
   return fail(VSF_ERR_ARG, "ns_gemm: unsupported operand layout");
 }
 
@@ -501,12 +492,8 @@ vsf_status vsf_ns_gemm(int32_t a_mn, int32_t b_mn, int32_t sym, int64_t M, int64
     return fail(VSF_ERR_ARG, "vsf_ns_gemm: bad leading dimension or batch stride");
   if (!((a_mn == 0 && b_mn == 0) || (a_mn && b_mn && sym) || (a_mn == 0 && b_mn && !sym)))
     return fail(VSF_ERR_ARG, "vsf_ns_gemm: operand layouts must be K/K, MN/MN (symmetric) or K/MN");
-  int dev = -1, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_ns_gemm: ") + cudaGetErrorString(e));
   return ns_gemm(a_mn != 0, b_mn != 0, sym != 0, M, N, K, batch, A, lda, sa, B, ldb, sb, alpha,
-                 beta, C, ldc, sc, D, ldd, sd, d_err, sms, static_cast<cudaStream_t>(stream));
+                 beta, C, ldc, sc, D, ldd, sd, d_err, static_cast<cudaStream_t>(stream));
 }
 
 vsf_status vsf_muon_select_roots(const vsf_plan* plan, int32_t* root, double* load_balance) {
@@ -580,10 +567,6 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
   uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
   unsigned* err = reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error);
-  int dev = -1, sms = 0;
-  cudaError_t de = cudaGetDevice(&dev);
-  if (de == cudaSuccess) de = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (de != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(de));
   const float mu = (float)hp->momentum;
   const float decay = (float)(1.0 - hp->lr * hp->weight_decay);
   const float na = (float)hp->ns_a, nb = (float)hp->ns_b, nc = (float)hp->ns_c;
@@ -624,20 +607,20 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
       vsf_status s = VSF_OK;
       if (!tall)
         s = ns_gemm(false, false, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
-                    nullptr, n, sa, A, n, sa, err, sms, st);
+                    nullptr, n, sa, A, n, sa, err, st);
       else
         s = ns_gemm(true, true, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
-                    nullptr, n, sa, A, n, sa, err, sms, st);
+                    nullptr, n, sa, A, n, sa, err, st);
       if (s == VSF_OK)
         s = ns_gemm(false, false, true, n, n, n, c.batch, A, n, sa, A, n, sa, nc, nb, A, n, sa, B,
-                    n, sa, err, sms, st);
+                    n, sa, err, st);
       if (s == VSF_OK) {
         if (!tall)  // X'[i][l] = a X[i][l] + sum_j B[i][j] X[j][l]
           s = ns_gemm(false, true, false, n, c.C, n, c.batch, B, n, sa, X, c.C, sx, 1.0f, na, X,
-                      c.C, sx, Xn, c.C, sx, err, sms, st);
+                      c.C, sx, Xn, c.C, sx, err, st);
         else        // X'[l][i] = a X[l][i] + sum_j X[l][j] B[i][j]
           s = ns_gemm(false, false, false, c.R, n, n, c.batch, X, c.C, sx, B, n, sa, 1.0f, na, X,
-                      c.C, sx, Xn, c.C, sx, err, sms, st);
+                      c.C, sx, Xn, c.C, sx, err, st);
       }
       if (s != VSF_OK) return s;
       std::swap(X, Xn);

@@ -21,41 +21,47 @@
 // i <= j to D[i][j] and D[j][i]; elements below the diagonal are never
 // written directly, so D comes out exactly symmetric.
 //
-// CTA structure (persistent: one CTA per SM, tiles round-robin):
-//   warp 0      TMA producer: 64-element K slices of both operands into a
-//               4-stage ring of 48 KB stages (128-byte swizzle), each stage
-//               guarded by a "full" mbarrier (transaction bytes) and an
-//               "empty" mbarrier (arrived by the MMAs' commit);
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
-//               accumulators); one thread issues tcgen05.mma (M = 128,
-//               N = 256, K = 16 per instruction) and commits each stage back
-//               to the producer and each finished accumulator to the
-//               epilogue;
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter of the
-//               accumulator, alpha * acc + beta * C in fp32, bf16 round to
-//               nearest even, stores (and mirrored stores). The two
-//               accumulators let the epilogue of one tile overlap the MMAs
-//               of the next.
-// Clusters of two (CL = 2): the two CTAs of a cluster compute vertically
-// adjacent tiles (rows m0 and m0 + 128, the same 256 columns), so they need
-// the same opB slice every stage. Each loads its own opA slice and half of
-// the opB slice, multicast into both CTAs' shared memory: 32 KB of L2 reads
-// per CTA and stage instead of 48. A stage is refilled only when both CTAs'
-// MMAs are done with it (each MMA commit arrives on both CTAs' "empty"
-// barriers).
+// Pair MMA: the two CTAs of a cluster compute one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256 across the pair, N = 256, K = 16). Each
+// CTA stages only its own 128 rows of opA and its own 128 rows of opB per
+// 64-element K slice (32 KB), so each SM's shared memory serves half of the
+// opB reads and a 6-stage ring fits. (A single-SM 128 x 256 tile needs 48 KB
+// per slice, written by the copies and read by the tensor core, about 190
+// bytes per clock through one SM's shared memory at the tensor rate; measured,
+// it kept the tensor pipe 74-79% busy and ran 8-20% slower.) Each CTA's
+// accumulator, its 128 rows x 256 columns, lives in its own TMEM.
 //
+// CTA structure (persistent: one cluster per SM pair, tiles round-robin):
+//   warp 0      TMA producer, in both CTAs: this CTA's opA and opB rows of
+//               each K slice (128-byte swizzle); the copies of both CTAs
+//               signal the leader's "full" barrier (.cta_group::2 copies),
+//               on which the leader posts the pair's byte count;
+//   warp 1      allocates 512 TMEM columns (two accumulators) in both CTAs;
+//               one thread of the leader (cluster rank 0) issues every MMA
+//               and commits each stage to both CTAs' "empty" barriers and
+//               each finished accumulator to both CTAs' "accumulator full"
+//               barriers (multicast);
+//   warps 2..5  epilogue, in both CTAs: tcgen05.ld of their 32-lane quarter
+//               of this CTA's accumulator, alpha * acc + beta * C in fp32,
+//               bf16 round to nearest even, stores (and mirrored stores);
+//               then an arrival on the leader's "accumulator empty" barrier.
+//               The two accumulators let the epilogue of one tile overlap
+//               the MMAs of the next.
 // Every wait is bounded (mbarrier.cuh): a broken pipeline sets bit 1 of the
-// device error word and the kernel ends (a timeout also stops the cluster
-// peer); before exit the producer waits for its issued copies and the MMA
-// thread for its issued MMAs, the cluster synchronises, and TMEM is freed.
+// device error word and stops both CTAs of the pair; the leader waits for
+// the pair's copies and its MMAs before exit, and the pair synchronises
+// before TMEM is freed. A pair whose two TMEM allocations differ in address
+// (the leader's MMAs write both at the leader's) sets bit 3 and computes
+// nothing.
 
-constexpr int kGemmBM = 128;   // rows of an output tile (TMEM lanes)
+constexpr int kGemmBM = 128;   // rows of a CTA's half of the output tile (TMEM lanes)
 constexpr int kGemmBN = 256;   // columns of an output tile (TMEM columns)
 constexpr int kGemmBK = 64;    // K elements per stage: one 128-byte swizzle row
-constexpr int kGemmStages = 4;
-constexpr uint32_t kGemmABytes = kGemmBM * kGemmBK * 2;  // 16 KB
-constexpr uint32_t kGemmBBytes = kGemmBN * kGemmBK * 2;  // 32 KB
+constexpr int kGemmStages = 6;
+constexpr uint32_t kGemmABytes = kGemmBM * kGemmBK * 2;        // 16 KB: this CTA's opA rows
+constexpr uint32_t kGemmBBytes = (kGemmBN / 2) * kGemmBK * 2;  // 16 KB: this CTA's opB rows
 constexpr uint32_t kGemmStageBytes = kGemmABytes + kGemmBBytes;
+constexpr uint32_t kGemmTmemCols = 2 * kGemmBN;               // two fp32 accumulators
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kGemmBarBytes = 8 * (2 * kGemmStages + 5);
 // +1024: the kernel rounds the dynamic shared memory base up to 1024 bytes
@@ -70,22 +76,24 @@ struct NsGemmArgs {
   int64_t ldc, sc;
   uint16_t* D;
   int64_t ldd, sd;
-  int tiles_per_matrix;  // work items per matrix: tiles (CL = 1) or vertical tile pairs (CL = 2)
-  int mgroups;           // row groups per matrix: 128-row blocks (CL = 1) or 256-row pairs
+  int tiles_per_matrix;  // 256 x 256 output tiles per matrix
+  int mgroups;           // 256-row groups per matrix
 };
 
 // ---------------------------------------------------------------- PTX wrappers
 
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+// TMEM allocation of the CTA pair: one warp of each CTA executes it, and the
+// pair gets `ncols` columns at the same address in both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
                : "memory");
 }
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -95,22 +103,25 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D (TMEM) (+)= A (shared) * B (shared)^T, kind::f16 (bf16 here), one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D (both CTAs' TMEM) (+)= A (both CTAs' shared memory) * B^T, kind::f16
+// (bf16 here), issued by one thread of the leader CTA.
+__device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// The mbarrier receives one arrival once every tcgen05 operation this thread
-// issued before has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// The mbarrier at `bar` in every CTA of cta_mask receives one arrival once
+// every pair MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_pair_commit(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -128,43 +139,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 3-D tensor copy (global -> shared) of one box at (x, y, z), completing on bar.
-__device__ __forceinline__ void tma3_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                         uint32_t bar) {
+// 3-D tensor copy (global -> this CTA's shared memory) of one box at
+// (x, y, z), completing on an mbarrier of either CTA of the pair (bar: a
+// shared::cluster address).
+__device__ __forceinline__ void tma3_g2s_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                              int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
-}
-
-// The same box written to the same shared-memory offset of every CTA in
-// cta_mask (cluster ranks), each CTA's mbarrier at `bar` receiving its bytes.
-__device__ __forceinline__ void tma3_g2s_multicast(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                                   int z, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-// tcgen05.commit arriving on the mbarrier at `bar` in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Sets the stop flag at the same shared-memory offset in cluster rank `rank`.
-__device__ __forceinline__ void remote_stop(volatile uint32_t* stop, uint32_t rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(ra)
-               : "r"(smem_u32(const_cast<uint32_t*>(stop))), "r"(rank));
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(1u) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -175,6 +159,29 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+// The shared::cluster address of the same offset in cluster rank `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+// Sets the stop flag at the same shared-memory offset in cluster rank `rank`.
+__device__ __forceinline__ void remote_stop(volatile uint32_t* stop, uint32_t rank) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(
+                   peer_addr(smem_u32(const_cast<uint32_t*>(stop)), rank)),
+               "r"(1u)
+               : "memory");
+}
+// Arrival on an mbarrier of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 // Shared-memory matrix descriptor of tcgen05 (128-byte swizzle): start
@@ -193,14 +200,15 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(bool a_mn, bool b_mn, int
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// Operand layouts in a stage (both from 128-byte-swizzled tensor copies):
-//   K-major, R rows x 64 K: row r at r * 128 bytes; 8-row groups 1024 bytes
+// Operand layouts in a stage (both from 128-byte-swizzled tensor copies of
+// this CTA's 128 rows):
+//   K-major, 128 rows x 64 K: row r at r * 128 bytes; 8-row groups 1024 bytes
 //     apart (stride offset); one MMA's 16 K elements are 32 bytes of each
 //     row, so K step kk starts kk * 32 bytes in.
-//   MN-major, 64 K rows x R: boxes of 64 MN elements x 64 K rows, 8 KB each,
-//     side by side (leading offset 8192 between 64-element MN groups); K row
-//     k at k * 128 bytes in its box, 8-row groups 1024 bytes apart; K step kk
-//     starts kk * 16 rows = kk * 2048 bytes in.
+//   MN-major, 64 K rows x 128: two boxes of 64 MN elements x 64 K rows, 8 KB
+//     each, side by side (leading offset 8192 between 64-element MN groups);
+//     K row k at k * 128 bytes in its box, 8-row groups 1024 bytes apart; K
+//     step kk starts kk * 16 rows = kk * 2048 bytes in.
 template <bool kMN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
   return kMN ? umma_smem_desc(base + kk * 2048u, 8192u, 1024u)
@@ -209,31 +217,29 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 
-// Work item t of the launch: matrix b, first row m0 of this CTA's tile
-// (rank: its position in a cluster of CL vertically adjacent tiles), first
+// Work item t of the launch: matrix b, and the 256 x 256 output tile whose
+// 128-row half this CTA (cluster rank `rank`) holds: first row m0, first
 // column n0. Items run column block by column block (consecutive items share
 // the opB panel); a symmetric product keeps, in column block J (columns
-// 256J .. 256J+255), the row blocks 0 .. 2J+1 that reach the diagonal, i.e.
-// the 128-row groups 0 .. 2J+1 (CL = 1) or the 256-row groups 0 .. J (CL = 2).
-template <int CL>
+// 256J .. 256J+255), the 256-row groups 0 .. J that reach the diagonal.
 __device__ __forceinline__ void gemm_tile(const NsGemmArgs& g, bool sym, int t, int rank, int& b,
                                           int& m0, int& n0) {
   b = t / g.tiles_per_matrix;
   int r = t - b * g.tiles_per_matrix;
   if (!sym) {
     const int J = r / g.mgroups;
-    m0 = (r - J * g.mgroups) * (kGemmBM * CL) + rank * kGemmBM;
+    m0 = (r - J * g.mgroups) * (2 * kGemmBM) + rank * kGemmBM;
     n0 = J * kGemmBN;
     return;
   }
   int J = 0;
   for (;;) {
-    const int cnt = imin(g.mgroups, CL == 1 ? 2 * J + 2 : J + 1);
+    const int cnt = imin(g.mgroups, J + 1);
     if (r < cnt) break;
     r -= cnt;
     ++J;
   }
-  m0 = r * (kGemmBM * CL) + rank * kGemmBM;
+  m0 = r * (2 * kGemmBM) + rank * kGemmBM;
   n0 = J * kGemmBN;
 }
 
@@ -242,11 +248,10 @@ __device__ __forceinline__ uint16_t bf16_rn(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-template <bool AMN, bool BMN, bool SYM, int CL>
+template <bool AMN, bool BMN, bool SYM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const NsGemmArgs g, unsigned* err) {
-  static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   extern __shared__ __align__(1024) unsigned char gsm_raw[];
   unsigned char* sm = gsm_raw + ((1024u - (smem_u32(gsm_raw) & 1023u)) & 1023u);
   const uint32_t s0 = smem_u32(sm);
@@ -260,50 +265,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __shared__ uint32_t stop_flag;
   volatile uint32_t* stop = &stop_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = CL == 1 ? 0 : (int)cluster_rank();
-  const int cid = blockIdx.x / CL, ncid = gridDim.x / CL;
-  constexpr uint16_t kBoth = (1u << CL) - 1u;  // every CTA of the cluster
+  const int rank = (int)cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x / 2, ncid = gridDim.x / 2;
+  constexpr uint16_t kBoth = 3;
 
   if (threadIdx.x == 0) {
     stop_flag = 0u;
     for (int s = 0; s < kGemmStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);  // one MMA commit from each CTA of the cluster
+      mbar_init(full_bar(s), 1);   // the leader's producer posts both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // the leader's MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), 4);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(i), 8);  // every epilogue warp of both CTAs (leader's barrier)
     }
     mbar_init(done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tmem_slot), kGemmTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  if (CL > 1)
-    cluster_barrier();  // the peer's barriers exist before any multicast signals them
-  else
-    __syncthreads();
+  cluster_barrier();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // the leader's MMAs write both CTAs' accumulators at the leader's address
+  if (threadIdx.x == 0 && ld_peer_u32(peer_addr(smem_u32(&tmem_slot), (uint32_t)(rank ^ 1))) != tmem) {
+    atomicOr(err, 8u);
+    stop_flag = 1u;
+    remote_stop(stop, (uint32_t)(rank ^ 1));
+  }
+  cluster_barrier();
   const int ntiles = g.batch * g.tiles_per_matrix;
   const int KB = (g.K + kGemmBK - 1) / kGemmBK;
-  // a timeout here also stops the cluster peer, which would otherwise keep
-  // multicasting into this CTA
-  auto halt_cluster = [&]() {
-    if (CL > 1) remote_stop(stop, (uint32_t)(rank ^ 1));
-  };
+  const uint32_t leader_full0 = peer_addr(full_bar(0), 0);
+  const uint32_t leader_tempty0 = peer_addr(tempty_bar(0), 0);
+  auto halt_cluster = [&]() { remote_stop(stop, (uint32_t)(rank ^ 1)); };
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- producer
-      uint32_t it = 0;  // stages issued
+    if (lane == 0 && *stop == 0u) {
+      // ---------------- producer (both CTAs): this CTA's opA and opB rows
+      uint32_t it = 0;
       bool halted = false;
       for (int t = cid; t < ntiles && !halted; t += ncid) {
         int b, m0, n0;
-        gemm_tile<CL>(g, SYM, t, rank, b, m0, n0);
+        gemm_tile(g, SYM, t, rank, b, m0, n0);
+        const int nb0 = n0 + rank * (kGemmBN / 2);  // this CTA's opB rows
         for (int kb = 0; kb < KB; ++kb) {
           const int s = it % kGemmStages;
           const uint32_t ph = (it / kGemmStages) & 1u;
@@ -313,53 +322,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           ++it;
-          mbar_expect_tx(full_bar(s), kGemmStageBytes);
+          const uint32_t fb = leader_full0 + 8u * s;  // the leader's full barrier
+          if (leader) mbar_expect_tx(full_bar(s), 2 * kGemmStageBytes);
           const uint32_t a = s0 + s * kGemmStageBytes, bb = a + kGemmABytes;
           const int k0 = kb * kGemmBK;
           if (AMN) {
-            tma3_g2s(a, &tmA, m0, k0, b, full_bar(s));
-            tma3_g2s(a + 8192u, &tmA, m0 + 64, k0, b, full_bar(s));
+            tma3_g2s_pair(a, &tmA, m0, k0, b, fb);
+            tma3_g2s_pair(a + 8192u, &tmA, m0 + 64, k0, b, fb);
           } else {
-            tma3_g2s(a, &tmA, k0, m0, b, full_bar(s));
+            tma3_g2s_pair(a, &tmA, k0, m0, b, fb);
           }
-          if (CL == 1) {
-            if (BMN) {
-              for (int h = 0; h < 4; ++h)
-                tma3_g2s(bb + h * 8192u, &tmB, n0 + 64 * h, k0, b, full_bar(s));
-            } else {
-              tma3_g2s(bb, &tmB, k0, n0, b, full_bar(s));
-            }
+          if (BMN) {
+            tma3_g2s_pair(bb, &tmB, nb0, k0, b, fb);
+            tma3_g2s_pair(bb + 8192u, &tmB, nb0 + 64, k0, b, fb);
           } else {
-            // this CTA's half of the opB slice, into both CTAs
-            if (BMN) {
-              for (int h = 2 * rank; h < 2 * rank + 2; ++h)
-                tma3_g2s_multicast(bb + h * 8192u, &tmB, n0 + 64 * h, k0, b, full_bar(s), kBoth);
-            } else {
-              tma3_g2s_multicast(bb + rank * (kGemmBBytes / 2), &tmB, k0, n0 + rank * (kGemmBN / 2),
-                                 b, full_bar(s), kBoth);
-            }
+            tma3_g2s_pair(bb, &tmB, k0, nb0, b, fb);
           }
         }
       }
-      // every issued copy lands before the CTA exits (one limit in all)
-      const uint64_t deadline = global_ns() + kWaitNs;
-      for (int s = 0; s < kGemmStages; ++s) {
-        if (it > (uint32_t)s) {
-          const uint32_t last = (it - 1 - s) / kGemmStages * kGemmStages + s;
-          mbar_drain(full_bar(s), (last / kGemmStages) & 1u, deadline, err);
+      // the leader sees every copy of both CTAs land; the follower's copies
+      // are covered by the leader's wait and the final cluster barrier
+      if (leader) {
+        const uint64_t deadline = global_ns() + kWaitNs;
+        for (int s = 0; s < kGemmStages; ++s) {
+          if (it > (uint32_t)s) {
+            const uint32_t last = (it - 1 - s) / kGemmStages * kGemmStages + s;
+            mbar_drain(full_bar(s), (last / kGemmStages) & 1u, deadline, err);
+          }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      constexpr uint32_t idesc = umma_idesc_bf16(AMN, BMN, kGemmBM, kGemmBN);
+    if (lane == 0 && leader && *stop == 0u) {
+      // ---------------- MMA issuer (leader only)
+      constexpr uint32_t idesc = umma_idesc_bf16(AMN, BMN, 2 * kGemmBM, kGemmBN);
       uint32_t it = 0;
       int lt = 0;
       bool halted = false;
       for (int t = cid; t < ntiles && !halted; t += ncid, ++lt) {
         const int buf = lt & 1;
-        if (!mbar_wait(tempty_bar(buf), ((uint32_t)(lt >> 1) & 1u) ^ 1u, err, stop)) {
+        const uint32_t tph = ((uint32_t)(lt >> 1) & 1u) ^ 1u;
+        if (!mbar_wait_cluster(tempty_bar(buf), tph, err, stop)) {
           halt_cluster();
           break;
         }
@@ -376,34 +379,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a = s0 + s * kGemmStageBytes, bb = a + kGemmABytes;
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            umma_bf16(d, operand_desc<AMN>(a, kk), operand_desc<BMN>(bb, kk), idesc,
-                      (kb | kk) != 0 ? 1u : 0u);
-          // the stage is free once these MMAs are done, in this CTA and (its
-          // opB half lives in both) in the peer
-          if (CL == 1)
-            umma_commit(empty_bar(s));
-          else
-            umma_commit_multicast(empty_bar(s), kBoth);
+            umma_pair_bf16(d, operand_desc<AMN>(a, kk), operand_desc<BMN>(bb, kk), idesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+          umma_pair_commit(empty_bar(s), kBoth);  // both CTAs may refill the stage
         }
-        if (!halted) umma_commit(tfull_bar(buf));  // the accumulator is complete
+        if (!halted) umma_pair_commit(tfull_bar(buf), kBoth);
       }
-      // every issued MMA completes before TMEM is freed
-      umma_commit(done_bar);
+      umma_pair_commit(done_bar, 1);  // this CTA only
       mbar_drain(done_bar, 0u, global_ns() + kWaitNs, err);
     }
   } else {
-    // ---------------- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+    // ---------------- epilogue (both CTAs): this CTA's 128 rows
     const int q = warp & 3;
     int lt = 0;
     for (int t = cid; t < ntiles; t += ncid, ++lt) {
       const int buf = lt & 1;
-      const bool ok =
-          __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(lt >> 1) & 1u, err, stop));
+      const uint32_t fph = (uint32_t)(lt >> 1) & 1u;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), fph, err, stop));
       tc_fence_after();
       if (ok) {
         int b, m0, n0;
-        gemm_tile<CL>(g, SYM, t, rank, b, m0, n0);
-        const int i = m0 + 32 * q + lane;  // this thread's output row
+        gemm_tile(g, SYM, t, rank, b, m0, n0);
+        const int i = m0 + 32 * q + lane;
         const bool row_ok = i < g.M;
         uint16_t* Db = g.D + (int64_t)b * g.sd;
         const uint16_t* Cb = g.beta != 0.0f ? g.C + (int64_t)b * g.sc : nullptr;
@@ -411,10 +408,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c = 0; c < kGemmBN / 32; ++c) {
           const int j0 = n0 + 32 * c;
           uint32_t r[32];
-          __syncwarp();  // tcgen05.ld is warp-collective: reconverge after a lane's `continue`
+          __syncwarp();
           tmem_ld32(tmem + (uint32_t)(buf * kGemmBN + 32 * c) + ((uint32_t)(32 * q) << 16), r);
           if (!row_ok || j0 >= g.N) continue;
-          if (SYM && j0 + 31 < i) continue;  // the whole chunk lies below the diagonal
+          if (SYM && j0 + 31 < i) continue;
           const bool full = j0 + 32 <= g.N;
           float v[32];
 #pragma unroll
@@ -457,7 +454,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               if (j0 + x < g.N && (!SYM || j0 + x >= i)) drow[x] = bf16_rn(v[x]);
           }
           if (SYM) {
-            // mirror: D[j][i] for j > i (lanes write consecutive i: coalesced)
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
               const int j = j0 + x;
@@ -468,18 +464,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8u * buf);
     }
   }
   tc_fence_before();
   __syncthreads();
-  // neither CTA of a cluster leaves while its peer may still write into it
-  if (CL > 1) cluster_barrier();
+  cluster_barrier();  // no CTA frees TMEM or leaves while the pair's MMAs or copies may touch it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, kGemmTmemCols);
   }
 }
+
 
 // Plain CUDA-core GEMM of the same contract for operands the tensor copies
 // cannot address (a leading dimension or batch stride that is not a
@@ -510,3 +506,4 @@ __global__ void __launch_bounds__(256) ns_gemm_simt_kernel(const uint16_t* __res
   Db[(int64_t)i * g.ldd + j] = bf16_rn(v);
   if (SYM && i != j) Db[(int64_t)j * g.ldd + i] = bf16_rn(v);
 }
+

@@ -682,7 +682,11 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
       if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (shared memory size)");
     }
     const TmaLaunch<uint16_t> tl = tma_launch<uint16_t>(plan->tma_warps);
+#ifdef VSF_TMA_CLUSTER_FORCE
+    for (int cand = VSF_TMA_CLUSTER_FORCE; cand <= VSF_TMA_CLUSTER_FORCE; ++cand) {
+#else
     for (int cand = 1; cand <= kMaxCluster; cand *= 2) {
+#endif
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cand * 64);
       cfg.blockDim = dim3(tl.threads);

@@ -5,9 +5,10 @@ Algorithmic bytes per real element of the shard step (bf16 gradients): pack
 plus 16 bytes of scales per quantisation block, unpack 2 + 2: 24 in all. With
 fp32 gradients pack moves 8 and AdamW 18 (30 in all); in zero-copy mode the
 step is the norm's read of the packed gradient plus AdamW (18). Muon's
-executed share of a symmetric product: the 128 x 256 output tiles of the
-library's tensor-core kernel that hold an element on or above the diagonal
-(checked by brute force), with the tile shape the library's own.
+executed share of a symmetric product: the 256 x 256 output tiles (one per
+CTA pair) of the library's tensor-core kernel that hold an element on or
+above the diagonal (checked by brute force), with the tile shape the
+library's own.
 """
 import os
 import re
@@ -29,7 +30,7 @@ def test_algorithmic_bytes_per_element(grad_bytes, zero_copy, per_elem):
     assert b["adam"] == (grad_bytes + 14) * N + 16 * Q
 
 
-def _sym_tiles_brute(n, bm=128, bn=256):
+def _sym_tiles_brute(n, bm=256, bn=256):
     """Tiles of an n x n output (bm x bn) that hold an element (i, j) with i <= j."""
     count = 0
     for I in range(-(-n // bm)):
@@ -48,7 +49,8 @@ def test_symmetric_tiles_are_those_touching_the_upper_triangle(n):
 
 def test_tile_shape_is_the_librarys():
     src = open(os.path.join(ROOT, "fsdp_buffer_layout_gb300", "csrc", "ns_gemm.cuh")).read()
-    bm = int(re.search(r"constexpr int kGemmBM = (\d+);", src).group(1))
+    # kGemmBM is one CTA's half of the pair's tile
+    bm = 2 * int(re.search(r"constexpr int kGemmBM = (\d+);", src).group(1))
     bn = int(re.search(r"constexpr int kGemmBN = (\d+);", src).group(1))
     assert (bench.GEMM_BM, bench.GEMM_BN) == (bm, bn)
-    assert bench.sym_fraction(4096) == 272 / 512
+    assert bench.sym_fraction(4096) == 136 / 256
