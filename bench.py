@@ -426,7 +426,9 @@ def gpu_arm(args, rank: int, world: int):
     # copy is queued on the compute stream (a device-to-host copy there would
     # wait for the previous step's copy-out in the copy engine and serialise
     # the pipeline).
-    e2e_steps = max(3, min(args.steps, 100))
+    # at least 40 steps, so that the pipeline's fill (one copy-in and one
+    # compute before the first copy-out) is a small part of the figure
+    e2e_steps = max(40, min(args.steps, 100))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     dev_norms = torch.zeros(e2e_steps, 2, dtype=torch.float64, device=dev)
     host_norms = torch.empty(e2e_steps, 2, dtype=torch.float64).pin_memory()
@@ -933,7 +935,16 @@ def muon_cpu_baseline(w, threads: int | None = None):
 # fewer blocks) summarised in profiles/adam8_tma_*.md. The line's `traffic`
 # is this ratio times the full launch's algorithmic bytes. A workload without
 # a capture of the current kernel has no entry (traffic null).
-TRAFFIC: dict = {}
+TRAFFIC: dict = {
+    "llama_1p3b": dict(ratio=1.0048, capture="llama_1p3b cut to 0.1 of its rows: 2.0854 GB "
+                       "DRAM for 2.0754 GB algorithmic, one launch (profiles/adam8_tma_traffic.md)"),
+    "llama_layer": dict(ratio=0.9867, capture="llama_layer cut to 0.5 of its rows: 1.5976 GB "
+                        "for 1.6191 GB, one launch (profiles/adam8_tma_traffic.md)"),
+    "moe_layer": dict(ratio=1.1157, capture="moe_layer cut to 0.15 of its rows: 2.1323 GB for "
+                      "1.9113 GB, one launch (profiles/adam8_tma_traffic.md)"),
+    "dsv3_block": dict(ratio=1.0525, capture="dsv3_block cut to 0.5 of its rows: 2.2251 GB for "
+                       "2.1142 GB, one launch (profiles/adam8_tma_traffic.md)"),
+}
 
 
 def reference_arm(args):
