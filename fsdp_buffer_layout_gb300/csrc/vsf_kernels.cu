@@ -682,11 +682,7 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
       if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (shared memory size)");
     }
     const TmaLaunch<uint16_t> tl = tma_launch<uint16_t>(plan->tma_warps);
-#ifdef VSF_TMA_CLUSTER_FORCE
-    for (int cand = VSF_TMA_CLUSTER_FORCE; cand <= VSF_TMA_CLUSTER_FORCE; ++cand) {
-#else
     for (int cand = 1; cand <= kMaxCluster; cand *= 2) {
-#endif
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cand * 64);
       cfg.blockDim = dim3(tl.threads);
@@ -759,13 +755,10 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
     std::vector<int32_t> list, ks, starts(ncl + 1, 0);
     list.reserve(ntma);
     ks.reserve(ntma);
-#ifndef VSF_UNIT_ORDER
-#define VSF_UNIT_ORDER 2
-#endif
     for (int c = 0; c < ncl; ++c) {
       std::vector<int>& mc = mine[c];
-      if (VSF_UNIT_ORDER >= 1) std::sort(mc.begin(), mc.end());  // 0: largest first
-      if (VSF_UNIT_ORDER == 2 && !mc.empty())  // each cluster starts elsewhere in the tensors
+      std::sort(mc.begin(), mc.end());  // tensor order ...
+      if (!mc.empty())                  // ... from a point of its own
         std::rotate(mc.begin(), mc.begin() + (size_t)c * mc.size() / ncl, mc.end());
       for (int u : mc) {
         list.push_back(plan->tma_blocks[u]);
