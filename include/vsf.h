@@ -318,12 +318,15 @@ vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, con
  *     p = p (1 - lr wd) - fp32(lr sqrt(max(1, R/C))) X;  bf16 copy.
  *   packed_grad: bf16, m*S; momentum: fp32, m*S (caller-zeroed before step
  *   1); master: fp32; packed_bf16: out. d_workspace: vsf_muon_workspace_bytes
- *   of caller memory (Newton-Schulz operands and the cuBLASLt workspace).
- *   Matrices of one shape, across tensors, run batched: vsf_muon_chunk_count
- *   gives the number of batches (each: 3 own kernels and 3 * ns_steps
- *   cuBLASLt GEMMs); 0 for a NULL plan. Errors: VSF_ERR_ARG (NULL, small
- *   workspace, ns_steps < 0), VSF_ERR_ALIGN (a pointer not 16-byte aligned),
- *   VSF_ERR_STATE (plan not uploaded), VSF_ERR_CUDA (launch or cuBLASLt).
+ *   of caller memory (the Newton-Schulz operands X, X', A, B of the largest
+ *   batch and the norm partials). The products run on the library's tcgen05
+ *   kernel (vsf_ns_gemm below); its bounded waits report through the plan's
+ *   device error word. Matrices of one shape, across tensors, run batched:
+ *   vsf_muon_chunk_count gives the number of batches (each: 3 element-wise
+ *   kernels and 3 * ns_steps products); 0 for a NULL plan. Errors:
+ *   VSF_ERR_ARG (NULL, small workspace, ns_steps < 0), VSF_ERR_ALIGN (a
+ *   pointer not 16-byte aligned), VSF_ERR_STATE (plan not uploaded),
+ *   VSF_ERR_CUDA (a launch or a tensor-map encoding failed).
  *   Argument errors are found before the first launch (buffers untouched);
  *   after VSF_ERR_CUDA, chunks before the failing one have been updated and
  *   the step's momentum, master and bf16 buffers are undefined. */
