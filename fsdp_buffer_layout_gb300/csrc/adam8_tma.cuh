@@ -144,16 +144,19 @@ struct TmaChunk {
 __device__ __forceinline__ int tma_width(const QBlock& b, int k) { return b.ncols * k; }
 template <int CH>
 __device__ __forceinline__ int tma_rows_per_chunk(const QBlock& b, int k) {
-  return CH / tma_width(b, k);
+  // a tile unit's width is a power of two (k tiles of a power-of-two width,
+  // one 256-column copy box): a shift, not a division, in every chunk
+  return CH >> (31 - __clz(tma_width(b, k)));
 }
 
 // Chunks [c0, c1) of a unit that CTA `crank` of CL owns.
 template <int CH>
 __device__ __forceinline__ void tma_share(const QBlock& b, int k, int CL, int crank, int& c0,
                                           int& c1) {
+  // rows per chunk and the cluster size are powers of two: shifts
   const int rpc = b.nrows == 1 ? 1 : tma_rows_per_chunk<CH>(b, k);
-  const int nch = b.nrows == 1 ? (b.ncols + CH - 1) / CH : (b.nrows + rpc - 1) / rpc;
-  const int per = (nch + CL - 1) / CL;
+  const int nch = b.nrows == 1 ? (b.ncols + CH - 1) / CH : (b.nrows + rpc - 1) >> (31 - __clz(rpc));
+  const int per = (nch + CL - 1) >> (31 - __clz(CL));
   c0 = min(nch, crank * per);
   c1 = min(nch, c0 + per);
 }
@@ -319,7 +322,8 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       // in one tile of the unit: tt (0 for a contiguous block).
       const int gpr = b.nrows == 1 ? 32 : tma_width(b, kt) >> 3;  // groups per row (<= 32)
       const int gpt = b.nrows == 1 ? 32 : b.ncols >> 3;           // groups per tile
-      const int tt = b.nrows == 1 ? 0 : (tid % gpr) / gpt;
+      const int gpt_log2 = 31 - __clz(gpt);  // gpr and gpt are powers of two
+      const int tt = b.nrows == 1 ? 0 : (tid & (gpr - 1)) >> gpt_log2;
       const int q = q0 + tt;
       c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
       c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
@@ -363,9 +367,9 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
           vx = fmaxf(vx, __shfl_xor_sync(0xffffffffu, vx, o));
         }
       }
-      if (lane < gpr && lane % gpt == 0) {
-        red[par][0][warp][lane / gpt] = mx;
-        red[par][1][warp][lane / gpt] = vx;
+      if (lane < gpr && (lane & (gpt - 1)) == 0) {
+        red[par][0][warp][lane >> gpt_log2] = mx;
+        red[par][1][warp][lane >> gpt_log2] = vx;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
       if (warp == 0) {
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       }
       c.im = f2(sm > 0.0f ? __fdiv_rn(127.0f, sm) : 0.0f);
       c.iv = f2(sv > 0.0f ? __fdiv_rn(255.0f, sv) : 0.0f);
-      if (crank == 0 && tid < kt * gpt && tid % gpt == 0 && *stop == 0u) {  // one thread per tile
+      if (crank == 0 && tid < kt * gpt && (tid & (gpt - 1)) == 0 && *stop == 0u) {  // one thread per tile
         m_scale[q] = sm;
         v_scale[q] = sv;
       }
