@@ -354,9 +354,18 @@ vsf_status launch_ns_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Ns
   constexpr int CL = 2;  // the CTA pair of one 256 x 256 tile
   constexpr uint32_t kSmem = kGemmSmem;
   auto fn = ns_gemm_kernel<AMN, BMN, SYM>;
-  // per instantiation, once: the shared memory limit and how many clusters
-  // fit on the GPU at a time (the persistent grid's size)
-  static int max_clusters = [&] {
+  // per instantiation and device, once: the shared memory limit and how many
+  // clusters fit on the GPU at a time (the persistent grid's size)
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(VSF_ERR_CUDA, std::string("ns_gemm: device ") +
+                                  (de != cudaSuccess ? cudaGetErrorString(de) : "id out of range"));
+  static std::mutex mu;
+  static int cached[64] = {};  // 0: not looked up yet
+  std::lock_guard<std::mutex> lock(mu);
+  int& max_clusters = cached[dev];
+  if (max_clusters == 0) max_clusters = [&] {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
         cudaSuccess)
       return -1;
@@ -376,6 +385,7 @@ vsf_status launch_ns_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Ns
     return std::max(1, n);
   }();
   if (max_clusters < 1) {
+    max_clusters = 0;  // look up again next time
     const cudaError_t e = cudaGetLastError();
     return fail(VSF_ERR_CUDA, std::string("ns_gemm (set-up): ") + cudaGetErrorString(e));
   }
