@@ -46,6 +46,8 @@ template <int W>
 struct TmaShape {
   static constexpr int threads = (W + 1) * 32;
   static constexpr int chunk = tma_chunk_elems(W);
+  // rows per chunk of a tile unit (chunk / 256 columns) are taken with a shift
+  static_assert((chunk & (chunk - 1)) == 0, "chunk sizes are powers of two");
   static constexpr int ctas_per_sm = kTmaWideWarps / W;
   static constexpr uint32_t ring_bytes = 200u * 1024u / ctas_per_sm;
 };
