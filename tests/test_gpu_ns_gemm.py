@@ -52,6 +52,7 @@ def _run(a_mn, b_mn, sym, M, N, K, batch, alpha, beta, seed, ld_pad=0, same=Fals
                   D[0].numel(), err.data_ptr(), torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, "a bounded wait of the GEMM ran out"
+    assert torch.isnan(D.float()[..., N:]).all(), "wrote into the leading-dimension padding"
     got = D.float().cpu()[..., :N].double()
     opA = _op(Ab.double()[..., :a_shape[1]], a_mn)
     opB = _op(Bb.double()[..., :b_shape[1]], b_mn)
@@ -126,15 +127,31 @@ def test_update_tall_k_by_k(M, N, K, batch):
     _run(False, False, False, M, N, K, batch, 1.0, 3.4445, seed=M + 5 * N)
 
 
-@pytest.mark.parametrize("layout", [(False, False, True), (False, False, False),
-                                    (True, True, True), (False, True, False)])
+LAYOUTS = [(False, False, True), (False, False, False), (True, True, True), (False, True, False)]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
 def test_unaligned_leading_dimension_takes_the_cuda_core_kernel(layout):
-    """Leading dimensions that are not multiples of 8 cannot be addressed by
-    the tensor copies; the CUDA-core kernel has the same contract."""
+    """Leading dimensions that are not multiples of 8 (K + 5 = 34, M + 5 = 50,
+    N + 5 = 42) cannot be addressed by the tensor copies; the CUDA-core kernel
+    has the same contract."""
     a_mn, b_mn, sym = layout
     M = 45
     N = M if sym else 37
-    _run(a_mn, b_mn, sym, M, N, 29, 2, 1.0, 0.0 if sym else -0.5, seed=3, ld_pad=3, same=sym)
+    for ld in (29 + 5, M + 5, N + 5):
+        assert ld % 8 != 0
+    _run(a_mn, b_mn, sym, M, N, 29, 2, 1.0, 0.0 if sym else -0.5, seed=3, ld_pad=5, same=sym)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_padded_leading_dimension_on_the_tensor_cores(layout):
+    """Rows padded beyond the matrix (K + 3 = 32, M + 3 = 48, N + 3 = 40: still
+    multiples of 8): the tensor copies read only the logical extent, and
+    nothing past it is written."""
+    a_mn, b_mn, sym = layout
+    M = 45
+    N = M if sym else 37
+    _run(a_mn, b_mn, sym, M, N, 29, 2, 1.0, 0.0 if sym else -0.5, seed=4, ld_pad=3, same=sym)
 
 
 def test_alpha_scales_the_product():
