@@ -541,7 +541,7 @@ def gpu_arm(args, rank: int, world: int):
                    "inputs": "fresh gradients each step: two seeded sets (steps 1 and 2) "
                              "alternate, on the device and in pinned host memory",
                    "plan_seconds": round(ss.info.plan_seconds, 6),
-                   "bulk_warps": ss.info.bulk_warps},
+                   "bulk_warps": ss.info.bulk_warps, "bulk_cluster": ss.info.bulk_cluster},
         "roofline": {"bound": "hbm", "achieved": round(adam_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(adam_gbs / peak, 4),
                      "frac_of_copy_ceiling": round(adam_gbs / ceiling["gbs"], 4),

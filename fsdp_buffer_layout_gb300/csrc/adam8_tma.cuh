@@ -158,25 +158,47 @@ __device__ __forceinline__ int tma_rows_per_chunk(const QBlock& b, int k) {
   return CH >> (31 - __clz(tma_width(b, k)));
 }
 
-// Chunks [c0, c1) of a unit that CTA `crank` of CL owns.
+// The part of a unit that CTA `crank` of CL owns: chunks [c0, c1). A
+// contiguous block is split into CL element ranges [e0, e1) of equal length
+// to 16 elements (its length is a multiple of 16, so every range starts on a
+// 16-byte boundary of the code arrays), each cut into CH-element chunks from
+// its start, the last one short; the CTAs then move the same bytes. A tile
+// unit is split by whole chunks of rows.
+struct TmaShare {
+  int c0, c1;
+  int e0, e1;  // element range inside a contiguous block
+};
+
 template <int CH>
-__device__ __forceinline__ void tma_share(const QBlock& b, int k, int CL, int crank, int& c0,
-                                          int& c1) {
+__device__ __forceinline__ TmaShare tma_share(const QBlock& b, int k, int CL, int crank) {
   // rows per chunk and the cluster size are powers of two: shifts
-  const int rpc = b.nrows == 1 ? 1 : tma_rows_per_chunk<CH>(b, k);
-  const int nch = b.nrows == 1 ? (b.ncols + CH - 1) / CH : (b.nrows + rpc - 1) >> (31 - __clz(rpc));
-  const int per = (nch + CL - 1) >> (31 - __clz(CL));
-  c0 = min(nch, crank * per);
-  c1 = min(nch, c0 + per);
+  const int cl_log2 = 31 - __clz(CL);
+  TmaShare sh;
+  if (b.nrows == 1) {
+    const int64_t n16 = b.ncols >> 4;
+    sh.e0 = (int)(((n16 * crank) >> cl_log2) << 4);
+    sh.e1 = (int)(((n16 * (crank + 1)) >> cl_log2) << 4);
+    sh.c0 = 0;
+    sh.c1 = (sh.e1 - sh.e0 + CH - 1) / CH;
+  } else {
+    const int rpc = tma_rows_per_chunk<CH>(b, k);
+    const int nch = (b.nrows + rpc - 1) >> (31 - __clz(rpc));
+    const int per = (nch + CL - 1) >> cl_log2;
+    sh.c0 = min(nch, crank * per);
+    sh.c1 = min(nch, sh.c0 + per);
+    sh.e0 = sh.e1 = 0;
+  }
+  return sh;
 }
 
 template <int CH>
-__device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int k, int c) {
+__device__ __forceinline__ TmaChunk tma_chunk(const QBlock& b, int k, const TmaShare& sh, int c) {
   TmaChunk ch;
   if (b.nrows == 1) {
-    ch.gstart = b.base + (int64_t)c * CH;
+    const int e = sh.e0 + c * CH;
+    ch.gstart = b.base + e;
     ch.rows = 1;
-    ch.row_len = (int)min64(CH, (int64_t)b.ncols - (int64_t)c * CH);
+    ch.row_len = min(CH, sh.e1 - e);
     ch.stride = 0;
     ch.row_log2 = 0;
   } else {
@@ -248,8 +270,8 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       for (int j = starts[cid]; j < starts[cid + 1] && !halted; ++j) {
         const QBlock b = qb[list[j]];
         const int kt = ktab[j];
-        int c0, c1;
-        tma_share<CH>(b, kt, CL, crank, c0, c1);
+        const TmaShare sh = tma_share<CH>(b, kt, CL, crank);
+        const int c0 = sh.c0, c1 = sh.c1;
         int mi = 0;
         if (b.tx >= 0)
           while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
@@ -261,8 +283,8 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
             // ring chunk = chunks c .. c + n - 1 of the share (n = 2 for a
             // phase-1 pair), adjacent in the buffer or boxes packed in order
             const int n = min(step, c1 - c);
-            const TmaChunk ch = tma_chunk<CH>(b, kt, c);
-            const TmaChunk cl = n == 2 ? tma_chunk<CH>(b, kt, c + 1) : ch;
+            const TmaChunk ch = tma_chunk<CH>(b, kt, sh, c);
+            const TmaChunk cl = n == 2 ? tma_chunk<CH>(b, kt, sh, c + 1) : ch;
             const uint32_t len0 = (uint32_t)ch.len();
             const uint32_t len = len0 + (n == 2 ? (uint32_t)cl.len() : 0u);
             // the slot is free once every consumer warp has used its last
@@ -343,8 +365,8 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       const int q = q0 + tt;
       c.dm = f2(__fdiv_rn(m_scale[q], 127.0f));
       c.dv = f2(__fdiv_rn(v_scale[q], 255.0f));
-      int c0, c1;
-      tma_share<CH>(b, kt, CL, crank, c0, c1);
+      const TmaShare sh = tma_share<CH>(b, kt, CL, crank);
+      const int c0 = sh.c0, c1 = sh.c1;
       const int par = nb & 1;
       // the block maxima of every CTA of the cluster (8 bytes per tile) will
       // land on this barrier
@@ -358,8 +380,8 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
         // every lane saw the data arrive
         const bool got = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err, stop));
         if (!got) continue;
-        int len = tma_chunk<CH>(b, kt, ci).len();
-        if (Lay::p1 == 2 && ci + 1 < c1) len += tma_chunk<CH>(b, kt, ci + 1).len();
+        int len = tma_chunk<CH>(b, kt, sh, ci).len();
+        if (Lay::p1 == 2 && ci + 1 < c1) len += tma_chunk<CH>(b, kt, sh, ci + 1).len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll
         for (int gi = 0; gi < Lay::p1 * kTmaGroups; ++gi) {
@@ -436,7 +458,7 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
         const int s = p % kTmaSlots;
         const bool got = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (p / kTmaSlots) & 1, err, stop));
         if (!got) continue;
-        const TmaChunk ch = tma_chunk<CH>(b, kt, ci);
+        const TmaChunk ch = tma_chunk<CH>(b, kt, sh, ci);
         const int len = ch.len();
         const unsigned char* sl = smem + s * Lay::slot;
 #pragma unroll

@@ -174,6 +174,7 @@ static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
   plan->small_blocks.clear();
   plan->max_big_elems = 0;
   plan->max_tma_elems = 0;
+  double tma_sum = 0.0, tma_sumsq = 0.0;
   std::vector<TensorInfo>& ts = plan->tensors;
   int64_t real = 0;
   for (TensorInfo& x : ts) {
@@ -244,7 +245,10 @@ static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
       } else if (dest == kTma || dest == kTmaTile) {
         plan->tma_blocks.push_back(q);
         plan->tma_tiles.push_back(dest == kTmaTile ? (int32_t)k : 1);
-        plan->max_tma_elems = std::max(plan->max_tma_elems, nr * nc * (dest == kTmaTile ? k : 1));
+        const int64_t unit = nr * nc * (dest == kTmaTile ? k : 1);
+        plan->max_tma_elems = std::max(plan->max_tma_elems, unit);
+        tma_sum += (double)unit;
+        tma_sumsq += (double)unit * (double)unit;
       } else if (dest == kRegister) {
         plan->big_blocks.push_back(q);
         plan->max_big_elems = std::max(plan->max_big_elems, nr * nc);
@@ -283,6 +287,7 @@ static vsf_status build_tables_for(vsf_plan* plan, int32_t r0, int32_t r1) {
     }
   }
 
+  plan->tma_unit_mean = tma_sum > 0.0 ? tma_sumsq / tma_sum : 0.0;
   const vsf_status checked = check_tables(*plan);
   if (checked != VSF_OK) return checked;
 
@@ -466,6 +471,7 @@ vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info) {
   info->n_element_chunks = (int64_t)plan->small_blocks.size();
   info->rank_begin = plan->rank_begin;
   info->rank_end = plan->rank_end;
+  info->bulk_cluster = plan->uploaded ? plan->tma_cluster : 0;
   return VSF_OK;
 }
 

@@ -112,6 +112,9 @@ struct vsf_plan {
   std::vector<int32_t> small_blocks;  // ELEM chunks: warp kernel
   int64_t max_big_elems = 0;
   int64_t max_tma_elems = 0;
+  // element-weighted mean unit size of the TMA units: sum n^2 / sum n (the
+  // size of the unit an average element belongs to)
+  double tma_unit_mean = 0.0;
   int tma_warps = vsf::kTmaWideWarps;  // shape of the bulk-copy kernel (consumer warps)
   int forced_warps = 0;                // vsf_plan_set_bulk_warps: 0 = the planner's choice
   vsf::DeviceLayout layout;

@@ -670,7 +670,15 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   }
 
   // Bulk-copy kernel: 16 / warps CTAs per SM (their rings take ~200 KB of
-  // shared memory together); the cluster size follows the same L2 budget.
+  // shared memory together). Its cluster size: the smallest power of two for
+  // which the phase-1 bytes of the units in flight (one unit per cluster,
+  // 4 B per element) stay within its own L2 budget, with units counted at
+  // their element-weighted mean size (the size of the unit an average
+  // element belongs to), as the clusters work through units of every size.
+#ifndef VSF_BULK_L2_BUDGET_MB
+#define VSF_BULK_L2_BUDGET_MB 100
+#endif
+  const double tma_budget = VSF_BULK_L2_BUDGET_MB * 1024.0 * 1024.0;
   int tma_CL = 1, tma_ncl = 1;
   {
     for (int w : {kTmaWideWarps, kTmaNarrowWarps}) {
@@ -699,7 +707,7 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
       if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload (bulk-copy clusters)");
       tma_CL = cand;
       tma_ncl = std::max(1, active);
-      if ((double)tma_ncl * (double)plan->max_tma_elems * 4.0 <= budget) break;
+      if ((double)tma_ncl * plan->tma_unit_mean * 4.0 <= tma_budget) break;
     }
   }
 

@@ -75,6 +75,7 @@ class ShardStep:
             self.sumsq = torch.zeros(2, dtype=torch.float64, device=dev)
             V.vsf_plan_upload(self.plan, self.workspace.data_ptr(), self.workspace.numel(),
                               self.stream.cuda_stream)
+        self.info = V.vsf_plan_get_info(self.plan)  # now with the upload's choices
 
     def close(self):
         if self.plan:

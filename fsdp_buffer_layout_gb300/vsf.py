@@ -45,7 +45,8 @@ class vsf_plan_info(ctypes.Structure):
                 ("order_used", ctypes.c_int32), ("bulk_warps", ctypes.c_int32),
                 ("n_bulk_units", ctypes.c_int64), ("n_register_blocks", ctypes.c_int64),
                 ("n_element_chunks", ctypes.c_int64), ("rank_begin", ctypes.c_int32),
-                ("rank_end", ctypes.c_int32)]
+                ("rank_end", ctypes.c_int32), ("bulk_cluster", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class vsf_muon_hparams(ctypes.Structure):

@@ -106,6 +106,10 @@ typedef struct {
    * register kernel (ragged or unaligned), element-granular chunks */
   int64_t n_bulk_units, n_register_blocks, n_element_chunks;
   int32_t rank_begin, rank_end; /* the plan's rank window (0, m unless restricted) */
+  int32_t bulk_cluster;  /* CTAs per thread-block cluster of the bulk-copy AdamW
+                          * kernel (1, 2, 4 or 8), chosen by vsf_plan_upload
+                          * from the units' sizes and the GPU; 0 before upload */
+  int32_t reserved;      /* 0 */
 } vsf_plan_info;
 
 typedef struct vsf_plan vsf_plan; /* opaque */

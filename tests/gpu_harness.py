@@ -127,7 +127,7 @@ def run_gpu(case: Case):
                    v_scale=host(ss.v_scale)[:ss.info.n_qblocks],
                    packed_bf16=host(ss.packed_bf16).view(np.uint16),
                    params=[host(p).view(np.uint16) for p in params], factors=factors,
-                   norms=norms)
+                   norms=norms, bulk_cluster=int(ss.info.bulk_cluster))
         if case.grad_dtype == 0:
             out["packed_grad"] = out["packed_grad"].view(np.uint16)
         return out

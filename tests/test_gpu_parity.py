@@ -128,6 +128,22 @@ def test_large_blocks_use_clusters():
     compare(case, run_gpu(case), run_oracle(case))
 
 
+@pytest.mark.parametrize("shape,block_rows,want", [
+    ((512, 2880), 128, 4),   # 368,640-element blocks (MoE expert stripes): 4 equal shares
+    ((508, 2896), 127, 4),   # 367,792 = 16 * 22,987: shares of unequal 16-element counts
+    ((256, 7168), 128, 8),   # 917,504-element blocks
+])
+def test_large_units_use_clusters_of_four_and_eight(shape, block_rows, want):
+    """Units whose phase-1 bytes would overflow the L2 budget in clusters of 2
+    go to clusters of 4 or 8, each CTA taking an equal element range (to 16
+    elements) of every unit; bit-exact like every other path."""
+    specs = [(shape, W.GRAN_ROWS, block_rows, 0), ((4096,), W.GRAN_ELEM, 0, 0)]
+    case = _normal_case(specs, m=4, g=128, steps=3)
+    g = run_gpu(case)
+    assert g["bulk_cluster"] == want, f"clusters of {g['bulk_cluster']}"
+    compare(case, g, run_oracle(case))
+
+
 def test_large_blocks_fp32_gradients():
     """fp32 gradients on large blocks: the bulk-copy ring then holds 2 slots
     of 80 KB instead of 3 of 64 KB, with clusters of 2 for the 352K-element
