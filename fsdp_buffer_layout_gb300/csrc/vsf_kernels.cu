@@ -672,11 +672,16 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   // Bulk-copy kernel: 16 / warps CTAs per SM (their rings take ~200 KB of
   // shared memory together). Its cluster size: the smallest power of two for
   // which the phase-1 bytes of the units in flight (one unit per cluster,
-  // 4 B per element) stay within its own L2 budget, with units counted at
-  // their element-weighted mean size (the size of the unit an average
-  // element belongs to), as the clusters work through units of every size.
+  // 4 B per element) stay within half the L2, with units counted at their
+  // element-weighted mean size (the size of the unit an average element
+  // belongs to), as the clusters work through units of every size. Measured
+  // on the four large workloads: 53-56 MB in flight kept every phase-2
+  // re-read in L2 or close to it; 80 MB (DSv3 block in clusters of 1) and
+  // 110 MB (Llama layer in clusters of 1, MoE layer in clusters of 2) ran
+  // 1.5-10% slower than the next cluster size up, and a cluster size beyond
+  // the first that fits lost again (shorter shares, wider exchange).
 #ifndef VSF_BULK_L2_BUDGET_MB
-#define VSF_BULK_L2_BUDGET_MB 100
+#define VSF_BULK_L2_BUDGET_MB 64
 #endif
   const double tma_budget = VSF_BULK_L2_BUDGET_MB * 1024.0 * 1024.0;
   int tma_CL = 1, tma_ncl = 1;
