@@ -30,8 +30,9 @@
 // absmax before any code can be written. One thread-block cluster takes one
 // block at a time; each CTA of the cluster owns an equal share. Phase 1 reads
 // gradient and codes (4 B per element for bf16 gradients, with an L2
-// evict-last hint), computes the new moments and their maxima; the CTAs swap
-// maxima through distributed shared memory and one cluster barrier; phase 2
+// evict-last hint), computes the new moments and their maxima; the CTAs of a
+// cluster swap maxima through distributed shared memory (a CTA on its own
+// keeps them in its shared memory); phase 2
 // re-reads the same share (an L2 hit: at most clusters x block bytes were
 // read in between), reads the master once, and writes master, bf16 copy and
 // codes with evict-first hints. HBM sees every byte once.
