@@ -282,17 +282,65 @@ int muon_per(int64_t batch, int64_t mat) {
   return (int)std::max<int64_t>(1, std::min(want, most));
 }
 
+// The chunks run on kMuonLanes stream lanes: lane 0 on the caller's stream,
+// the others on the plan's own streams, forked from and joined back into the
+// caller's stream. The chunks of different shapes are independent, so one
+// lane's launches fill the SMs that another's last partial round of tiles
+// (and its element-wise kernels) leave idle. Chunks go to the lane with the
+// fewest Newton-Schulz FLOPs so far, largest first, and keep their order
+// within a lane; each lane has its own workspace. Measured Muon steps (same
+// box): four lanes against two took 2% off the MoE layer (4 batches) and the
+// 1.3B model (8), and moved the Llama layer (3) and DSv3 block (2) within 1%;
+// two lanes against one took 2-7% off every workload.
+#ifndef VSF_MUON_LANES
+#define VSF_MUON_LANES 4
+#endif
+constexpr int kMuonLanes = VSF_MUON_LANES;
+static_assert(kMuonLanes >= 1 && kMuonLanes <= 8, "1 to 8 stream lanes");
+
+std::vector<int> muon_lane_of(const std::vector<MuonChunk>& chunks) {
+  std::vector<int> order(chunks.size()), lane(chunks.size(), 0);
+  std::vector<double> fl(chunks.size());
+  for (size_t i = 0; i < chunks.size(); ++i) {
+    order[i] = (int)i;
+    MuonMatrix mm;
+    mm.tensor = 0;
+    mm.batch = chunks[i].batch;
+    mm.R = chunks[i].R;
+    mm.C = chunks[i].C;
+    fl[i] = ns_flops(mm);
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return fl[a] > fl[b]; });
+  double load[kMuonLanes] = {};
+  for (int i : order) {
+    int l = 0;
+    for (int j = 1; j < kMuonLanes; ++j)
+      if (load[j] < load[l]) l = j;
+    lane[(size_t)i] = l;
+    load[l] += fl[(size_t)i];
+  }
+  return lane;
+}
+
+struct MuonLaneLayout {
+  size_t partials = 0, x = 0, xn = 0, a = 0, b = 0;
+};
 struct MuonLayout {
-  size_t partials = 0, x = 0, xn = 0, a = 0, b = 0, bytes = 0;
+  MuonLaneLayout lane[kMuonLanes];
+  size_t bytes = 0;
 };
 
 MuonLayout muon_layout(const vsf_plan* plan) {
-  int64_t max_elems = 0, max_sq = 0, max_part = 0;
-  for (const MuonChunk& c : muon_chunks(plan)) {
+  const std::vector<MuonChunk> chunks = muon_chunks(plan);
+  const std::vector<int> lane_of = muon_lane_of(chunks);
+  int64_t max_elems[kMuonLanes] = {}, max_sq[kMuonLanes] = {}, max_part[kMuonLanes] = {};
+  for (size_t i = 0; i < chunks.size(); ++i) {
+    const MuonChunk& c = chunks[i];
+    const int l = lane_of[i];
     const int64_t n = std::min(c.R, c.C);
-    max_elems = std::max(max_elems, c.batch * c.R * c.C);
-    max_sq = std::max(max_sq, c.batch * n * n);
-    max_part = std::max(max_part, c.batch * muon_per(c.batch, c.R * c.C));
+    max_elems[l] = std::max(max_elems[l], c.batch * c.R * c.C);
+    max_sq[l] = std::max(max_sq[l], c.batch * n * n);
+    max_part[l] = std::max(max_part[l], c.batch * muon_per(c.batch, c.R * c.C));
   }
   MuonLayout L;
   size_t cur = 0;
@@ -301,13 +349,35 @@ MuonLayout muon_layout(const vsf_plan* plan) {
     cur = at + bytes;
     return at;
   };
-  L.partials = section(sizeof(double) * std::max<int64_t>(1, max_part));
-  L.x = section(2 * std::max<int64_t>(1, max_elems));
-  L.xn = section(2 * std::max<int64_t>(1, max_elems));
-  L.a = section(2 * std::max<int64_t>(1, max_sq));
-  L.b = section(2 * std::max<int64_t>(1, max_sq));
+  for (int l = 0; l < kMuonLanes; ++l) {
+    L.lane[l].partials = section(sizeof(double) * std::max<int64_t>(1, max_part[l]));
+    L.lane[l].x = section(2 * std::max<int64_t>(1, max_elems[l]));
+    L.lane[l].xn = section(2 * std::max<int64_t>(1, max_elems[l]));
+    L.lane[l].a = section(2 * std::max<int64_t>(1, max_sq[l]));
+    L.lane[l].b = section(2 * std::max<int64_t>(1, max_sq[l]));
+  }
   L.bytes = (cur + 255) / 256 * 256;
   return L;
+}
+
+// The plan's lanes beyond the caller's stream: a non-blocking stream and a
+// join event each, and the fork event.
+struct MuonLanes {
+  int device = -1;
+  cudaStream_t stream[kMuonLanes] = {};  // [0] unused: the caller's stream
+  cudaEvent_t join[kMuonLanes] = {};
+  cudaEvent_t fork = nullptr;
+};
+
+void muon_lanes_free(void* p) {
+  MuonLanes* ml = static_cast<MuonLanes*>(p);
+  if (ml == nullptr) return;
+  if (ml->fork) cudaEventDestroy(ml->fork);
+  for (int l = 1; l < kMuonLanes; ++l) {
+    if (ml->join[l]) cudaEventDestroy(ml->join[l]);
+    if (ml->stream[l]) cudaStreamDestroy(ml->stream[l]);
+  }
+  delete ml;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -482,6 +552,29 @@ vsf_status ns_gemm(bool a_mn, bool b_mn, bool sym, int64_t M, int64_t N, int64_t
 }
 
 }  // namespace
+
+vsf_status muon_lanes_create(vsf_plan* plan) {
+  MuonLanes* have = static_cast<MuonLanes*>(plan->muon_lanes);
+  if (have != nullptr && have->device == plan->device) return VSF_OK;
+  if (plan->muon_lanes_free != nullptr) plan->muon_lanes_free(plan->muon_lanes);
+  plan->muon_lanes = nullptr;
+  plan->muon_lanes_free = nullptr;
+  MuonLanes* ml = new MuonLanes();
+  ml->device = plan->device;
+  cudaError_t e = cudaEventCreateWithFlags(&ml->fork, cudaEventDisableTiming);
+  for (int l = 1; l < kMuonLanes && e == cudaSuccess; ++l) {
+    e = cudaStreamCreateWithFlags(&ml->stream[l], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ml->join[l], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    muon_lanes_free(ml);
+    return fail(VSF_ERR_CUDA, std::string("vsf_plan_upload (Muon stream): ") + cudaGetErrorString(e));
+  }
+  plan->muon_lanes = ml;
+  plan->muon_lanes_free = muon_lanes_free;
+  return VSF_OK;
+}
+
 }  // namespace vsf
 
 using namespace vsf;
@@ -569,83 +662,121 @@ vsf_status vsf_muon_step(const vsf_plan* plan, const uint16_t* packed_grad, floa
     if (reinterpret_cast<uintptr_t>(p) & 15)
       return fail(VSF_ERR_ALIGN, "vsf_muon_step: pointer not 16-byte aligned");
   if (hp->ns_steps < 0) return fail(VSF_ERR_ARG, "vsf_muon_step: ns_steps must be >= 0");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const MuonLanes* ml = static_cast<const MuonLanes*>(plan->muon_lanes);
+  if (ml == nullptr) return fail(VSF_ERR_STATE, "vsf_muon_step: plan has no Muon stream");
+  const std::vector<MuonChunk> chunks = muon_chunks(plan);
+  const std::vector<int> lane_of = muon_lane_of(chunks);
+  bool used[kMuonLanes] = {};
+  for (int l : lane_of) used[l] = true;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  cudaStream_t lanes[kMuonLanes];
+  bool forked = false;
+  for (int l = 0; l < kMuonLanes; ++l) {
+    lanes[l] = l == 0 ? caller : ml->stream[l];
+    forked = forked || (l > 0 && used[l]);
+  }
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
-  double* partials = reinterpret_cast<double*>(ws + L.partials);
-  uint16_t* X = reinterpret_cast<uint16_t*>(ws + L.x);
-  uint16_t* Xn = reinterpret_cast<uint16_t*>(ws + L.xn);
-  uint16_t* A = reinterpret_cast<uint16_t*>(ws + L.a);
-  uint16_t* B = reinterpret_cast<uint16_t*>(ws + L.b);
   unsigned* err = reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error);
   const float mu = (float)hp->momentum;
   const float decay = (float)(1.0 - hp->lr * hp->weight_decay);
   const float na = (float)hp->ns_a, nb = (float)hp->ns_b, nc = (float)hp->ns_c;
   const Bounds bd{plan->total, reinterpret_cast<unsigned*>(plan->d_ws + plan->layout.error)};
 
-  for (const MuonChunk& c : muon_chunks(plan)) {
-    MatTable tab;
-    for (int64_t j = 0; j < c.batch; ++j) tab.off[j] = c.off[(size_t)j];
-    const int64_t mat = c.R * c.C;
-    const int per = muon_per(c.batch, mat);
-    const dim3 grid((unsigned)per, (unsigned)c.batch);
-    // 8-wide accesses when every matrix of the chunk starts on 8 elements
-    bool vec = mat % 8 == 0;
-    for (int64_t j = 0; j < c.batch; ++j) vec = vec && c.off[(size_t)j] % 8 == 0;
-    if (vec) {
-      muon_momentum_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                             partials, bd);
-      muon_normalize_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                              partials, hp->eps, X, bd);
-    } else {
-      muon_momentum_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                             partials, bd);
-      muon_normalize_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
-                                                              partials, hp->eps, X, bd);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
-    // Newton-Schulz on the row-major R x C matrices of the chunk (X holds
-    // them back to back, stride R*C; A and B are n x n, n = min(R, C)).
-    // Wide (R <= C): A = X X^T, B = c A A + b A, X' = a X + B X.
-    // Tall (R > C):  A = X^T X, B = c A A + b A, X' = a X + X B.
-    // A and B are symmetric, so the B operand of A A is A's rows and that of
-    // X B is B's rows; X^T X reads X's columns (MN-major) and B X reads X's
-    // columns as its second operand.
-    const bool tall = c.R > c.C;
-    const int64_t n = std::min(c.R, c.C), k = std::max(c.R, c.C), sx = mat, sa = n * n;
-    for (int it = 0; it < hp->ns_steps; ++it) {
-      vsf_status s = VSF_OK;
-      if (!tall)
-        s = ns_gemm(false, false, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
-                    nullptr, n, sa, A, n, sa, err, st);
-      else
-        s = ns_gemm(true, true, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
-                    nullptr, n, sa, A, n, sa, err, st);
-      if (s == VSF_OK)
-        s = ns_gemm(false, false, true, n, n, n, c.batch, A, n, sa, A, n, sa, nc, nb, A, n, sa, B,
-                    n, sa, err, st);
-      if (s == VSF_OK) {
-        if (!tall)  // X'[i][l] = a X[i][l] + sum_j B[i][j] X[j][l]
-          s = ns_gemm(false, true, false, n, c.C, n, c.batch, B, n, sa, X, c.C, sx, 1.0f, na, X,
-                      c.C, sx, Xn, c.C, sx, err, st);
-        else        // X'[l][i] = a X[l][i] + sum_j X[l][j] B[i][j]
-          s = ns_gemm(false, false, false, c.R, n, n, c.batch, X, c.C, sx, B, n, sa, 1.0f, na, X,
-                      c.C, sx, Xn, c.C, sx, err, st);
-      }
-      if (s != VSF_OK) return s;
-      std::swap(X, Xn);
-    }
-    const float alpha = (float)(hp->lr * std::sqrt(std::max(1.0, (double)c.R / (double)c.C)));
-    if (vec)
-      muon_update_kernel<8><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
-                                                           alpha, bd);
-    else
-      muon_update_kernel<1><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
-                                                           alpha, bd);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
+  if (forked) {  // the other lanes start after the caller's earlier work
+    cudaError_t e = cudaEventRecord(ml->fork, caller);
+    for (int l = 1; l < kMuonLanes && e == cudaSuccess; ++l)
+      if (used[l]) e = cudaStreamWaitEvent(lanes[l], ml->fork, 0);
+    if (e != cudaSuccess)
+      return fail(VSF_ERR_CUDA, std::string("vsf_muon_step (fork): ") + cudaGetErrorString(e));
   }
-  return VSF_OK;
+  // Enqueues every chunk of the step; the caller's stream then waits for the
+  // other lanes, also when an enqueue failed part way.
+  auto run = [&]() -> vsf_status {
+    for (size_t ci = 0; ci < chunks.size(); ++ci) {
+      const MuonChunk& c = chunks[ci];
+      const int lane = lane_of[ci];
+      cudaStream_t st = lanes[lane];
+      const MuonLaneLayout& LL = L.lane[lane];
+      double* partials = reinterpret_cast<double*>(ws + LL.partials);
+      uint16_t* X = reinterpret_cast<uint16_t*>(ws + LL.x);
+      uint16_t* Xn = reinterpret_cast<uint16_t*>(ws + LL.xn);
+      uint16_t* A = reinterpret_cast<uint16_t*>(ws + LL.a);
+      uint16_t* B = reinterpret_cast<uint16_t*>(ws + LL.b);
+      MatTable tab;
+      for (int64_t j = 0; j < c.batch; ++j) tab.off[j] = c.off[(size_t)j];
+      const int64_t mat = c.R * c.C;
+      const int per = muon_per(c.batch, mat);
+      const dim3 grid((unsigned)per, (unsigned)c.batch);
+      // 8-wide accesses when every matrix of the chunk starts on 8 elements
+      bool vec = mat % 8 == 0;
+      for (int64_t j = 0; j < c.batch; ++j) vec = vec && c.off[(size_t)j] % 8 == 0;
+      if (vec) {
+        muon_momentum_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                               partials, bd);
+        muon_normalize_kernel<8><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                                partials, hp->eps, X, bd);
+      } else {
+        muon_momentum_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                               partials, bd);
+        muon_normalize_kernel<1><<<grid, kMuonThreads, 0, st>>>(packed_grad, momentum, tab, mat, mu,
+                                                                partials, hp->eps, X, bd);
+      }
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
+      // Newton-Schulz on the row-major R x C matrices of the chunk (X holds
+      // them back to back, stride R*C; A and B are n x n, n = min(R, C)).
+      // Wide (R <= C): A = X X^T, B = c A A + b A, X' = a X + B X.
+      // Tall (R > C):  A = X^T X, B = c A A + b A, X' = a X + X B.
+      // A and B are symmetric, so the B operand of A A is A's rows and that of
+      // X B is B's rows; X^T X reads X's columns (MN-major) and B X reads X's
+      // columns as its second operand.
+      const bool tall = c.R > c.C;
+      const int64_t n = std::min(c.R, c.C), k = std::max(c.R, c.C), sx = mat, sa = n * n;
+      for (int it = 0; it < hp->ns_steps; ++it) {
+        vsf_status s = VSF_OK;
+        if (!tall)
+          s = ns_gemm(false, false, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
+                      nullptr, n, sa, A, n, sa, err, st);
+        else
+          s = ns_gemm(true, true, true, n, n, k, c.batch, X, c.C, sx, X, c.C, sx, 1.0f, 0.0f,
+                      nullptr, n, sa, A, n, sa, err, st);
+        if (s == VSF_OK)
+          s = ns_gemm(false, false, true, n, n, n, c.batch, A, n, sa, A, n, sa, nc, nb, A, n, sa, B,
+                      n, sa, err, st);
+        if (s == VSF_OK) {
+          if (!tall)  // X'[i][l] = a X[i][l] + sum_j B[i][j] X[j][l]
+            s = ns_gemm(false, true, false, n, c.C, n, c.batch, B, n, sa, X, c.C, sx, 1.0f, na, X,
+                        c.C, sx, Xn, c.C, sx, err, st);
+          else        // X'[l][i] = a X[l][i] + sum_j X[l][j] B[i][j]
+            s = ns_gemm(false, false, false, c.R, n, n, c.batch, X, c.C, sx, B, n, sa, 1.0f, na, X,
+                        c.C, sx, Xn, c.C, sx, err, st);
+        }
+        if (s != VSF_OK) return s;
+        std::swap(X, Xn);
+      }
+      const float alpha = (float)(hp->lr * std::sqrt(std::max(1.0, (double)c.R / (double)c.C)));
+      if (vec)
+        muon_update_kernel<8><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
+                                                             alpha, bd);
+      else
+        muon_update_kernel<1><<<grid, kMuonThreads, 0, st>>>(X, master, packed_bf16, tab, mat, decay,
+                                                             alpha, bd);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return fail(VSF_ERR_CUDA, std::string("vsf_muon_step: ") + cudaGetErrorString(e));
+    }
+    return VSF_OK;
+  };
+  const vsf_status s = run();
+  cudaError_t je = cudaSuccess;  // join: work after the call on the caller's stream sees every lane
+  for (int l = 1; l < kMuonLanes; ++l) {
+    if (!used[l]) continue;
+    cudaError_t e = cudaEventRecord(ml->join[l], lanes[l]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(caller, ml->join[l], 0);
+    if (je == cudaSuccess) je = e;
+  }
+  if (je != cudaSuccess && s == VSF_OK)
+    return fail(VSF_ERR_CUDA, std::string("vsf_muon_step (join): ") + cudaGetErrorString(je));
+  return s;
 }
 
 }  // extern "C"

@@ -130,11 +130,22 @@ struct vsf_plan {
   int tma_cluster = 1;
   int tma_clusters = 0;
   std::vector<unsigned char> upload_image;  // host source of the last upload copy
+  // Muon's second stream and its fork/join events, created at upload on the
+  // plan's device (muon.cu owns the type and frees it).
+  void* muon_lanes = nullptr;
+  void (*muon_lanes_free)(void*) = nullptr;
   // Tensor maps of the tile tensors, encoded for the last pointers seen.
   mutable std::mutex maps_mu;
   mutable std::vector<unsigned char> maps_blob;  // kernel-parameter image
   mutable const void* maps_key[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   mutable int maps_dtype = -1;
+
+  vsf_plan() = default;
+  vsf_plan(const vsf_plan&) = delete;
+  vsf_plan& operator=(const vsf_plan&) = delete;
+  ~vsf_plan() {
+    if (muon_lanes_free != nullptr) muon_lanes_free(muon_lanes);
+  }
 };
 
 namespace vsf {
@@ -147,5 +158,8 @@ struct Range {
   Range& operator=(const Range&) = delete;
 };
 vsf_status fail(vsf_status s, const std::string& msg);
+// Creates Muon's second stream and its events on the current device (once
+// per plan; muon.cu).
+vsf_status muon_lanes_create(vsf_plan* plan);
 vsf_status build_tables(vsf_plan* plan, int32_t r0, int32_t r1);
 }  // namespace vsf

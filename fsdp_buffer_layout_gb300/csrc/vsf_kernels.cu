@@ -798,6 +798,8 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   plan->adam_clusters = std::max(1, nclusters);
   plan->tma_cluster = tma_CL;
   plan->tma_clusters = tma_ncl;
+  const vsf_status lanes = muon_lanes_create(plan);
+  if (lanes != VSF_OK) return lanes;
   plan->uploaded = true;
   return VSF_OK;
 }

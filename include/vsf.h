@@ -205,7 +205,10 @@ vsf_status vsf_plan_device_error_offset(const vsf_plan* plan, size_t* offset);
  * aligned, vsf_plan_workspace_bytes long) on `stream`, zeroes its scratch,
  * and binds the plan to the current CUDA device. Must precede every per-step
  * call; the workspace must stay allocated while the plan is used. Calls that
- * share one plan (and so one workspace) must be ordered on the device. */
+ * share one plan (and so one workspace) must be ordered on the device. The
+ * first upload on a device also creates the plan's own non-blocking streams
+ * (three) and events, which vsf_muon_step forks onto; vsf_plan_destroy
+ * releases them. */
 vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void* stream);
 
 /* Copy-in with the fused squared-norm reduction ([FSDP] 关键观察; [VSF]
@@ -322,12 +325,17 @@ vsf_status vsf_group_add(const vsf_plan* plan, void* dst, int32_t dst_dtype, con
  *     p = p (1 - lr wd) - fp32(lr sqrt(max(1, R/C))) X;  bf16 copy.
  *   packed_grad: bf16, m*S; momentum: fp32, m*S (caller-zeroed before step
  *   1); master: fp32; packed_bf16: out. d_workspace: vsf_muon_workspace_bytes
- *   of caller memory (the Newton-Schulz operands X, X', A, B of the largest
- *   batch and the norm partials). The products run on the library's tcgen05
- *   kernel (vsf_ns_gemm below); its bounded waits report through the plan's
- *   device error word. Matrices of one shape, across tensors, run batched:
- *   vsf_muon_chunk_count gives the number of batches (each: 3 element-wise
- *   kernels and 3 * ns_steps products); 0 for a NULL plan. Errors:
+ *   of caller memory (per stream lane, the Newton-Schulz operands X, X', A, B
+ *   of its largest batch and the norm partials). The products run on the
+ *   library's tcgen05 kernel (vsf_ns_gemm below); its bounded waits report
+ *   through the plan's device error word. Matrices of one shape, across
+ *   tensors, run batched: vsf_muon_chunk_count gives the number of batches
+ *   (each: 3 element-wise kernels and 3 * ns_steps products); 0 for a NULL
+ *   plan. The batches are independent and run on four stream lanes:
+ *   `stream` itself and the plan's own three streams, which wait for
+ *   `stream`'s earlier work (an event) and which `stream` waits for before
+ *   its later work, so the call is ordered on `stream` like a single launch
+ *   (also under stream capture). Errors:
  *   VSF_ERR_ARG (NULL, small workspace, ns_steps < 0), VSF_ERR_ALIGN (a
  *   pointer not 16-byte aligned), VSF_ERR_STATE (plan not uploaded),
  *   VSF_ERR_CUDA (a launch or a tensor-map encoding failed).

@@ -161,3 +161,41 @@ def test_muon_update_one_step(shape):
         assert np.allclose(state[0]["O"], O, rtol=0, atol=0)
     finally:
         ss.close()
+
+
+def test_two_lanes_are_ordered_on_the_callers_stream():
+    """The batched chunks run on two stream lanes (the caller's stream and the
+    plan's own). A copy of the bf16 buffer enqueued after the step on the
+    caller's stream, and waited for on that stream alone, must see every
+    chunk's update, including those of the plan's own lane; and the lanes
+    change no arithmetic, so a second plan on the default stream gives the
+    same bits."""
+    from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    specs = [TensorSpec((2048, 4096), W.GRAN_ROWS, 64), TensorSpec((4096, 1024), W.GRAN_ROWS, 64),
+             TensorSpec((2, 1024, 1024), W.GRAN_ROWS, 128)]
+    side = torch.cuda.Stream()
+    outs = []
+    for stream in (side, None):
+        ss = ShardStep(specs, 4, 128, stream=stream)
+        try:
+            assert ss.muon_chunks() == 3
+            for t, n in enumerate(ss.numels):
+                g = fill_bf16(key(13, 1, t, KIND_GRAD), DIST_NORMAL, 1e-3, 0, np.empty(n, np.uint16))
+                o = ss.offsets[t]
+                ss.packed_grad.view(torch.int16)[o:o + n].copy_(torch.from_numpy(g.view(np.int16)))
+            torch.cuda.synchronize()
+            ss.muon_step()
+            with torch.cuda.stream(ss.stream):
+                snap = ss.packed_bf16.clone()
+            ss.stream.synchronize()  # the caller's stream only
+            got = snap.view(torch.int16).cpu()
+            torch.cuda.synchronize()
+            assert torch.equal(got, ss.packed_bf16.view(torch.int16).cpu())
+            for t, n in enumerate(ss.numels):  # every tensor was updated
+                o = ss.offsets[t]
+                assert got[o:o + n].any()
+            assert ss.device_error() == 0
+            outs.append(got)
+        finally:
+            ss.close()
+    assert torch.equal(outs[0], outs[1])
