@@ -116,6 +116,11 @@ struct TileMaps {
   int32_t count;
 };
 
+// Fetch the line holding *p into this SM's L1 (no register, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Asynchronous remote store of a float2 into a peer's shared memory: the
 // peer's mbarrier at the offset of local_bar receives the 8 bytes as
 // transaction bytes, so the peer sees the data once that phase completes,
@@ -268,10 +273,21 @@ __global__ void __launch_bounds__(TmaShape<W>::threads, TmaShape<W>::ctas_per_sm
       uint32_t p = 0;  // ring positions issued so far
       bool halted = false;
       for (int j = starts[cid]; j < starts[cid + 1] && !halted; ++j) {
-        const QBlock b = qb[list[j]];
+        const int q0 = list[j];
+        const QBlock b = qb[q0];
         const int kt = ktab[j];
         const TmaShare sh = tma_share<CH>(b, kt, CL, crank);
         const int c0 = sh.c0, c1 = sh.c1;
+        // The consumers start the unit by reading its tiles' old scales;
+        // fetch those lines into this SM's L1 now, ahead of them. Measured
+        // on the wide shape: 1.3B model 3.436 -> 3.362 ms, MoE layer 2.226 ->
+        // 2.215; the narrow shape (DSv3 block) ran 0.3% slower with it.
+        if constexpr (W == kTmaWideWarps) {
+          prefetch_l1(m_scale + q0);
+          prefetch_l1(m_scale + q0 + kt - 1);
+          prefetch_l1(v_scale + q0);
+          prefetch_l1(v_scale + q0 + kt - 1);
+        }
         int mi = 0;
         if (b.tx >= 0)
           while (mi + 1 < maps.count && maps.tensor[mi] != b.tensor) ++mi;
