@@ -126,18 +126,22 @@ __device__ __forceinline__ float2 s8pair_to_f2(uint32_t word_xor80, int first) {
 // (never -128). The lower clamp comes first and keeps a NaN a NaN
 // (max.NaN), which the conversion then turns into 0. It matters when a
 // block's scale is so small that 127 / scale overflows to infinity.
+// Both conversions leave the code in byte 0 of the word (the upper bytes
+// extend it); every caller takes byte 0 only (pack4, or a cast to an 8-bit
+// type), so no mask is spent on them.
 __device__ __forceinline__ uint32_t cvt_sat_s8(float x) {
   float y;
   asm("max.NaN.f32 %0, %1, 0fC2FE0000;" : "=f"(y) : "f"(x));  // max(x, -127)
   uint32_t r;
   asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(y));
-  return r & 0xffu;
+  return r;
 }
 __device__ __forceinline__ uint32_t cvt_sat_u8(float x) {
   uint32_t r;
   asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r & 0xffu;
+  return r;
 }
+// Bytes 0 of a, b, c, d, in that order from the low byte.
 __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
