@@ -28,9 +28,11 @@ constexpr int kMaxCopyGrid = 4096;
 // when every unit has at most kTmaNarrowMaxUnit elements. Small units leave a
 // single pipeline per SM idle while its consumers wait for the block maxima;
 // four pipelines per SM overlap those waits. The bound keeps the narrow
-// shape cluster-free: 4 CTAs on each of 152 SMs, each holding one unit's
-// gradient and codes (4 bytes an element for bf16 gradients) in L2 between
-// the two passes, stay within the 128 MB L2 budget (608 * 4 * 48 Ki = 114 MB).
+// shape's clusters small: 4 CTAs on each of 152 SMs, each cluster holding
+// one unit's gradient and codes (4 bytes an element for bf16 gradients) in
+// L2 between the two passes, keep 608 * 4 * 48 Ki = 114 MB in flight at the
+// bound in clusters of 1, and half that in clusters of 2, which the bulk
+// kernel's L2 rule (half the L2) then picks.
 constexpr int kTmaGroups = 2;
 constexpr int kTmaWideWarps = 16;
 constexpr int kTmaNarrowWarps = 4;
