@@ -143,3 +143,11 @@ def test_forced_shape_survives_restrict_and_rejects_other_values():
         assert V.vsf_plan_get_info(p).bulk_warps == 4
     finally:
         V.vsf_plan_destroy(p)
+
+
+def test_cluster_size_is_reported_only_after_upload():
+    """vsf_plan_info.bulk_cluster is chosen by vsf_plan_upload (it needs the
+    GPU's occupancy); before upload it reads 0, and the reserved word is 0."""
+    info = _info([((96, 11008), W.GRAN_ROWS, 32, 0)])
+    assert info.bulk_cluster == 0
+    assert info.reserved == 0

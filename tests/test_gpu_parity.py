@@ -136,8 +136,12 @@ def test_large_blocks_use_clusters():
 def test_large_units_use_clusters_of_four_and_eight(shape, block_rows, want):
     """Units whose phase-1 bytes would overflow the L2 budget in clusters of 2
     go to clusters of 4 or 8, each CTA taking an equal element range (to 16
-    elements) of every unit; bit-exact like every other path."""
-    specs = [(shape, W.GRAN_ROWS, block_rows, 0), ((4096,), W.GRAN_ELEM, 0, 0)]
+    elements) of every unit, empty for most CTAs of a 16- or 48-element unit;
+    bit-exact like every other path."""
+    specs = [(shape, W.GRAN_ROWS, block_rows, 0), ((4096,), W.GRAN_ELEM, 0, 0),
+             # 16- and 48-element blocks: most CTAs of a cluster get an empty
+             # share of such a unit and still take part in its exchange
+             ((8, 16), W.GRAN_ROWS, 1, 0), ((4, 48), W.GRAN_ROWS, 1, 0)]
     case = _normal_case(specs, m=4, g=128, steps=3)
     g = run_gpu(case)
     assert g["bulk_cluster"] == want, f"clusters of {g['bulk_cluster']}"
