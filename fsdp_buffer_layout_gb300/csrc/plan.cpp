@@ -452,6 +452,128 @@ vsf_status vsf_plan_set_bulk_warps(vsf_plan* plan, int32_t warps) {
 
 void vsf_plan_destroy(vsf_plan* plan) { delete plan; }
 
+namespace {
+constexpr uint32_t kPlanMagic = 0x50465356u;  // "VSFP"
+constexpr uint32_t kPlanVersion = 1;
+
+// Fixed-size part of a serialized plan, then n descriptors, n offsets and
+// the checksum of everything before it.
+struct PlanHeader {
+  uint32_t magic, version;
+  int32_t n, m;
+  int64_t g_coll;
+  int32_t order, rank_begin, rank_end, forced_warps;
+  int64_t S;
+};
+
+uint64_t fnv1a(const unsigned char* p, size_t len) {
+  uint64_t h = 0xcbf29ce484222325ull;
+  for (size_t i = 0; i < len; ++i) {
+    h ^= p[i];
+    h *= 0x100000001b3ull;
+  }
+  return h;
+}
+
+size_t plan_bytes(int32_t n) {
+  return sizeof(PlanHeader) + (size_t)n * (sizeof(vsf_tensor_desc) + sizeof(int64_t)) +
+         sizeof(uint64_t);
+}
+}  // namespace
+
+vsf_status vsf_plan_serialize(const vsf_plan* plan, void* buf, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_serialize: NULL argument");
+  const size_t need = plan_bytes(plan->n);
+  if (buf == nullptr) {
+    *bytes = need;
+    return VSF_OK;
+  }
+  if (*bytes < need) {
+    *bytes = need;
+    return fail(VSF_ERR_ARG, "vsf_plan_serialize: buffer too small");
+  }
+  unsigned char* p = static_cast<unsigned char*>(buf);
+  PlanHeader h;
+  std::memset(&h, 0, sizeof(h));
+  h.magic = kPlanMagic;
+  h.version = kPlanVersion;
+  h.n = plan->n;
+  h.m = plan->m;
+  h.g_coll = plan->g_coll;
+  h.order = plan->order_used;
+  h.rank_begin = plan->rank_begin;
+  h.rank_end = plan->rank_end;
+  h.forced_warps = plan->forced_warps;
+  h.S = plan->S;
+  std::memcpy(p, &h, sizeof(h));
+  size_t at = sizeof(h);
+  for (int t = 0; t < plan->n; ++t) {
+    const vsf::TensorInfo& x = plan->tensors[t];
+    vsf_tensor_desc d;
+    std::memset(&d, 0, sizeof(d));
+    d.ndim = x.ndim;
+    d.gran = x.gran;
+    for (int k = 0; k < x.ndim; ++k) d.shape[k] = x.shape[k];
+    d.block_rows = x.block_rows;
+    d.tile_cols = x.tile_cols;
+    std::memcpy(p + at, &d, sizeof(d));
+    at += sizeof(d);
+  }
+  for (int t = 0; t < plan->n; ++t) {
+    std::memcpy(p + at, &plan->tensors[t].offset, sizeof(int64_t));
+    at += sizeof(int64_t);
+  }
+  const uint64_t sum = fnv1a(p, at);
+  std::memcpy(p + at, &sum, sizeof(sum));
+  *bytes = need;
+  return VSF_OK;
+}
+
+vsf_status vsf_plan_deserialize(const void* buf, size_t bytes, vsf_plan** out) {
+  if (buf == nullptr || out == nullptr) return fail(VSF_ERR_ARG, "vsf_plan_deserialize: NULL argument");
+  *out = nullptr;
+  const unsigned char* p = static_cast<const unsigned char*>(buf);
+  if (bytes < sizeof(PlanHeader)) return fail(VSF_ERR_ARG, "vsf_plan_deserialize: truncated");
+  PlanHeader h;
+  std::memcpy(&h, p, sizeof(h));
+  if (h.magic != kPlanMagic) return fail(VSF_ERR_ARG, "vsf_plan_deserialize: not a serialized plan");
+  if (h.version != kPlanVersion) return fail(VSF_ERR_ARG, "vsf_plan_deserialize: unknown version");
+  if (h.n < 1 || h.n > vsf::kMaxTensors || bytes != plan_bytes(h.n))
+    return fail(VSF_ERR_ARG, "vsf_plan_deserialize: size does not match the tensor count");
+  const size_t body = bytes - sizeof(uint64_t);
+  uint64_t sum;
+  std::memcpy(&sum, p + body, sizeof(sum));
+  if (sum != fnv1a(p, body)) return fail(VSF_ERR_ARG, "vsf_plan_deserialize: checksum mismatch");
+  std::vector<vsf_tensor_desc> descs((size_t)h.n);
+  std::vector<int64_t> offsets((size_t)h.n);
+  size_t at = sizeof(h);
+  std::memcpy(descs.data(), p + at, sizeof(vsf_tensor_desc) * descs.size());
+  at += sizeof(vsf_tensor_desc) * descs.size();
+  std::memcpy(offsets.data(), p + at, sizeof(int64_t) * offsets.size());
+  if (h.order < VSF_ORDER_DEFAULT || h.order > VSF_ORDER_SHAPE)
+    return fail(VSF_ERR_ARG, "vsf_plan_deserialize: bad order policy");
+  vsf_plan* plan = nullptr;
+  vsf_status st = vsf_plan_create(descs.data(), h.n, h.m, h.g_coll, h.order, &plan);
+  if (st != VSF_OK) return st;
+  if (plan->S != h.S) {
+    vsf_plan_destroy(plan);
+    return fail(VSF_ERR_STATE, "vsf_plan_deserialize: the planner gives another S for these inputs");
+  }
+  for (int t = 0; t < h.n; ++t)
+    if (plan->tensors[t].offset != offsets[(size_t)t]) {
+      vsf_plan_destroy(plan);
+      return fail(VSF_ERR_STATE, "vsf_plan_deserialize: the planner gives other offsets for these inputs");
+    }
+  if (h.rank_begin != 0 || h.rank_end != h.m) st = vsf_plan_restrict(plan, h.rank_begin, h.rank_end);
+  if (st == VSF_OK && h.forced_warps != 0) st = vsf_plan_set_bulk_warps(plan, h.forced_warps);
+  if (st != VSF_OK) {
+    vsf_plan_destroy(plan);
+    return st;
+  }
+  *out = plan;
+  return VSF_OK;
+}
+
 vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info) {
   if (plan == nullptr || info == nullptr) return fail(VSF_ERR_ARG, "NULL argument");
   std::memset(info, 0, sizeof(*info));

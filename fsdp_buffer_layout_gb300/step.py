@@ -212,6 +212,8 @@ class ShardStep:
         out["plan"] = dict(S=int(self.info.S), offsets=list(self.offsets),
                            ranks=(int(self.info.rank_begin), int(self.info.rank_end)),
                            quantized=bool(self.quantized))
+        # the whole plan, from which vsf_plan_deserialize rebuilds it
+        out["plan_bytes"] = V.vsf_plan_serialize(self.plan)
         return out
 
     def load_state_dict(self, sd: dict) -> None:

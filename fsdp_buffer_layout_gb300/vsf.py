@@ -82,6 +82,10 @@ def lib():
             L.vsf_plan_create.argtypes = [P(vsf_tensor_desc), i32, i32, i64, i32, P(vp)]
             L.vsf_plan_destroy.restype = None
             L.vsf_plan_destroy.argtypes = [vp]
+            L.vsf_plan_serialize.restype = st
+            L.vsf_plan_serialize.argtypes = [vp, vp, P(ctypes.c_size_t)]
+            L.vsf_plan_deserialize.restype = st
+            L.vsf_plan_deserialize.argtypes = [vp, ctypes.c_size_t, P(vp)]
             L.vsf_plan_get_info.restype = st
             L.vsf_plan_get_info.argtypes = [vp, P(vsf_plan_info)]
             L.vsf_plan_offsets.restype = st
@@ -186,6 +190,22 @@ def vsf_plan_create(descs, m: int, g_coll: int, order: int = VSF_ORDER_DEFAULT) 
 
 def vsf_plan_destroy(plan: int) -> None:
     lib().vsf_plan_destroy(plan)
+
+
+def vsf_plan_serialize(plan: int) -> bytes:
+    """The plan as bytes (its inputs, rank window, forced shape, S, offsets)."""
+    n = ctypes.c_size_t(0)
+    _check(lib().vsf_plan_serialize(plan, None, ctypes.byref(n)))
+    buf = ctypes.create_string_buffer(n.value)
+    _check(lib().vsf_plan_serialize(plan, buf, ctypes.byref(n)))
+    return buf.raw[:n.value]
+
+
+def vsf_plan_deserialize(data: bytes) -> int:
+    """A new plan from vsf_plan_serialize's bytes (planned again and checked)."""
+    out = ctypes.c_void_p()
+    _check(lib().vsf_plan_deserialize(data, len(data), ctypes.byref(out)))
+    return out.value
 
 
 def vsf_selftest_wait_timeout(d_err: int, limit_ns: int, stream: int) -> None:

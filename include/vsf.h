@@ -162,6 +162,28 @@ vsf_status vsf_plan_set_bulk_warps(vsf_plan* plan, int32_t warps);
 
 vsf_status vsf_plan_get_info(const vsf_plan* plan, vsf_plan_info* info);
 
+/* Checkpointing a plan. The layout is a deterministic function of the
+ * descriptors, m, g_coll and the order policy ([VSF] 核心方法 › Grouped
+ * communication, Algorithm 1), so a plan is stored as those inputs plus
+ * its rank window and forced kernel shape, and the S and offsets it
+ * produced (to check against on load). Host only; no CUDA call.
+ *
+ * vsf_plan_serialize writes the plan into buf. With buf == NULL it only sets
+ * *bytes to the size needed. Otherwise *bytes is the capacity of buf on
+ * entry and the size written on return. Errors: VSF_ERR_ARG (NULL plan or
+ * bytes; capacity too small, *bytes then set to the size needed). The
+ * format is the host's native byte order (little-endian on x86-64 and
+ * Arm64), versioned, with a 64-bit FNV-1a checksum.
+ *
+ * vsf_plan_deserialize plans again from the stored inputs, checks that S and
+ * every offset equal the stored ones, restricts to the stored rank window and
+ * forces the stored kernel shape. The result is a new, not yet uploaded plan
+ * in *out. Errors: VSF_ERR_ARG (NULL, truncated buffer, bad magic, version
+ * or checksum, inconsistent sizes), VSF_ERR_STATE (the planner now gives
+ * another layout for the same inputs), and the errors of vsf_plan_create. */
+vsf_status vsf_plan_serialize(const vsf_plan* plan, void* buf, size_t* bytes);
+vsf_status vsf_plan_deserialize(const void* buf, size_t bytes, vsf_plan** out);
+
 /* Per-tensor element offsets into the m*S buffer; offsets has n entries. */
 vsf_status vsf_plan_offsets(const vsf_plan* plan, int64_t* offsets);
 
