@@ -948,13 +948,13 @@ def muon_cpu_baseline(w, threads: int | None = None):
 # is this ratio times the full launch's algorithmic bytes. A workload without
 # a capture of the current kernel has no entry (traffic null).
 TRAFFIC: dict = {
-    "llama_1p3b": dict(ratio=1.0017, capture="llama_1p3b cut to 0.1 of its rows: 2.0789 GB "
+    "llama_1p3b": dict(ratio=1.0013, capture="llama_1p3b cut to 0.1 of its rows: 2.0782 GB "
                        "DRAM for 2.0754 GB algorithmic, one launch (profiles/adam8_tma_traffic.md)"),
-    "llama_layer": dict(ratio=0.9890, capture="llama_layer cut to 0.5 of its rows: 1.6012 GB "
+    "llama_layer": dict(ratio=0.9893, capture="llama_layer cut to 0.5 of its rows: 1.6018 GB "
                         "for 1.6191 GB, one launch (profiles/adam8_tma_traffic.md)"),
-    "moe_layer": dict(ratio=0.9995, capture="moe_layer cut to 0.15 of its rows: 1.9103 GB for "
+    "moe_layer": dict(ratio=0.9973, capture="moe_layer cut to 0.15 of its rows: 1.9061 GB for "
                       "1.9113 GB, one launch (profiles/adam8_tma_traffic.md)"),
-    "dsv3_block": dict(ratio=0.9725, capture="dsv3_block cut to 0.5 of its rows: 2.0561 GB for "
+    "dsv3_block": dict(ratio=0.9730, capture="dsv3_block cut to 0.5 of its rows: 2.0572 GB for "
                        "2.1142 GB, one launch (profiles/adam8_tma_traffic.md)"),
 }
 

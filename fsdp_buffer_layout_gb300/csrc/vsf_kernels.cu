@@ -612,8 +612,14 @@ vsf_status vsf_plan_upload(vsf_plan* plan, void* d_workspace, size_t bytes, void
   if (e != cudaSuccess) return cuda_fail(e, "vsf_plan_upload");
 
   // Copy grid: equal spans of the real elements inside the rank window
-  // (each tensor's [lo, hi)), cut on 8-element multiples.
-  const int grid = std::max(1, std::min(kMaxCopyGrid, sms * kCopyCtasPerSm));
+  // (each tensor's [lo, hi)), cut on 8-element multiples. kCopyCtasPerSm
+  // CTAs per SM for large buffers; a small buffer gets at least one full
+  // unrolled pass of 16-byte loads per CTA instead of thousands of nearly
+  // empty CTAs (and as many partials for the norm to reduce).
+  constexpr int64_t kMinCopyElems = (int64_t)kCopyUnroll * kCopyThreads * 8;
+  const int64_t by_work = (plan->real + kMinCopyElems - 1) / kMinCopyElems;
+  const int grid = (int)std::max<int64_t>(
+      1, std::min<int64_t>(by_work, std::min(kMaxCopyGrid, sms * kCopyCtasPerSm)));
   std::vector<CopySpan> spans(grid + 1);
   {
     std::vector<int64_t> starts(plan->n + 1, 0);
