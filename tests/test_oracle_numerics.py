@@ -356,3 +356,41 @@ def test_group_add_bf16_matches_numpy_and_torch_rounding():
     oracle.group_op(2, [4096], [0], acc, a)
     oracle.group_op(2, [4096], [0], acc, b)
     assert np.array_equal(acc, s32)
+
+
+def test_blocks_are_independent_across_calls():
+    """The 8-bit step of one quantisation block reads and writes only that
+    block's elements and its own two scales ([VSF] case study › 8-bit Adam:
+    block-wise quantisation, no block crosses a rank), so running a tensor's
+    blocks as several runs of consecutive blocks, in any order, gives the
+    same state bit for bit as one call over all of them. The full-size GPU
+    parity relies on this to replay large tensors on host threads."""
+    w = W.tiny()
+    d = oracle.Desc.from_workload(w)
+    S, off = oracle.plan(d, w.m, w.g_coll)
+    qb = oracle.qblocks(d, w.g_coll, off)
+    hp = oracle.hparams(w)
+    t = int(np.argmax([x.numel for x in w.tensors]))
+    ids = np.nonzero(qb["tensor"] == t)[0]
+    blocks = {k: np.ascontiguousarray(qb[k][ids]) for k in ("base", "nrows", "ncols", "stride")}
+    blocks["base"] = blocks["base"] - int(off[t])
+    n = w.tensors[t].numel
+    assert ids.size >= 8
+
+    def fresh():
+        return dict(p=W.master_init(w, t).copy(), mq=np.zeros(n, np.int8), vq=np.zeros(n, np.uint8),
+                    msc=np.zeros(ids.size, np.float32), vsc=np.zeros(ids.size, np.float32),
+                    bf=np.zeros(n, np.uint16))
+
+    whole, parts = fresh(), fresh()
+    runs = [(0, 3), (3, 4), (4, ids.size)]
+    for s in range(1, 4):
+        g = W.grad(w, s, t)
+        oracle.adam_all(blocks, g, 0.25, True, whole["mq"], whole["vq"], whole["msc"], whole["vsc"],
+                        whole["p"], whole["bf"], s, hp)
+        for lo, hi in reversed(runs):
+            sub = {k: v[lo:hi] for k, v in blocks.items()}
+            oracle.adam_all(sub, g, 0.25, True, parts["mq"], parts["vq"], parts["msc"][lo:hi],
+                            parts["vsc"][lo:hi], parts["p"], parts["bf"], s, hp)
+    for k in whole:
+        assert np.array_equal(whole[k].view(np.uint8), parts[k].view(np.uint8)), k
