@@ -27,8 +27,10 @@ HP = dict(lr=0.02, momentum=0.95, weight_decay=0.01, eps=1e-7, ns_steps=5, ns_a=
           ns_b=-4.7750, ns_c=2.0315)
 
 
-def _run(specs, m, g_coll, steps):
+def _run(specs, m, g_coll, steps, ns_steps=5):
+    from fsdp_buffer_layout_gb300 import vsf as V
     from fsdp_buffer_layout_gb300.step import ShardStep, TensorSpec
+    hp = dict(HP, ns_steps=ns_steps)
     ss = ShardStep([TensorSpec(*s) for s in specs], m, g_coll)
     try:
         numels = ss.numels
@@ -45,7 +47,7 @@ def _run(specs, m, g_coll, steps):
             for t, gr in enumerate(grads):
                 pk[ss.offsets[t]:ss.offsets[t] + numels[t]].copy_(
                     torch.from_numpy(gr.view(np.int16)))
-            ss.muon_step()
+            ss.muon_step(V.make_muon_hparams(ns_steps=ns_steps))
             for t, sp in enumerate(specs):
                 shape = sp[0]
                 if len(shape) < 2:
@@ -54,11 +56,11 @@ def _run(specs, m, g_coll, steps):
                 g32 = (grads[t].astype(np.uint32) << 16).view(np.float32).reshape(-1, R, C)
                 M = state[t]["M"].reshape(-1, R, C)
                 P = state[t]["p"].reshape(-1, R, C)
-                outs = [muon.muon_matrix(g32[e], M[e], P[e], HP) for e in range(g32.shape[0])]
+                outs = [muon.muon_matrix(g32[e], M[e], P[e], hp) for e in range(g32.shape[0])]
                 state[t]["M"] = np.stack([o[0] for o in outs]).ravel()
                 state[t]["p"] = np.stack([o[1] for o in outs]).ravel()
                 state[t]["O"] = np.stack([o[3] for o in outs]).ravel()
-                Oe = np.stack([muon.muon_matrix(g32[e], M[e], P[e], HP, exact=True)[3]
+                Oe = np.stack([muon.muon_matrix(g32[e], M[e], P[e], hp, exact=True)[3]
                                for e in range(g32.shape[0])]).ravel()
                 diff = state[t]["O"].astype(np.float64) - Oe
                 state[t]["d_frob"] += np.linalg.norm(diff)
@@ -199,3 +201,40 @@ def test_two_lanes_are_ordered_on_the_callers_stream():
         finally:
             ss.close()
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("ns_steps", [0, 1, 2])
+def test_iteration_counts(ns_steps):
+    """Newton-Schulz with 0, 1 or 2 iterations instead of 5 (with none, the
+    update applies O = X0). Wide, tall and batched matrices, 8-aligned and
+    not, three steps, against the oracle. With iterations the bound is the
+    one of test_muon_matches_oracle; with none, O = X0 is one bf16 rounding
+    of the normalised momentum on both sides, which may differ by one bf16
+    unit (2^-8 relative) where the two norms round differently: the masters
+    must agree to 2% of how far the three updates moved them."""
+    specs = [((256, 512), W.GRAN_ROWS, 32, 0), ((512, 256), W.GRAN_ROWS, 32, 0),
+             ((2, 128, 256), W.GRAN_ROWS, 64, 0), ((5, 9, 7), W.GRAN_ROWS, 5, 0)]
+    ss, state, masters = _run(specs, 4, 128, steps=3, ns_steps=ns_steps)
+    try:
+        for t, sp in enumerate(specs):
+            o, n = ss.offsets[t], ss.numels[t]
+            got_p = ss.master[o:o + n].cpu().numpy()
+            got_M = ss.momentum[o:o + n].cpu().numpy()
+            assert np.array_equal(got_M.view(np.uint32), state[t]["M"].view(np.uint32))
+            R, C = sp[0][-2], sp[0][-1]
+            alpha = float(np.float32(HP["lr"] * math.sqrt(max(1.0, R / C))))
+            ulp = 3 * 2 * float(np.spacing(np.abs(got_p)).max())
+            diff = np.abs(got_p.astype(np.float64) - state[t]["p"].astype(np.float64))
+            if ns_steps:
+                assert diff.max() <= alpha * 2 * state[t]["d_max"] + ulp
+            else:  # a bf16 unit of O is 2^-8 of it: far below the update itself
+                decay3 = np.float64(np.float32(1.0 - HP["lr"] * HP["weight_decay"])) ** 3
+                moved = np.abs(state[t]["p"].astype(np.float64) - masters[t] * decay3).max()
+                assert moved > 0
+                assert diff.max() <= 0.02 * moved + ulp
+            bf = ss.packed_bf16.view(torch.int16)[o:o + n].cpu().numpy().view(np.uint16)
+            assert np.array_equal(bf, (muon.bf16_from_f32(got_p).view(np.uint32) >> 16)
+                                  .astype(np.uint16))
+        assert ss.device_error() == 0
+    finally:
+        ss.close()
