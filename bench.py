@@ -1052,8 +1052,11 @@ def main():
     if args.optimizer == "muon" and args.zero_copy:
         ap.error("--zero-copy applies to the AdamW step")
     if world > 1:
+        import torch
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)  # one GPU per rank, bound before NCCL starts
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     arm = group_ops_arm if args.group_ops else muon_arm if args.optimizer == "muon" else gpu_arm
     line = arm(args, rank, world)
     if rank == 0:
