@@ -238,3 +238,30 @@ def test_iteration_counts(ns_steps):
         assert ss.device_error() == 0
     finally:
         ss.close()
+
+
+@pytest.mark.slow
+def test_full_llama_layer_one_step():
+    """One Muon step of the whole Llama layer (q, k, v, o 4096 x 4096; gate and
+    up 11008 x 4096, down 4096 x 11008; two norm vectors) at its own m and
+    g_coll, against the oracle matrix by matrix, with the bound of
+    test_muon_matches_oracle; the norm vectors stay untouched."""
+    w = W.llama_layer()
+    specs = [(t.shape, t.gran, t.block_rows, t.tile_cols) for t in w.tensors]
+    ss, state, masters = _run(specs, w.m, w.g_coll, steps=1)
+    try:
+        for t, sp in enumerate(specs):
+            o, n = ss.offsets[t], ss.numels[t]
+            got_p = ss.master[o:o + n].cpu().numpy()
+            if len(sp[0]) < 2:
+                assert np.array_equal(got_p, masters[t])
+                continue
+            R, C = sp[0][-2], sp[0][-1]
+            alpha = float(np.float32(HP["lr"] * math.sqrt(max(1.0, R / C))))
+            ulp = 2 * float(np.spacing(np.abs(got_p)).max())
+            diff = got_p.astype(np.float64) - state[t]["p"].astype(np.float64)
+            assert np.abs(diff).max() <= alpha * 2 * state[t]["d_max"] + ulp, t
+            assert np.linalg.norm(diff) <= alpha * 2 * state[t]["d_frob"] + ulp * math.sqrt(n), t
+        assert ss.device_error() == 0
+    finally:
+        ss.close()
