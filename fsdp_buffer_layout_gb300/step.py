@@ -196,6 +196,21 @@ class ShardStep:
         self.adam(step)
         self.unpack(params)
 
+    def window_step(self, grads, params, step: int, all_reduce):
+        """The step of a rank window (ranks=(r0, r1)) in one process of many:
+        pack -> this window's fp64 sum of squares -> all_reduce (the sum over
+        every process's window: the path's one exchange) -> factor -> 8-bit
+        AdamW -> unpack. all_reduce(t) sums the one-element float64 tensor t
+        in place across the processes (see sum_all_reduce)."""
+        self.pack(grads)
+        self.group_sumsq()
+        total = self.sumsq[:1]
+        with torch.cuda.stream(self.stream):
+            all_reduce(total)
+        self.scale_from_sumsq(total)
+        self.adam(step)
+        self.unpack(params)
+
     def device_error(self) -> int:
         """The device error word (0 = every bounded wait succeeded)."""
         off = V.vsf_plan_device_error_offset(self.plan)
@@ -231,3 +246,19 @@ class ShardStep:
     def load_master(self, t: int, values: torch.Tensor):
         o = self.offsets[t]
         self.master[o:o + self.numels[t]].copy_(values.reshape(-1))
+
+
+def sum_all_reduce(group=None):
+    """all_reduce for ShardStep.window_step over a torch.distributed group:
+    in place on the device with NCCL, through a host copy with gloo."""
+    import torch.distributed as dist
+
+    def reduce(t: torch.Tensor) -> None:
+        if dist.get_backend(group) == "nccl":
+            dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+            return
+        h = t.cpu()  # waits for the sum of squares on the current stream
+        dist.all_reduce(h, op=dist.ReduceOp.SUM, group=group)
+        t.copy_(h)
+
+    return reduce

@@ -98,3 +98,25 @@ def test_two_rank_norm_matches_single_process(max_norm):
         else:
             assert abs(f - want_f) <= np.spacing(np.float32(want_f))
         assert tmax == 2.0  # every rank reports the slowest rank's time
+
+
+def _sum_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from fsdp_buffer_layout_gb300.step import sum_all_reduce
+        t = torch.tensor([0.5 * (rank + 1)], dtype=torch.float64)
+        sum_all_reduce()(t)
+        out[rank] = float(t.item())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_window_step_all_reduce_sums_over_processes():
+    """sum_all_reduce, the exchange ShardStep.window_step calls, sums the
+    one-element fp64 tensor of every process in place (gloo: 3 processes)."""
+    world = 3
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_sum_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+        assert [out[r] for r in range(world)] == [3.0] * world
