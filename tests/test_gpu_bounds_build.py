@@ -5,7 +5,9 @@ against the packed buffers' extent and set bit 4 of the device error word
 instead of accessing out of range. It stands in for a memory checker: the
 parity, rank-window, group-op, Muon and resume suites run against it in a
 child process, and every step (or every ShardStep at close) must leave the
-error word clear.
+error word clear. The tests marked slow (the largest full-size cases, which
+the normal build runs) are left out of the child's run to bound its time;
+the Llama layer's and DSv3 block's full-size windows stay in.
 """
 import os
 import re
@@ -25,7 +27,7 @@ def test_suites_pass_under_the_bounds_checking_build():
     from fsdp_buffer_layout_gb300 import _build
     lib = _build.build(variant="bounds")
     env = dict(os.environ, VSF_LIBRARY=lib)
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-m", "gpu", "-x",
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-m", "gpu and not slow", "-x",
                         "-p", "no:cacheprovider"] + SUITES,
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=3000)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]

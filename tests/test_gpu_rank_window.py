@@ -56,8 +56,11 @@ def test_windows_cut_tile_and_row_tensors():
 
 @pytest.mark.parametrize("name,windows", [("dsv3_block", [(0, 7), (7, 128)]),
                                           ("llama_layer", [(0, 3), (3, 8)]),
-                                          ("moe_layer", [(0, 10), (10, 64)]),
-                                          ("llama_1p3b", [(0, 100), (100, 613), (613, 1024)])])
+                                          pytest.param("moe_layer", [(0, 10), (10, 64)],
+                                                       marks=pytest.mark.slow),
+                                          pytest.param("llama_1p3b",
+                                                       [(0, 100), (100, 613), (613, 1024)],
+                                                       marks=pytest.mark.slow)])
 def test_full_size_windows_equal_the_whole_plan(name, windows):
     """At full size the windows must give what the whole plan gives on the
     GPU (itself bit-exact against the oracle in the full-size parity tests),
