@@ -199,9 +199,11 @@ class ShardStep:
     def window_step(self, grads, params, step: int, all_reduce):
         """The step of a rank window (ranks=(r0, r1)) in one process of many:
         pack -> this window's fp64 sum of squares -> all_reduce (the sum over
-        every process's window: the path's one exchange) -> factor -> 8-bit
-        AdamW -> unpack. all_reduce(t) sums the one-element float64 tensor t
-        in place across the processes (see sum_all_reduce)."""
+        every process's window: the path's one exchange; "veScale-FSDP:
+        Flexible and High-Performance FSDP at Scale (MLSys 2026)" summary
+        page, 核心方法 > Distributed Buffer, fused group norm) -> factor ->
+        8-bit AdamW -> unpack. all_reduce(t) sums the one-element float64
+        tensor t in place across the processes (see sum_all_reduce)."""
         self.pack(grads)
         self.group_sumsq()
         total = self.sumsq[:1]
